@@ -1,0 +1,168 @@
+"""Seeded synthetic DiT-MLP workloads (numpy PCG64, BF16 round-to-nearest-even).
+
+The source pages measure Krea 3's MLP on real image edits (a 1 MP reference
+latent plus a 4 MP output latent) whose activations and weights are not
+available; these generators stand in for them with the shapes and value laws
+of the five workloads the library is measured on:
+
+=============  ======================================================================
+pr1            x[128][256] ~ N(0,1); W[512][256] ~ N(0,0.02); b[512] ~ N(0,0.01)
+dit_up         x[4096][3072] = z*c[k], z ~ N(0,1), c[k] ~ LogNormal(0,0.5) per channel;
+               W1[12288][3072] ~ N(0,0.02); b1[12288] ~ N(0,0.01)
+dit_down       z[16384][12288] ~ N(0,1) fp32 (the input is MXFP6 of GELU(z));
+               W2[3072][12288] ~ N(0,0.01); b2[3072] ~ N(0,0.01)
+full_mlp       x[20480][3072] ~ N(0,1); W1[12288][3072], W2[3072][12288] ~ N(0,0.02);
+               b1, b2 ~ N(0,0.01)
+outlier_mlp    x[20480][4096] ~ Student-t(3); 41 channels (1%, seeded permutation)
+               scaled x100; 1% of (row, 32-block) pairs set to +0 (Bernoulli 0.01);
+               W1[16384][4096], W2[4096][16384] ~ N(0,0.02); b1, b2 ~ N(0,0.01)
+=============  ======================================================================
+
+Every workload uses seed 0 by default. Each tensor draws from its own child of
+SeedSequence(seed), spawned in the fixed order x, W1, b1, W2, b2, channel
+scales, masks, so that shrinking one tensor never changes another. Values are
+drawn in fp32 and rounded to BF16 with round-to-nearest-even; BF16 tensors are
+returned as uint16 bit patterns.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "bf16_round",
+    "bf16_to_f32",
+    "workload",
+    "pr1",
+    "dit_up",
+    "dit_down",
+    "full_mlp",
+    "outlier_mlp",
+    "WORKLOADS",
+]
+
+_ORDER = ("x", "w1", "b1", "w2", "b2", "chan", "mask")
+
+
+def bf16_round(x) -> np.ndarray:
+    """fp32 -> BF16 bit patterns (uint16), round-to-nearest-even. Inputs are finite."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    bits = x.view(np.uint32).astype(np.uint64)
+    rounded = (bits + 0x7FFF + ((bits >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_to_f32(bits) -> np.ndarray:
+    """BF16 bit patterns -> fp32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _rngs(seed: int) -> dict:
+    children = np.random.SeedSequence(seed).spawn(len(_ORDER))
+    return {name: np.random.Generator(np.random.PCG64(c)) for name, c in zip(_ORDER, children)}
+
+
+def _normal_bf16(rng, shape, sigma: float) -> np.ndarray:
+    out = np.empty(shape, dtype=np.uint16)
+    rows = shape[0]
+    step = max(1, (1 << 22) // max(1, int(np.prod(shape[1:]))))
+    for lo in range(0, rows, step):
+        hi = min(rows, lo + step)
+        z = rng.standard_normal((hi - lo,) + tuple(shape[1:]), dtype=np.float32)
+        out[lo:hi] = bf16_round(z * np.float32(sigma))
+    return out
+
+
+def pr1(seed: int = 0, M: int = 128, K: int = 256, N: int = 512) -> dict:
+    """Single GEMM: activations x[M][K], weight w[N][K], bias b[N] (BF16 bits)."""
+    r = _rngs(seed)
+    return {
+        "x": _normal_bf16(r["x"], (M, K), 1.0),
+        "w": _normal_bf16(r["w1"], (N, K), 0.02),
+        "b": _normal_bf16(r["b1"], (N,), 0.01),
+    }
+
+
+def dit_up(seed: int = 0, M: int = 4096, d: int = 3072, ff: int = 12288) -> dict:
+    """Up-projection: x = z * c[channel] with log-normal channel scales."""
+    r = _rngs(seed)
+    chan = r["chan"].lognormal(0.0, 0.5, size=d).astype(np.float32)
+    x = np.empty((M, d), dtype=np.uint16)
+    step = max(1, (1 << 22) // d)
+    for lo in range(0, M, step):
+        hi = min(M, lo + step)
+        z = r["x"].standard_normal((hi - lo, d), dtype=np.float32)
+        x[lo:hi] = bf16_round(z * chan[None, :])
+    return {
+        "x": x,
+        "w": _normal_bf16(r["w1"], (ff, d), 0.02),
+        "b": _normal_bf16(r["b1"], (ff,), 0.01),
+        "chan": chan,
+    }
+
+
+def dit_down(seed: int = 0, M: int = 16384, ff: int = 12288, d: int = 3072) -> dict:
+    """Down-projection: z[M][ff] ~ N(0,1) fp32 (input is MXFP6 of GELU(z)), W2, b2."""
+    r = _rngs(seed)
+    z = np.empty((M, ff), dtype=np.float32)
+    step = max(1, (1 << 22) // ff)
+    for lo in range(0, M, step):
+        hi = min(M, lo + step)
+        z[lo:hi] = r["x"].standard_normal((hi - lo, ff), dtype=np.float32)
+    return {
+        "z": z,
+        "w": _normal_bf16(r["w2"], (d, ff), 0.01),
+        "b": _normal_bf16(r["b2"], (d,), 0.01),
+    }
+
+
+def full_mlp(seed: int = 0, M: int = 20480, d: int = 3072, ff: int = 12288) -> dict:
+    """Full DiT MLP block: x, W1, b1, W2, b2 (BF16 bits)."""
+    r = _rngs(seed)
+    return {
+        "x": _normal_bf16(r["x"], (M, d), 1.0),
+        "w1": _normal_bf16(r["w1"], (ff, d), 0.02),
+        "b1": _normal_bf16(r["b1"], (ff,), 0.01),
+        "w2": _normal_bf16(r["w2"], (d, ff), 0.02),
+        "b2": _normal_bf16(r["b2"], (d,), 0.01),
+    }
+
+
+def outlier_mlp(seed: int = 0, M: int = 20480, d: int = 4096, ff: int = 16384) -> dict:
+    """Outlier-heavy wide MLP: heavy-tailed activations, hot channels, zero blocks."""
+    r = _rngs(seed)
+    n_hot = int(round(0.01 * d))
+    hot = np.sort(r["chan"].permutation(d)[:n_hot])
+    gain = np.ones(d, dtype=np.float32)
+    gain[hot] = 100.0
+    x = np.empty((M, d), dtype=np.uint16)
+    step = max(1, (1 << 21) // d)
+    for lo in range(0, M, step):
+        hi = min(M, lo + step)
+        t = r["x"].standard_t(3.0, size=(hi - lo, d)).astype(np.float32)
+        t *= gain[None, :]
+        zero = r["mask"].random((hi - lo, d // 32)) < 0.01
+        t.reshape(hi - lo, d // 32, 32)[zero] = 0.0
+        x[lo:hi] = bf16_round(t)
+    return {
+        "x": x,
+        "w1": _normal_bf16(r["w1"], (ff, d), 0.02),
+        "b1": _normal_bf16(r["b1"], (ff,), 0.01),
+        "w2": _normal_bf16(r["w2"], (d, ff), 0.02),
+        "b2": _normal_bf16(r["b2"], (d,), 0.01),
+        "hot_channels": hot,
+    }
+
+
+WORKLOADS = {
+    "pr1": pr1,
+    "dit_up": dit_up,
+    "dit_down": dit_down,
+    "full_mlp": full_mlp,
+    "outlier_mlp": outlier_mlp,
+}
+
+
+def workload(name: str, **kw) -> dict:
+    """Generate a named workload (see the table in this module's docstring)."""
+    return WORKLOADS[name](**kw)
