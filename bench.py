@@ -1,0 +1,568 @@
+#!/usr/bin/env python3
+"""Throughput of the MXFP6 MLP hot path on GB300, one JSON line on stdout.
+
+Default workload (N=1): the full DiT MLP block, M=20480 tokens (16384 output +
+4096 reference), d=3072, ff=12288 -- one step is the whole hot path over one
+batch: K1 quantize x -> K3 up-projection + bias + GELU + MXFP6 requant -> K2
+down-projection + bias + BF16 store. The weights are quantized once, before
+timing (they are inference weights). `value` is MLP GEMM TFLOP/s over the whole
+step (2*M*d*ff*2 flops per step, quantizer time included).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Timing: CUDA events on the launching stream around exactly K steps, after W
+warm-up steps, with a synchronize (and, under torchrun, a barrier) on both sides;
+the maximum over ranks is reported. Between steps the inputs rotate over two
+independent copies (weights, activations, outputs: 2 x 556 MB > 129 MB L2), so no
+step reads operands another step left in L2. nvidia-smi clocks are sampled during
+the timed region.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MXFP6 MLP GEMM TFLOPS (% of GB300 FP6 peak); ms per DiT MLP; quantize GB/s"
+FP6_SPEC_PEAK_TFLOPS = 5000.0   # NVIDIA GB300 NVL72: 720 PF FP8/FP6 with sparsity / 72 GPUs / 2
+FP6_PER_BF16 = 2.0              # dense FP8/FP6 tensor rate = 2 x BF16 (4.5 vs 2.25 PF nominal)
+
+CONFIGS = {
+    "full_mlp": dict(kind="mlp", M=20480, d=3072, ff=12288,
+                     workload="full DiT MLP block (M=20480 tokens = 16384 output + 4096 reference, d=3072, ff=12288)"),
+    "outlier_mlp": dict(kind="mlp", M=20480, d=4096, ff=16384,
+                        workload="outlier-heavy wide MLP (M=20480, d=4096, ff=16384, Student-t(3), 1% hot channels x100, 1% zero blocks)"),
+    "dit_up": dict(kind="up", M=4096, d=3072, ff=12288,
+                   workload="DiT MLP up-projection (M=4096, K=3072, N=12288, bias+GELU+MXFP6 requant)"),
+    "dit_down": dict(kind="down", M=16384, d=3072, ff=12288,
+                     workload="DiT MLP down-projection (M=16384, K=12288, N=3072, bias+BF16 store)"),
+    "pr1": dict(kind="gemm", M=128, d=256, ff=512,
+                workload="single MXFP6 GEMM (M=128, K=256, N=512, bias+BF16)"),
+}
+
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the current kernels, keyed by (config, kernel); None where no
+# capture of the current kernel exists. Source summaries live in profiles/.
+NCU_TRAFFIC_BYTES: dict = {}
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sustained": p["bf16_tflops_sustained"],
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shard_rows(m_per_rank: int, world: int, rank: int) -> tuple[int, int]:
+    """Weak scaling: every rank owns its own batch of m_per_rank tokens (rows
+    [rank*m, (rank+1)*m) of the job's token set); the MLP is token-local, so no
+    rank needs another's rows and no collective sits on the data path."""
+    return rank * m_per_rank, (rank + 1) * m_per_rank
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        bus = _pci_bus_id(device_index)
+        if bus:
+            cmd += ["-i", bus]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def _pci_bus_id(device_index: int) -> str | None:
+    try:
+        import torch
+
+        p = torch.cuda.get_device_properties(device_index)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def _bf16_dev(bits, dev):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+class Workload:
+    """Device-resident inputs and outputs of one copy of the configuration."""
+
+    def __init__(self, mx, cfg: dict, seed: int, dev, m_rows: int):
+        import torch
+
+        self.cfg = cfg
+        kind = cfg["kind"]
+        M, d, ff = m_rows, cfg["d"], cfg["ff"]
+        self.M, self.d, self.ff = M, d, ff
+        if kind in ("mlp",):
+            gen = synth.outlier_mlp if cfg is CONFIGS["outlier_mlp"] else synth.full_mlp
+            w = gen(seed=seed, M=M, d=d, ff=ff)
+            self.x = _bf16_dev(w["x"], dev)
+            self.w1 = mx.mx_quantize(_bf16_dev(w["w1"], dev))
+            self.w2 = mx.mx_quantize(_bf16_dev(w["w2"], dev))
+            self.b1 = _bf16_dev(w["b1"], dev)
+            self.b2 = _bf16_dev(w["b2"], dev)
+            self.xq = mx.MxTensor(torch.empty((M, d * 3 // 4), dtype=torch.uint8, device=dev),
+                                  torch.empty(mx.mx_scales_bytes(M, d), dtype=torch.uint8, device=dev), M, d)
+            self.hq = mx.MxTensor(torch.empty((M, ff * 3 // 4), dtype=torch.uint8, device=dev),
+                                  torch.empty(mx.mx_scales_bytes(M, ff), dtype=torch.uint8, device=dev), M, ff)
+            self.y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+            self.host = w
+        elif kind in ("up", "gemm"):
+            w = synth.dit_up(seed=seed, M=M, d=d, ff=ff) if kind == "up" else synth.pr1(seed=seed, M=M, K=d, N=ff)
+            self.x = _bf16_dev(w["x"], dev)
+            self.w1 = mx.mx_quantize(_bf16_dev(w["w"], dev))
+            self.b1 = _bf16_dev(w["b"], dev)
+            self.xq = mx.MxTensor(torch.empty((M, d * 3 // 4), dtype=torch.uint8, device=dev),
+                                  torch.empty(mx.mx_scales_bytes(M, d), dtype=torch.uint8, device=dev), M, d)
+            if kind == "up":
+                self.hq = mx.MxTensor(torch.empty((M, ff * 3 // 4), dtype=torch.uint8, device=dev),
+                                      torch.empty(mx.mx_scales_bytes(M, ff), dtype=torch.uint8, device=dev), M, ff)
+            else:
+                self.y = torch.empty((M, ff), dtype=torch.bfloat16, device=dev)
+            self.host = w
+        elif kind == "down":
+            w = synth.dit_down(seed=seed, M=M, ff=ff, d=d)
+            z = torch.from_numpy(w["z"]).to(dev)
+            h = torch.nn.functional.gelu(z, approximate="tanh").to(torch.bfloat16)
+            del z
+            self.hq = mx.mx_quantize(h)
+            del h
+            self.w2 = mx.mx_quantize(_bf16_dev(w["w"], dev))
+            self.b2 = _bf16_dev(w["b"], dev)
+            self.y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+            self.host = {"w": w["w"], "b": w["b"]}
+        torch.cuda.synchronize()
+
+    def stages(self, mx):
+        """The step's launches as (name, callable) in stream order."""
+        kind = self.cfg["kind"]
+        out = []
+        if kind in ("mlp", "up", "gemm"):
+            out.append(("K1 quantize", lambda: mx.mx_quantize(self.x, out=self.xq)))
+        if kind in ("mlp", "up"):
+            out.append(("K3 up GEMM+GELU+requant",
+                        lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_GELU_MXFP6, out=self.hq)))
+        if kind == "gemm":
+            out.append(("K2 GEMM+bias+BF16", lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16,
+                                                                   out=self.y)))
+        if kind in ("mlp", "down"):
+            out.append(("K2 down GEMM+bias+BF16",
+                        lambda: mx.mx_gemm(self.hq, self.w2, self.b2, mx.MX_EPI_BIAS_BF16, out=self.y)))
+        return out
+
+
+def stage_work(cfg: dict, M: int) -> dict:
+    """Algorithmic flops / bytes per launch of each stage."""
+    d, ff = cfg["d"], cfg["ff"]
+    kind = cfg["kind"]
+    out = {}
+    if kind in ("mlp", "up", "gemm"):
+        out["K1 quantize"] = {"bytes": M * d * (2 + 0.75 + 1 / 32), "flops": 0.0}
+    if kind in ("mlp", "up"):
+        out["K3 up GEMM+GELU+requant"] = {"flops": 2.0 * M * d * ff,
+                                          "bytes": M * d * 0.78125 + ff * d * 0.78125 + M * ff * 0.78125}
+    if kind == "gemm":
+        out["K2 GEMM+bias+BF16"] = {"flops": 2.0 * M * d * ff, "bytes": (M + ff) * d * 0.78125 + M * ff * 2}
+    if kind in ("mlp", "down"):
+        out["K2 down GEMM+bias+BF16"] = {"flops": 2.0 * M * d * ff,
+                                         "bytes": M * ff * 0.78125 + d * ff * 0.78125 + M * d * 2}
+    return out
+
+
+def run_gpu(args) -> dict | None:
+    import torch
+
+    import microscaled_precision_gemm_gb300 as mx
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    mx.load()
+    cfg = CONFIGS[args.config]
+    M = cfg["M"]
+    lo, hi = shard_rows(M, world, rank)
+    # two independent copies; copy i uses seed (2*rank + i) so every rank's batch is its own
+    copies = [Workload(mx, cfg, seed=2 * rank + i, dev=dev, m_rows=hi - lo) for i in range(2)]
+    stream = torch.cuda.current_stream()
+    stage_names = [n for n, _ in copies[0].stages(mx)]
+    launches = [c.stages(mx) for c in copies]
+
+    for i in range(args.warmup):
+        for _, fn in launches[i % 2]:
+            fn()
+    torch.cuda.synchronize()
+    if mx.mx_device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side wait timeout during warm-up")
+
+    n_st = len(stage_names)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index or 0)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        e = ev[i]
+        e[0].record(stream)
+        for j, (_, fn) in enumerate(launches[i % 2]):
+            fn()
+            e[j + 1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(start.elapsed_time(stop), world)
+    per_stage = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
+                 for j in range(n_st)]
+    if mx.mx_device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side wait timeout in the timed region")
+
+    ms_step = total_ms / args.steps
+    work = stage_work(cfg, hi - lo)
+    step_flops = sum(w["flops"] for w in work.values()) * world
+    value = step_flops / (ms_step * 1e-3) / 1e12
+    peaks = load_peaks()
+    fp6_peak = FP6_PER_BF16 * peaks["bf16_sustained"]
+    stage_report = {}
+    for name, ms in zip(stage_names, per_stage):
+        w = work[name]
+        rep = {"ms": ms}
+        if w["flops"]:
+            rep["tflops"] = w["flops"] / (ms * 1e-3) / 1e12
+            rep["frac_fp6_peak_measured"] = rep["tflops"] / fp6_peak
+            rep["frac_fp6_peak_spec"] = rep["tflops"] / FP6_SPEC_PEAK_TFLOPS
+        rep["gbs"] = w["bytes"] / (ms * 1e-3) / 1e9
+        stage_report[name] = rep
+    # dominant kernel = largest share of the step
+    dom = max(stage_names, key=lambda n: stage_report[n]["ms"])
+    dw = work[dom]
+    if dw["flops"]:
+        roof = {"kernel": dom, "bound": "tensor", "achieved": stage_report[dom]["tflops"], "peak": fp6_peak,
+                "unit": "TFLOP/s", "frac": stage_report[dom]["tflops"] / fp6_peak,
+                "peak_basis": f"2 x {peaks['source']} sustained bf16 cuBLAS ({peaks['bf16_sustained']} TFLOP/s): "
+                              "dense FP6/FP8 rate = 2 x BF16 (of measured)",
+                "traffic": NCU_TRAFFIC_BYTES.get((args.config, dom))}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": stage_report[dom]["gbs"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": stage_report[dom]["gbs"] / peaks["hbm_gbs"],
+                "traffic": NCU_TRAFFIC_BYTES.get((args.config, dom))}
+
+    # end to end through the public API with host buffers (rank 0's view; all ranks run it)
+    e2e = run_e2e(mx, copies, cfg, args, world)
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp6_e2m3 (fp32 accumulate)",
+        "data": "synthetic (seeded numpy PCG64, BF16 RNE; random-init weights)",
+        "config": {"workload": cfg["workload"], "M_per_gpu": hi - lo, "d": cfg["d"], "ff": cfg["ff"],
+                   "l2": "inputs, weights and outputs rotate over 2 independent copies per step "
+                         "(working set per copy > L2); no L2 reuse between consecutive steps",
+                   "parallelism": f"token-sharded x{world}, weights replicated, no collective"},
+        "ms_per_mlp": ms_step if cfg["kind"] == "mlp" else None,
+        "stages": stage_report,
+        "roofline": roof,
+        "pct_fp6_peak_spec_5pf": value / FP6_SPEC_PEAK_TFLOPS,
+        "gpu_launches": args.steps * n_st,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if "K1 quantize" in stage_report:
+        line["quantize_gbs"] = stage_report["K1 quantize"]["gbs"]
+        line["quantize_frac_hbm"] = stage_report["K1 quantize"]["gbs"] / peaks["hbm_gbs"]
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_budget)
+    return line
+
+
+def run_e2e(mx, copies, cfg, args, world) -> dict:
+    """Same metric through mx_mlp (or the config's calls) with pinned host input
+    and output buffers; host->device and device->host copies inside the timed region."""
+    import torch
+
+    kind = cfg["kind"]
+    c = copies[0]
+    if kind == "mlp":
+        src, dst = c.x, c.y
+    elif kind == "down":
+        src, dst = c.hq.codes, c.y
+    elif kind == "up":
+        src, dst = c.x, c.hq.codes
+    else:
+        src, dst = c.x, c.y
+    h_in = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
+    h_in.copy_(src)
+    h_out = torch.empty(dst.shape, dtype=dst.dtype, pin_memory=True)
+    steps = max(1, min(args.steps, 50))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        src.copy_(h_in, non_blocking=True)
+        if kind == "mlp":
+            mx.mx_mlp(c.x, c.w1, c.b1, c.w2, c.b2, y=c.y)
+        else:
+            for _, fn in c.stages(mx):
+                fn()
+        h_out.copy_(dst, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world) / steps
+    flops = sum(w["flops"] for w in stage_work(cfg, c.M).values()) * world
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": int(src.numel() * src.element_size()),
+            "d2h_bytes_per_step": int(dst.numel() * dst.element_size())}
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleWorkload:
+    """The configuration's inputs with oracle-quantized weights (setup, untimed)."""
+
+    def __init__(self, cfg: dict, sample_rows: int):
+        import oracle as O
+
+        self.O = O
+        self.cfg = cfg
+        kind = cfg["kind"]
+        M = cfg["M"]
+        if kind == "mlp":
+            gen = synth.outlier_mlp if cfg is CONFIGS["outlier_mlp"] else synth.full_mlp
+            w = gen(M=M, d=cfg["d"], ff=cfg["ff"])
+            self.w1q, self.w1s = O.quantize_bf16(w["w1"])
+            self.w2q, self.w2s = O.quantize_bf16(w["w2"])
+        elif kind in ("up", "gemm"):
+            w = synth.dit_up(M=M) if kind == "up" else synth.pr1()
+            self.w1q, self.w1s = O.quantize_bf16(w["w"])
+        else:
+            w = synth.dit_down(M=min(M, sample_rows * 8))
+            self.w2q, self.w2s = O.quantize_bf16(w["w"])
+            w["x_f32"] = w.pop("z")
+        self.w = w
+
+    def step(self, rows: np.ndarray) -> float:
+        """One bounded sample of the hot path on `rows`; returns its algorithmic flops."""
+        O, w, kind = self.O, self.w, self.cfg["kind"]
+        d, ff = self.cfg["d"], self.cfg["ff"]
+        if kind == "mlp":
+            O.mlp(w["x"][rows], self.w1q, self.w1s, w["b1"], self.w2q, self.w2s, w["b2"])
+            return 4.0 * len(rows) * d * ff
+        if kind == "up":
+            xq, xs = O.quantize_bf16(w["x"][rows])
+            g = O.up_projection(xq, xs, self.w1q, self.w1s, w["b"])
+            O.quantize_f32(g.astype(np.float32))
+            return 2.0 * len(rows) * d * ff
+        if kind == "gemm":
+            xq, xs = O.quantize_bf16(w["x"][rows])
+            O.gemm(xq, xs, self.w1q, self.w1s, w["b"])
+            return 2.0 * len(rows) * d * ff
+        z = w["x_f32"][rows % w["x_f32"].shape[0]]
+        hq, hs = O.quantize_f32(O.gelu_tanh(z.astype(np.float64)).astype(np.float32))
+        O.down_projection(hq, hs, self.w2q, self.w2s, w["b"])
+        return 2.0 * len(rows) * d * ff
+
+
+def cpu_baseline(cfg: dict, budget_s: float) -> dict:
+    """The oracle, as it stands, on a bounded row sample of the same workload."""
+    ow = OracleWorkload(cfg, sample_rows=64)
+    rng = np.random.default_rng(0)
+    M = cfg["M"]
+    # calibrate on 8 rows, then size the sample to about budget_s of CPU work
+    t0 = time.perf_counter()
+    ow.step(rng.integers(0, M, 8))
+    per_row = (time.perf_counter() - t0) / 8
+    n = int(max(8, min(M, budget_s / max(per_row, 1e-6))))
+    rows = np.sort(rng.choice(M, size=n, replace=False))
+    t0 = time.perf_counter()
+    flops = ow.step(rows)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "seconds": dt, "sample": f"{n} of {M} token rows of the same workload (weights quantized by the "
+                                     f"oracle beforehand, untimed); fp64 numpy + brute-force E2M3 search"}
+
+
+def run_reference(args) -> dict | None:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    cfg = CONFIGS[args.config]
+    ow = OracleWorkload(cfg, sample_rows=64)
+    rng = np.random.default_rng(1)
+    M = cfg["M"]
+    t0 = time.perf_counter()
+    ow.step(rng.integers(0, M, 4))
+    per_row = (time.perf_counter() - t0) / 4
+    total_budget = args.cpu_budget * 4
+    rows_per_step = int(max(1, min(M, total_budget / max(per_row, 1e-6) / max(1, args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        ow.step(rng.integers(0, M, rows_per_step))
+    flops = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        flops += ow.step(rng.integers(0, M, rows_per_step))
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"{rows_per_step} random token rows of {M} per step (weights quantized by the oracle "
+              f"beforehand, untimed)")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded numpy PCG64, BF16 RNE; random-init weights)",
+        "config": {"workload": cfg["workload"], "M_per_gpu": M, "d": cfg["d"], "ff": cfg["ff"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="full_mlp", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU work for the baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line))
+    world, _, _ = dist_env()
+    if world > 1 and args.impl != "reference":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

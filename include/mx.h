@@ -1,0 +1,159 @@
+/*
+ * mx.h -- C ABI of the GB300 (sm_103a) MXFP6 MLP library.
+ *
+ * The operation is the MXFP6 hot path of a diffusion transformer's MLP, as the
+ * page "Optimizing Krea 3 on AMD Instinct MI355X" describes it:
+ *   - section "Quality set the precision limit": MXFP6 = 6-bit floating-point
+ *     elements with one shared scale per block;
+ *   - section "We built a faster MXFP6 kernel" (Figure 1): the MLP's GEMMs run
+ *     in MXFP6 with the 6-bit values packed in memory;
+ *   - section "Fusion cut intermediate memory traffic": the activations are
+ *     quantized once, and the down-projection reads the up-projection's MXFP6
+ *     output directly (no BF16 round trip, no separate requantization pass).
+ * The number format (which the pages leave open) is OCP MX v1.0's: E2M3
+ * elements, one E8M0 scale per 32 consecutive K-elements, shared exponent
+ * floor(log2(block amax)) - 2, round-to-nearest-even, saturation at +-7.5.
+ *
+ * Conventions for every entry point
+ *   - Every pointer except the ones marked "host" is a device pointer on the
+ *     current CUDA device; the caller allocates and owns every buffer. The
+ *     library allocates no device memory and keeps no per-call state.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream).
+ *   - Argument errors are detected on the host before anything is launched and
+ *     nothing is written. CUDA launch errors return MX_ERR_CUDA. Kernels never
+ *     trap: a device-side wait that runs out (2 s) sets a bit that
+ *     mx_device_error() reports, and the kernel returns.
+ *   - Only compute capability 10.3 (GB300) is supported; anything else returns
+ *     MX_ERR_UNSUPPORTED_DEVICE. There is no CPU fallback.
+ *
+ * Storage format (MXFP6 tensor of `rows` x K, K-major)
+ *   codes : rows * 3K/4 bytes, 32-byte aligned. Row r holds its K 6-bit codes
+ *           packed little-endian: code j at bits [6j, 6j+6) of the row's bits.
+ *           A code is E2M3: bit 5 sign, bits 4..3 exponent (bias 1), bits 2..0
+ *           mantissa.
+ *   scales: mx_scales_bytes(rows, K) bytes, 16-byte aligned, one E8M0 byte per
+ *           (row, 32-element K-block) in the tiled order of the tensor cores'
+ *           scale-factor copy: 512-byte atoms per (128-row group, 4 K-blocks),
+ *           atoms of a row group consecutive along K; inside an atom row
+ *           r = 32*r1 + r0 and K-block j are at byte 16*r0 + 4*r1 + j. Rows are
+ *           padded to a multiple of 128; padding scales are 0.
+ *           mx_scales_to_plain() converts to plain [rows][K/32] order.
+ */
+#ifndef MX_H_
+#define MX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MX_OK = 0,
+  MX_ERR_INVALID_ARG = 1,          /* null pointer, negative size, bad enum, ld_x < K   */
+  MX_ERR_UNSUPPORTED_SHAPE = 2,    /* K % 128 != 0 or K == 0; N % 256 != 0; too large   */
+  MX_ERR_MISALIGNED = 3,           /* codes not 32-byte aligned, others not 16-byte      */
+  MX_ERR_WORKSPACE_TOO_SMALL = 4,  /* mx_mlp workspace below mx_mlp_workspace_bytes()    */
+  MX_ERR_UNSUPPORTED_DEVICE = 5,   /* current device is not compute capability 10.3      */
+  MX_ERR_CUDA = 6                  /* a CUDA runtime/driver call or a launch failed       */
+} mx_status;
+
+typedef enum {
+  MX_EPI_BIAS_BF16 = 0,        /* out = bf16_rne(acc + bias): the down-projection (K2)      */
+  MX_EPI_BIAS_GELU_MXFP6 = 1   /* out = MXFP6(gelu_tanh(acc + bias)): the up-projection (K3) */
+} mx_epilogue;
+
+/* Bytes of the packed codes of a rows x K MXFP6 tensor: rows * 3K/4. */
+size_t mx_codes_bytes(int64_t rows, int64_t K);
+
+/* Bytes of the tiled scales of a rows x K MXFP6 tensor: ceil(rows/128)*128 * K/32. */
+size_t mx_scales_bytes(int64_t rows, int64_t K);
+
+/*
+ * mx_quantize -- K1: BF16 [rows][K] (row stride ld_x elements) -> MXFP6.
+ * Per 32-element block: amax; scale exponent s = floor(log2 amax) - 2 clamped to
+ * [-127, 127] (E8M0 code s + 127; an all-zero block gets code 0); each element
+ * is v * 2^-s rounded to the nearest E2M3 value, ties to the even code, magnitude
+ * saturated to 7.5, sign kept (so -0 -> 0x20). A block holding Inf/NaN gets scale
+ * 0xFF and zero codes. Used for activations (every MLP call) and once for weights.
+ *   x      : device, 16-byte aligned, rows x ld_x BF16 (only the first K of a row are read)
+ *   rows   : >= 0 (0 is a no-op)          K: multiple of 128, > 0
+ *   ld_x   : >= K, multiple of 8
+ *   codes  : device, mx_codes_bytes(rows, K) bytes, 32-byte aligned (written)
+ *   scales : device, mx_scales_bytes(rows, K) bytes, 16-byte aligned (written,
+ *            padding rows included)
+ */
+mx_status mx_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, void* codes, void* scales,
+                      cudaStream_t stream);
+
+/*
+ * mx_gemm -- K2/K3: C = A * B^T on MXFP6 operands, fp32 accumulation in tensor
+ * memory, then the fused epilogue `epi`:
+ *   MX_EPI_BIAS_BF16      : out = BF16 [M][N] row-major, bf16_rne(C + bias)
+ *   MX_EPI_BIAS_GELU_MXFP6: g = gelu_tanh(C + bias) in fp32, with
+ *                           gelu_tanh(v) = 0.5 v (1 + tanh(sqrt(2/pi)(v + 0.044715 v^3)));
+ *                           out = MXFP6 codes of g [M][N] (same rule as mx_quantize,
+ *                           blocks of 32 along N), out_scales = its tiled scales.
+ *   a_codes/a_scales : A, M x K MXFP6 (activations)
+ *   b_codes/b_scales : B, N x K MXFP6 (weights, nn.Linear layout)
+ *   bias             : device BF16 [N], 16-byte aligned, or NULL (no bias)
+ *   M >= 0 (any value; 0 is a no-op), N % 256 == 0, K % 128 == 0 and K > 0,
+ *   M, N, K < 2^31.
+ *   out              : BF16 [M][N] (16-byte aligned) or codes mx_codes_bytes(M, N)
+ *   out_scales       : MXFP6 epilogue only: mx_scales_bytes(M, N) bytes; else ignored
+ *   debug_prequant   : MXFP6 epilogue only, may be NULL: fp32 [M][N] receives g,
+ *                      the exact value the requantization rounded (test hook).
+ */
+mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
+                  const void* bias, int64_t M, int64_t N, int64_t K, mx_epilogue epi, void* out,
+                  void* out_scales, float* debug_prequant, cudaStream_t stream);
+
+/* Workspace bytes mx_mlp needs for M tokens: MXFP6 x (M x d) and MXFP6 h (M x ff). */
+size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff);
+
+/*
+ * mx_mlp -- the whole MXFP6 MLP block in three launches on `stream`:
+ *   K1 xq = MXFP6(x); K3 hq = MXFP6(gelu_tanh(xq W1^T + b1)); K2 y = bf16(hq W2^T + b2).
+ *   x        : BF16 [M][d] (16-byte aligned); y: BF16 [M][d] (written)
+ *   w1_*     : W1 as MXFP6, ff x d (quantized once with mx_quantize)
+ *   w2_*     : W2 as MXFP6, d x ff
+ *   b1, b2   : BF16 [ff], [d], or NULL
+ *   d % 256 == 0, ff % 256 == 0 (both are K of one GEMM and N of the other)
+ *   workspace: device, >= mx_mlp_workspace_bytes(M, d, ff) bytes, 256-byte aligned;
+ *              holds xq and hq; must not overlap any other argument.
+ */
+mx_status mx_mlp(const void* x, int64_t M, int64_t d, int64_t ff, const void* w1_codes, const void* w1_scales,
+                 const void* b1, const void* w2_codes, const void* w2_scales, const void* b2, void* y,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mx_status_string(mx_status status);
+
+/*
+ * mx_scales_to_plain -- host-side layout helper: tiled scales (host, as written
+ * by the kernels) -> plain row-major [rows][K/32] (host). K % 128 == 0.
+ */
+mx_status mx_scales_to_plain(const void* tiled_host, void* plain_host, int64_t rows, int64_t K);
+
+/* Inverse of mx_scales_to_plain (host). Padding rows of `tiled_host` are set to 0. */
+mx_status mx_scales_from_plain(const void* plain_host, void* tiled_host, int64_t rows, int64_t K);
+
+/*
+ * mx_device_error -- synchronizes the current device and reads the device-side
+ * error word of the library's kernels (0 = none; bit 0: a producer wait ran out,
+ * bit 1: an MMA wait, bit 2: an epilogue wait, bit 3: draining after an abort ran
+ * out). clear != 0 resets it. Returns MX_ERR_CUDA if the read itself fails.
+ */
+mx_status mx_device_error(unsigned* flags_host, int clear);
+
+/* Library ABI version (major * 100 + minor). */
+int mx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX_H_ */

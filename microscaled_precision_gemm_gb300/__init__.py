@@ -1,0 +1,265 @@
+"""Python binding of the GB300 MXFP6 MLP library (C ABI: include/mx.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. PyTorch supplies device memory and the current stream. The library is
+loaded from this package's ``_lib/libmxfp6.so`` (built by ``_build.build()``);
+if it is missing, every call raises -- there is no fallback.
+
+Entry points keep the C names:
+
+* ``mx_quantize(x)`` -- BF16 [rows][K] -> (codes uint8 [rows][3K/4], tiled scales uint8)
+* ``mx_gemm(a, b, bias, epilogue)`` -- block-scaled MXFP6 GEMM with a fused epilogue
+* ``mx_mlp(x, w1, b1, w2, b2)`` -- quantize -> up-proj + GELU + requant -> down-proj
+* ``mx_scales_to_plain`` / ``mx_scales_from_plain`` -- host-side scale layout helpers
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import _build
+
+__all__ = [
+    "MxError",
+    "MX_EPI_BIAS_BF16",
+    "MX_EPI_BIAS_GELU_MXFP6",
+    "MxTensor",
+    "load",
+    "library_path",
+    "mx_codes_bytes",
+    "mx_scales_bytes",
+    "mx_mlp_workspace_bytes",
+    "mx_quantize",
+    "mx_gemm",
+    "mx_mlp",
+    "mx_status_string",
+    "mx_scales_to_plain",
+    "mx_scales_from_plain",
+    "mx_device_error",
+    "mx_version",
+    "EXPORTED_SYMBOLS",
+]
+
+MX_EPI_BIAS_BF16 = 0
+MX_EPI_BIAS_GELU_MXFP6 = 1
+
+EXPORTED_SYMBOLS = (
+    "mx_codes_bytes",
+    "mx_scales_bytes",
+    "mx_quantize",
+    "mx_gemm",
+    "mx_mlp_workspace_bytes",
+    "mx_mlp",
+    "mx_status_string",
+    "mx_scales_to_plain",
+    "mx_scales_from_plain",
+    "mx_device_error",
+    "mx_version",
+)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MxError(RuntimeError):
+    """A library call returned a status other than MX_OK."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {mx_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load libmxfp6.so and declare its signatures. Raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build the MXFP6 CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()'); there is no CPU fallback")
+        lib = ctypes.CDLL(path)
+        vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+        sigs = {
+            "mx_codes_bytes": (sz, [i64, i64]),
+            "mx_scales_bytes": (sz, [i64, i64]),
+            "mx_quantize": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp]),
+            "mx_gemm": (ctypes.c_int, [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]),
+            "mx_mlp_workspace_bytes": (sz, [i64, i64, i64]),
+            "mx_mlp": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "mx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "mx_scales_to_plain": (ctypes.c_int, [vp, vp, i64, i64]),
+            "mx_scales_from_plain": (ctypes.c_int, [vp, vp, i64, i64]),
+            "mx_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]),
+            "mx_version": (ctypes.c_int, []),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise MxError(status, where)
+
+
+def mx_status_string(status: int) -> str:
+    return load().mx_status_string(int(status)).decode()
+
+
+def mx_version() -> int:
+    return load().mx_version()
+
+
+def mx_codes_bytes(rows: int, k: int) -> int:
+    return load().mx_codes_bytes(rows, k)
+
+
+def mx_scales_bytes(rows: int, k: int) -> int:
+    return load().mx_scales_bytes(rows, k)
+
+
+def mx_mlp_workspace_bytes(m: int, d: int, ff: int) -> int:
+    return load().mx_mlp_workspace_bytes(m, d, ff)
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+@dataclass
+class MxTensor:
+    """An MXFP6 matrix on the device: packed codes [rows][3K/4] and tiled scales."""
+
+    codes: "object"   # torch.uint8 [rows, 3K/4]
+    scales: "object"  # torch.uint8 [mx_scales_bytes(rows, K)]
+    rows: int
+    k: int
+
+
+def _empty_u8(n: int, device):
+    return _torch().empty(int(n), dtype=_torch().uint8, device=device)
+
+
+def mx_quantize(x, out: MxTensor | None = None, stream=None) -> MxTensor:
+    """K1: quantize a BF16 [rows][K] CUDA tensor (row stride may exceed K) to MXFP6."""
+    torch = _torch()
+    lib = load()
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("mx_quantize wants a CUDA bfloat16 [rows][K] tensor with unit column stride")
+    rows, k = x.shape
+    if out is None:
+        codes = _empty_u8(lib.mx_codes_bytes(rows, k), x.device).view(rows, -1) if rows else \
+            _empty_u8(0, x.device).view(0, k // 4 * 3)
+        out = MxTensor(codes, _empty_u8(lib.mx_scales_bytes(rows, k), x.device), rows, k)
+    st = lib.mx_quantize(_ptr(x), rows, k, x.stride(0), _ptr(out.codes), _ptr(out.scales), _stream_handle(stream))
+    _check(st, "mx_quantize")
+    return out
+
+
+def mx_gemm(a: MxTensor, b: MxTensor, bias=None, epilogue: int = MX_EPI_BIAS_BF16, out=None,
+            debug_prequant=None, stream=None):
+    """K2/K3: a [M][K] x b [N][K]^T on MXFP6 with the fused epilogue.
+
+    Returns a BF16 [M][N] tensor (MX_EPI_BIAS_BF16) or an MxTensor of [M][N]
+    (MX_EPI_BIAS_GELU_MXFP6). ``debug_prequant`` (fp32 [M][N]) receives the
+    GELU output the requantization rounds.
+    """
+    torch = _torch()
+    lib = load()
+    if a.k != b.k:
+        raise ValueError("inner dimensions differ")
+    m, n, k = a.rows, b.rows, a.k
+    dev = a.codes.device
+    if epilogue == MX_EPI_BIAS_BF16:
+        if out is None:
+            out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        out_ptr, out_sc = _ptr(out), None
+    else:
+        if out is None:
+            out = MxTensor(_empty_u8(lib.mx_codes_bytes(m, n), dev).view(m, -1) if m else
+                           _empty_u8(0, dev).view(0, n // 4 * 3),
+                           _empty_u8(lib.mx_scales_bytes(m, n), dev), m, n)
+        out_ptr, out_sc = _ptr(out.codes), _ptr(out.scales)
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != n):
+        raise ValueError("bias must be bfloat16 [N]")
+    st = lib.mx_gemm(_ptr(a.codes), _ptr(a.scales), _ptr(b.codes), _ptr(b.scales), _ptr(bias), m, n, k,
+                     int(epilogue), out_ptr, out_sc, _ptr(debug_prequant), _stream_handle(stream))
+    _check(st, "mx_gemm")
+    return out
+
+
+def mx_mlp(x, w1: MxTensor, b1, w2: MxTensor, b2, y=None, workspace=None, stream=None):
+    """K1 + K3 + K2: y = bf16(MXFP6(gelu(MXFP6(x) W1^T + b1)) W2^T + b2)."""
+    torch = _torch()
+    lib = load()
+    m, d = x.shape
+    ff = w1.rows
+    if w1.k != d or w2.rows != d or w2.k != ff:
+        raise ValueError("weight shapes do not match x")
+    if y is None:
+        y = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
+    need = lib.mx_mlp_workspace_bytes(m, d, ff)
+    if workspace is None:
+        workspace = _empty_u8(max(need, 256), x.device)
+    st = lib.mx_mlp(_ptr(x), m, d, ff, _ptr(w1.codes), _ptr(w1.scales), _ptr(b1), _ptr(w2.codes),
+                    _ptr(w2.scales), _ptr(b2), _ptr(y), _ptr(workspace), workspace.numel(),
+                    _stream_handle(stream))
+    _check(st, "mx_mlp")
+    return y
+
+
+def mx_scales_to_plain(tiled, rows: int, k: int) -> np.ndarray:
+    """Host: tiled scale bytes -> plain uint8 [rows][K/32]."""
+    lib = load()
+    t = np.ascontiguousarray(np.asarray(tiled, dtype=np.uint8).reshape(-1))
+    if t.size < lib.mx_scales_bytes(rows, k):
+        raise ValueError("tiled scale buffer too small")
+    out = np.empty((rows, k // 32), dtype=np.uint8)
+    _check(lib.mx_scales_to_plain(t.ctypes.data, out.ctypes.data, rows, k), "mx_scales_to_plain")
+    return out
+
+
+def mx_scales_from_plain(plain, rows: int, k: int) -> np.ndarray:
+    """Host: plain uint8 [rows][K/32] -> tiled scale bytes (padding rows zero)."""
+    lib = load()
+    p = np.ascontiguousarray(np.asarray(plain, dtype=np.uint8).reshape(rows, k // 32))
+    out = np.empty(lib.mx_scales_bytes(rows, k), dtype=np.uint8)
+    _check(lib.mx_scales_from_plain(p.ctypes.data, out.ctypes.data, rows, k), "mx_scales_from_plain")
+    return out
+
+
+def mx_device_error(clear: bool = True) -> int:
+    """Synchronize and read the kernels' device error word (0 = no wait ran out)."""
+    flags = ctypes.c_uint(0)
+    _check(load().mx_device_error(ctypes.byref(flags), int(clear)), "mx_device_error")
+    return flags.value

@@ -1,0 +1,237 @@
+// C ABI (include/mx.h): argument validation, device checks and the three-launch
+// MLP orchestration. Everything here is host code; the arithmetic lives in the
+// kernels (quantize.cu, gemm.cu).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "internal.h"
+#include "mx.h"
+#include "mx_layout.cuh"
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+constexpr int kMaxDevices = 64;
+
+std::atomic<int> g_device_ok[kMaxDevices];   // 0 unknown, 1 sm_103, -1 other
+std::atomic<int> g_device_sms[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Checks the current device once per device; fills the SM count.
+mx_status device_check(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MX_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MX_ERR_UNSUPPORTED_DEVICE;
+  int state = g_device_ok[dev].load(std::memory_order_relaxed);
+  if (state == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MX_ERR_CUDA;
+    state = (major == 10 && minor == 3) ? 1 : -1;
+    g_device_sms[dev].store(sms, std::memory_order_relaxed);
+    g_device_ok[dev].store(state, std::memory_order_relaxed);
+  }
+  if (state != 1) return MX_ERR_UNSUPPORTED_DEVICE;
+  *num_sms = g_device_sms[dev].load(std::memory_order_relaxed);
+  return MX_OK;
+}
+
+mx_status check_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, const void* codes,
+                         const void* scales) {
+  if (rows < 0 || K < 0 || ld_x < K) return MX_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || K > kMaxDim || rows > kMaxDim || ld_x > (int64_t{1} << 40))
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  if (ld_x % 8 != 0) return MX_ERR_MISALIGNED;
+  if (rows == 0) return MX_OK;
+  if (x == nullptr || codes == nullptr || scales == nullptr) return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 32) || !aligned(scales, 16)) return MX_ERR_MISALIGNED;
+  return MX_OK;
+}
+
+mx_status check_gemm(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
+                     const void* bias, int64_t M, int64_t N, int64_t K, int epi, const void* out,
+                     const void* out_scales, const float* dbg) {
+  if (epi != MX_EPI_BIAS_BF16 && epi != MX_EPI_BIAS_GELU_MXFP6) return MX_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return MX_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N % 256 != 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  if (((M + 127) / 128) * (N / 256) > kMaxDim) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0 || N == 0) return MX_OK;
+  if (a_codes == nullptr || a_scales == nullptr || b_codes == nullptr || b_scales == nullptr || out == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (epi == MX_EPI_BIAS_GELU_MXFP6 && out_scales == nullptr) return MX_ERR_INVALID_ARG;
+  if (!aligned(a_codes, 32) || !aligned(b_codes, 32) || !aligned(a_scales, 16) || !aligned(b_scales, 16))
+    return MX_ERR_MISALIGNED;
+  if (bias != nullptr && !aligned(bias, 16)) return MX_ERR_MISALIGNED;
+  if (epi == MX_EPI_BIAS_BF16 && !aligned(out, 16)) return MX_ERR_MISALIGNED;
+  if (epi == MX_EPI_BIAS_GELU_MXFP6 && (!aligned(out, 32) || !aligned(out_scales, 16)))
+    return MX_ERR_MISALIGNED;
+  if (epi == MX_EPI_BIAS_GELU_MXFP6 && dbg != nullptr && !aligned(dbg, 16)) return MX_ERR_MISALIGNED;
+  return MX_OK;
+}
+
+struct MlpLayout {
+  size_t xq, xs, hq, hs, total;
+};
+
+MlpLayout mlp_layout(int64_t M, int64_t d, int64_t ff) {
+  MlpLayout l;
+  l.xq = 0;
+  l.xs = align256(l.xq + static_cast<size_t>(mxk::codes_bytes(M, d)));
+  l.hq = align256(l.xs + static_cast<size_t>(mxk::scales_bytes(M, d)));
+  l.hs = align256(l.hq + static_cast<size_t>(mxk::codes_bytes(M, ff)));
+  l.total = align256(l.hs + static_cast<size_t>(mxk::scales_bytes(M, ff)));
+  return l;
+}
+
+mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
+                      const void* bias, int64_t M, int64_t N, int64_t K, int epi, void* out, void* out_scales,
+                      float* dbg, int num_sms, cudaStream_t stream) {
+  if (M == 0 || N == 0) return MX_OK;
+  mxk::GemmArgs a;
+  a.a_codes = a_codes;
+  a.a_scales = a_scales;
+  a.b_codes = b_codes;
+  a.b_scales = b_scales;
+  a.bias = bias;
+  a.out = out;
+  a.out_scales = out_scales;
+  a.debug_prequant = (epi == MX_EPI_BIAS_GELU_MXFP6) ? dbg : nullptr;
+  a.m = M;
+  a.n = N;
+  a.k = K;
+  a.epilogue = epi;
+  bool encode_failed = false;
+  cudaError_t e = mxk::launch_gemm(a, num_sms, stream, &encode_failed);
+  if (encode_failed) return MX_ERR_CUDA;
+  return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mx_codes_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return static_cast<size_t>(mxk::codes_bytes(rows, K));
+}
+
+size_t mx_scales_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return static_cast<size_t>(mxk::scales_bytes(rows, K));
+}
+
+mx_status mx_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, void* codes, void* scales,
+                      cudaStream_t stream) {
+  mx_status st = check_quantize(x, rows, K, ld_x, codes, scales);
+  if (st != MX_OK || rows == 0) return st;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  return mxk::launch_quantize_bf16(x, rows, K, ld_x, codes, scales, sms, stream) == cudaSuccess ? MX_OK
+                                                                                                : MX_ERR_CUDA;
+}
+
+mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
+                  const void* bias, int64_t M, int64_t N, int64_t K, mx_epilogue epi, void* out,
+                  void* out_scales, float* debug_prequant, cudaStream_t stream) {
+  mx_status st = check_gemm(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, static_cast<int>(epi), out,
+                            out_scales, debug_prequant);
+  if (st != MX_OK || M == 0 || N == 0) return st;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  return gemm_launch(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, static_cast<int>(epi), out, out_scales,
+                     debug_prequant, sms, stream);
+}
+
+size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff) {
+  if (M < 0 || d < 0 || ff < 0) return 0;
+  return mlp_layout(M, d, ff).total;
+}
+
+mx_status mx_mlp(const void* x, int64_t M, int64_t d, int64_t ff, const void* w1_codes, const void* w1_scales,
+                 const void* b1, const void* w2_codes, const void* w2_scales, const void* b2, void* y,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (M < 0 || d < 0 || ff < 0) return MX_ERR_INVALID_ARG;
+  if (d == 0 || ff == 0 || d % 256 != 0 || ff % 256 != 0 || M > kMaxDim || d > kMaxDim || ff > kMaxDim)
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MX_OK;
+  if (x == nullptr || w1_codes == nullptr || w1_scales == nullptr || w2_codes == nullptr ||
+      w2_scales == nullptr || y == nullptr || workspace == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
+  const MlpLayout l = mlp_layout(M, d, ff);
+  if (workspace_bytes < l.total) return MX_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* xq = ws + l.xq;
+  void* xs = ws + l.xs;
+  void* hq = ws + l.hq;
+  void* hs = ws + l.hs;
+  mx_status st = check_quantize(x, M, d, d, xq, xs);
+  if (st != MX_OK) return st;
+  st = check_gemm(xq, xs, w1_codes, w1_scales, b1, M, ff, d, MX_EPI_BIAS_GELU_MXFP6, hq, hs, nullptr);
+  if (st != MX_OK) return st;
+  st = check_gemm(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr);
+  if (st != MX_OK) return st;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  if (mxk::launch_quantize_bf16(x, M, d, d, xq, xs, sms, stream) != cudaSuccess) return MX_ERR_CUDA;
+  st = gemm_launch(xq, xs, w1_codes, w1_scales, b1, M, ff, d, MX_EPI_BIAS_GELU_MXFP6, hq, hs, nullptr, sms,
+                   stream);
+  if (st != MX_OK) return st;
+  return gemm_launch(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr, sms,
+                     stream);
+}
+
+const char* mx_status_string(mx_status status) {
+  switch (status) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG: null pointer, negative size or bad enum";
+    case MX_ERR_UNSUPPORTED_SHAPE: return "MX_ERR_UNSUPPORTED_SHAPE: need K % 128 == 0, N % 256 == 0, sizes < 2^31";
+    case MX_ERR_MISALIGNED: return "MX_ERR_MISALIGNED: codes need 32-byte, other buffers 16-byte alignment";
+    case MX_ERR_WORKSPACE_TOO_SMALL: return "MX_ERR_WORKSPACE_TOO_SMALL: see mx_mlp_workspace_bytes";
+    case MX_ERR_UNSUPPORTED_DEVICE: return "MX_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA: a CUDA call or kernel launch failed";
+  }
+  return "unknown mx_status";
+}
+
+mx_status mx_scales_to_plain(const void* tiled_host, void* plain_host, int64_t rows, int64_t K) {
+  if (tiled_host == nullptr || plain_host == nullptr || rows < 0 || K < 0) return MX_ERR_INVALID_ARG;
+  if (K % 128 != 0) return MX_ERR_UNSUPPORTED_SHAPE;
+  const uint8_t* t = static_cast<const uint8_t*>(tiled_host);
+  uint8_t* p = static_cast<uint8_t*>(plain_host);
+  const int64_t kb = K / 32;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < kb; ++b) p[r * kb + b] = t[mxk::scale_word_offset(r, b / 4, K) + (b % 4)];
+  return MX_OK;
+}
+
+mx_status mx_scales_from_plain(const void* plain_host, void* tiled_host, int64_t rows, int64_t K) {
+  if (tiled_host == nullptr || plain_host == nullptr || rows < 0 || K < 0) return MX_ERR_INVALID_ARG;
+  if (K % 128 != 0) return MX_ERR_UNSUPPORTED_SHAPE;
+  const uint8_t* p = static_cast<const uint8_t*>(plain_host);
+  uint8_t* t = static_cast<uint8_t*>(tiled_host);
+  const int64_t kb = K / 32;
+  const int64_t padded = mxk::pad_rows(rows);
+  for (int64_t r = 0; r < padded; ++r)
+    for (int64_t b = 0; b < kb; ++b)
+      t[mxk::scale_word_offset(r, b / 4, K) + (b % 4)] = r < rows ? p[r * kb + b] : 0;
+  return MX_OK;
+}
+
+mx_status mx_device_error(unsigned* flags_host, int clear) {
+  if (flags_host == nullptr) return MX_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MX_ERR_CUDA;
+  return mxk::read_device_error(flags_host, clear != 0) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+int mx_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,475 @@
+// K2 / K3: block-scaled MXFP6 x MXFP6 GEMM on the 5th-generation tensor cores.
+//
+//   C[m][n] = sum_k deq(A)[m][k] * deq(B)[n][k]        A: [M][K], B: [N][K], K-major
+//
+// "Optimizing Krea 3 on AMD Instinct MI355X", section "We built a faster MXFP6
+// kernel" (Figure 1): the MLP's GEMMs run in MXFP6, with 6-bit values packed in
+// memory (not one per byte) and no operand re-reads between neighbouring tiles.
+// Section "Fusion cut intermediate memory traffic": the up-projection's epilogue
+// writes the MXFP6 intermediate the down-projection reads directly.
+//
+// Design (sm_103a, one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: per 128-deep K step, one 16U6 tiled load for each
+//               operand (12 bytes per 16 codes in HBM, 16-byte slots in shared
+//               memory, 128-byte swizzle) and three 512-byte bulk copies of the
+//               tiled scale atoms, into a 4-stage mbarrier ring.
+//   warp 1      MMA issuer (one thread): copies the stage's scale atoms into tensor
+//               memory (tcgen05.cp) and issues four tcgen05.mma kind::mxf8f6f4
+//               block_scale (M=128, N=256, K=32, E2M3 x E2M3, E8M0 scales) into an
+//               fp32 accumulator of 256 tensor-memory columns.
+//   warps 2-9   epilogue: each warp drains 32 rows x 128 columns of the accumulator
+//               into registers, releases tensor memory to the next tile's MMAs at
+//               once, then applies bias + BF16 store (K2) or bias + tanh-GELU +
+//               MXFP6 requantization (K3), overlapping the next tile's mainloop.
+// Every wait is bounded (2 s on the global timer); on expiry the kernel records an
+// error bit, drains its in-flight copies and MMAs (again bounded), frees tensor
+// memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "mx_layout.cuh"
+#include "ptx.cuh"
+
+namespace mxk {
+
+__device__ unsigned int g_error_word;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint32_t kABytes = BM * BK;  // 16-byte shared slot per 16 codes -> 1 byte per element
+constexpr uint32_t kBBytes = BN * BK;
+constexpr uint32_t kSfaBytes = kAtomBytes;
+constexpr uint32_t kSfbBytes = 2 * kAtomBytes;
+// A 16U6 load writes the 12 data bytes of each 16-byte shared slot (the 4 padding
+// bytes are left untouched), so it completes 3/4 of the slot bytes on the mbarrier.
+constexpr uint32_t kStageTx = (kABytes + kBBytes) / 4 * 3 + kSfaBytes + kSfbBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = BN;  // scale slots after the accumulator: stage s at +16 s (A +0, B +8)
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+struct __align__(1024) SharedStorage {
+  uint8_t a[kStages][kABytes];
+  uint8_t b[kStages][kBBytes];
+  uint8_t sfa[kStages][kSfaBytes];
+  uint8_t sfb[kStages][kSfbBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tmem_full;
+  uint64_t tmem_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Descriptor of one 512-byte scale atom: 32 rows of 16 bytes, no swizzle,
+// 8-row core matrices 128 B apart.
+__device__ __forceinline__ uint64_t desc_scale_atom(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 32) |
+         (static_cast<uint64_t>(1) << 46);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: A, B = E2M3, K-major,
+// fp32 accumulate, E8M0 scales, M = 128, N = 256; j selects the scale byte
+// (K-block) inside each 32-bit tensor-memory scale column, for A and B alike.
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t j) {
+  return (j << 4) | (3u << 7) | (3u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(BM >> 4) << 24) | (j << 29);
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned err_bit) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(&g_error_word, err_bit);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      atomicOr(&g_error_word, kErrDrain);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap* ta, const CUtensorMap* tb,
+                                             const uint8_t* __restrict__ sfa_g, const uint8_t* __restrict__ sfb_g,
+                                             int num_n, int tiles, int kblocks, volatile int* abort_flag) {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t filled = 0, fill_parity = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    const int mb = tile / num_n;
+    const int nb = tile - mb * num_n;
+    const uint8_t* sfa_row = sfa_g + static_cast<int64_t>(mb) * kblocks * kAtomBytes;
+    const uint8_t* sfb_row0 = sfb_g + static_cast<int64_t>(2 * nb) * kblocks * kAtomBytes;
+    const uint8_t* sfb_row1 = sfb_row0 + static_cast<int64_t>(kblocks) * kAtomBytes;
+    for (int kb = 0; kb < kblocks; ++kb) {
+      if (!wait_bounded(&s.empty[stage], phase ^ 1u, abort_flag, kErrWaitProducer)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&s.full[stage], kStageTx);
+      tma_load_2d(s.a[stage], ta, &s.full[stage], kb * BK, mb * BM);
+      tma_load_2d(s.b[stage], tb, &s.full[stage], kb * BK, nb * BN);
+      bulk_load(s.sfa[stage], sfa_row + static_cast<int64_t>(kb) * kAtomBytes, kAtomBytes, &s.full[stage]);
+      bulk_load(s.sfb[stage], sfb_row0 + static_cast<int64_t>(kb) * kAtomBytes, kAtomBytes, &s.full[stage]);
+      bulk_load(s.sfb[stage] + kAtomBytes, sfb_row1 + static_cast<int64_t>(kb) * kAtomBytes, kAtomBytes,
+                &s.full[stage]);
+      filled |= 1u << stage;
+      fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (!ok) {
+    for (int st = 0; st < kStages; ++st)
+      if ((filled >> st) & 1u) wait_drain(&s.full[st], (fill_parity >> st) & 1u);
+  }
+}
+
+__device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, int tiles, int kblocks,
+                                        volatile int* abort_flag) {
+  int stage = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  bool ok = true, issued = false;
+  for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    if (!wait_bounded(&s.tmem_empty, acc_phase ^ 1u, abort_flag, kErrWaitMma)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    for (int kb = 0; kb < kblocks; ++kb) {
+      if (!wait_bounded(&s.full[stage], phase, abort_flag, kErrWaitMma)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sf_a = tmem + kSfCol0 + 16u * stage;
+      const uint32_t sf_b = sf_a + 8u;
+      tc_cp_32x128b_warpx4(sf_a, desc_scale_atom(smem_u32(s.sfa[stage])));
+      tc_cp_32x128b_warpx4(sf_b, desc_scale_atom(smem_u32(s.sfb[stage])));
+      tc_cp_32x128b_warpx4(sf_b + 4u, desc_scale_atom(smem_u32(s.sfb[stage] + kAtomBytes)));
+      const uint64_t ad = desc_sw128(smem_u32(s.a[stage]));
+      const uint64_t bd = desc_sw128(smem_u32(s.b[stage]));
+#pragma unroll
+      for (uint32_t j = 0; j < 4; ++j) {
+        // K step j: 32 elements = 32 bytes further along the swizzled 128-byte row
+        tc_mma_mx(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j), sf_a, sf_b, (kb | static_cast<int>(j)) != 0);
+      }
+      tc_commit(&s.empty[stage]);
+      issued = true;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    tc_commit(&s.tmem_full);
+    acc_phase ^= 1u;
+  }
+  if (!ok && issued) {
+    tc_commit(&s.drain);
+    wait_drain(&s.drain, 0);
+  }
+}
+
+__device__ __forceinline__ void load_bias32(const uint16_t* __restrict__ bias, int n, float (&b)[32]) {
+  if (bias == nullptr) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) b[i] = 0.0f;
+    return;
+  }
+  const uint4* p = reinterpret_cast<const uint4*>(bias + n);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 w = __ldg(p + v);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      b[8 * v + 2 * i] = __uint_as_float(ws[i] << 16);
+      b[8 * v + 2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+// tanh-GELU as v * sigmoid(2u) = v / (1 + exp(-2u)), u = sqrt(2/pi) (v + 0.044715 v^3):
+// the same function as 0.5 v (1 + tanh(u)) without its cancellation for v < 0.
+__device__ __forceinline__ float gelu_tanh(float v) {
+  const float u = 0.7978845608028654f * fmaf(0.044715f * v, v * v, v);
+  const float e = __expf(fminf(-2.0f * u, 80.0f));
+  return __fdividef(v, 1.0f + e);
+}
+
+template <int EPI, bool DBG>
+__device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, int num_n,
+                                             int tiles, int m_total, int n_total,
+                                             const uint16_t* __restrict__ bias, void* __restrict__ out,
+                                             uint8_t* __restrict__ out_scales, float* __restrict__ dbg,
+                                             volatile int* abort_flag) {
+  const int q = warp & 3;           // tensor-memory lane quadrant this warp may access
+  const int h = (warp - 2) >> 2;    // column half of the 256-wide tile
+  uint32_t acc_phase = 0;
+  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int mb = tile / num_n;
+    const int nb = tile - mb * num_n;
+    int ok = 0;
+    if (lane == 0) ok = wait_bounded(&s.tmem_full, acc_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t r[4][32];
+    const uint32_t t0 = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * 128);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(t0 + 32u * c, r[c]);
+    tc_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.tmem_empty);
+    acc_phase ^= 1u;
+
+    const int64_t row = static_cast<int64_t>(mb) * BM + 32 * q + lane;
+    const bool live = row < m_total;
+    const int col0 = nb * BN + h * 128;
+    if constexpr (EPI == 0) {
+      uint16_t* y = static_cast<uint16_t*>(out);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int n = col0 + 32 * c;
+        float b[32];
+        load_bias32(bias, n, b);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = cvt_bf16x2(__uint_as_float(r[c][2 * i + 1]) + b[2 * i + 1],
+                             __uint_as_float(r[c][2 * i]) + b[2 * i]);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(y + row * n_total + n);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+    } else {
+      uint8_t* codes = static_cast<uint8_t*>(out);
+      uint32_t scale_word = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int n = col0 + 32 * c;
+        float b[32];
+        load_bias32(bias, n, b);
+        float g[32];
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          g[i] = gelu_tanh(__uint_as_float(r[c][i]) + b[i]);
+          amax = max(amax, __float_as_uint(g[i]) & 0x7FFFFFFFu);
+        }
+        if constexpr (DBG) {
+          if (live) {
+            float4* d = reinterpret_cast<float4*>(dbg + row * n_total + n);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) d[v] = make_float4(g[4 * v], g[4 * v + 1], g[4 * v + 2], g[4 * v + 3]);
+          }
+        }
+        uint32_t sc;
+        uint64_t w[3] = {0, 0, 0};
+        if (amax >= 0x7F800000u) {  // Inf or NaN: E8M0 NaN, zero codes
+          sc = 0xFFu;
+        } else {
+          const int e = static_cast<int>(amax >> 23);
+          sc = static_cast<uint32_t>(e > 2 ? e - 2 : 0);
+          const float fac = __uint_as_float((254u - sc) << 23);  // 2^-s, exact
+#pragma unroll
+          for (int p = 0; p < 16; ++p) {
+            const uint32_t pr = cvt_e2m3x2(g[2 * p + 1] * fac, g[2 * p] * fac);
+            const uint64_t pair = (pr & 0x3Fu) | (((pr >> 8) & 0x3Fu) << 6);
+            const int bit = 12 * p;
+            w[bit / 64] |= pair << (bit % 64);
+            if (bit % 64 > 52) w[bit / 64 + 1] |= pair >> (64 - bit % 64);
+          }
+        }
+        if (live) {
+          uint64_t* dst = reinterpret_cast<uint64_t*>(codes + row * (n_total / 4 * 3) + n / 4 * 3);
+          dst[0] = w[0];
+          dst[1] = w[1];
+          dst[2] = w[2];
+        }
+        scale_word |= sc << (8 * c);
+      }
+      // padding rows of the last row tile get zero scales
+      if (!live) scale_word = 0;
+      *reinterpret_cast<uint32_t*>(out_scales + scale_word_offset(row, col0 / kAtomK, n_total)) = scale_word;
+    }
+  }
+}
+
+template <int EPI, bool DBG>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   const uint8_t* __restrict__ sfa_g, const uint8_t* __restrict__ sfb_g,
+                   const uint16_t* __restrict__ bias, void* __restrict__ out, uint8_t* __restrict__ out_scales,
+                   float* __restrict__ dbg, int m_total, int n_total, int k_total) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  SharedStorage& s =
+      *reinterpret_cast<SharedStorage*>(smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr));
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int num_n = n_total / BN;
+  const int tiles = ((m_total + BM - 1) / BM) * num_n;
+  const int kblocks = k_total / BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    mbar_init(&s.tmem_full, 1);
+    mbar_init(&s.tmem_empty, kEpiWarps);
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmap_a);
+    prefetch_tensormap(&tmap_b);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) run_producer(s, &tmap_a, &tmap_b, sfa_g, sfb_g, num_n, tiles, kblocks, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma(s, tmem, tiles, kblocks, abort_flag);
+  } else {
+    run_epilogue<EPI, DBG>(s, tmem, warp, lane, num_n, tiles, m_total, n_total, bias, out, out_scales, dbg,
+                           abort_flag);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Tensor map over packed 6-bit codes [rows][k]: 16U6 groups, box {128 codes, box_rows}.
+static bool make_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t k, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  std::memset(map, 0, sizeof(*map));
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 4 * 3)};
+  cuuint32_t box[2] = {BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B, 2, const_cast<void*>(codes), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int EPI, bool DBG>
+static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
+                                   cudaStream_t stream) {
+  auto kern = mx_gemm_kernel<EPI, DBG>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(
+      ta, tb, static_cast<const uint8_t*>(a.a_scales), static_cast<const uint8_t*>(a.b_scales),
+      static_cast<const uint16_t*>(a.bias), a.out, static_cast<uint8_t*>(a.out_scales), a.debug_prequant,
+      static_cast<int>(a.m), static_cast<int>(a.n), static_cast<int>(a.k));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, bool* encode_failed) {
+  *encode_failed = false;
+  CUtensorMap ta, tb;
+  if (!make_codes_map(&ta, a.a_codes, a.m, a.k, BM) || !make_codes_map(&tb, a.b_codes, a.n, a.k, BN)) {
+    *encode_failed = true;
+    return cudaSuccess;
+  }
+  const int64_t tiles = ((a.m + BM - 1) / BM) * (a.n / BN);
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  if (a.epilogue == 0) return launch_instance<0, false>(ta, tb, a, grid, stream);
+  if (a.debug_prequant != nullptr) return launch_instance<1, true>(ta, tb, a, grid, stream);
+  return launch_instance<1, false>(ta, tb, a, grid, stream);
+}
+
+cudaError_t read_device_error(unsigned* flags, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(flags, g_error_word, sizeof(unsigned));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned));
+}
+
+}  // namespace mxk

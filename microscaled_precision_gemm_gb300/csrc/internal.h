@@ -1,0 +1,41 @@
+// Internal launchers shared between the kernel translation units and the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace mxk {
+
+// Bits of the device-side error word (read by mx_device_error).
+enum : unsigned {
+  kErrWaitProducer = 1u << 0,   // TMA producer gave up waiting for a free stage
+  kErrWaitMma = 1u << 1,        // MMA issuer gave up waiting for operands / accumulator
+  kErrWaitEpilogue = 1u << 2,   // epilogue gave up waiting for the accumulator
+  kErrDrain = 1u << 3,          // copies or MMAs still in flight after an abort
+};
+
+cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t ld_x, void* codes, void* scales,
+                                 int num_sms, cudaStream_t stream);
+
+struct GemmArgs {
+  const void* a_codes;
+  const void* a_scales;
+  const void* b_codes;
+  const void* b_scales;
+  const void* bias;        // bf16 [N] or null
+  void* out;               // bf16 [M][N] or packed codes [M][3N/4]
+  void* out_scales;        // tiled scales of the MXFP6 output
+  float* debug_prequant;   // fp32 [M][N] or null (MXFP6 epilogue only)
+  int64_t m, n, k;
+  int epilogue;            // 0: bias + BF16, 1: bias + GELU + MXFP6
+};
+
+// Returns cudaSuccess or the first CUDA error; `encode_failed` is set when the
+// tensor-map encoder rejected the operands.
+cudaError_t launch_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream, bool* encode_failed);
+
+// Reads (and optionally clears) the device error word of the current device.
+cudaError_t read_device_error(unsigned* flags, bool clear);
+
+}  // namespace mxk

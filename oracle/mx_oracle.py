@@ -36,6 +36,9 @@ hand-derived fixtures under tests/golden/.
 
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 __all__ = [
@@ -138,6 +141,21 @@ def shared_exponent(amax) -> np.ndarray:
     return np.clip(s, -127, 127)
 
 
+def _nearest_chunk(f: np.ndarray) -> np.ndarray:
+    # Every |t| >= 8 has 7.5 as its nearest value, as 8 does; capping at 8
+    # keeps each distance below exact in fp64 (huge |t| would round them).
+    a = np.minimum(np.abs(f), 8.0)
+    best = np.abs(a - _MAGNITUDES[0])
+    code = np.zeros(a.shape, dtype=np.uint8)
+    for j in range(1, 32):
+        d = np.abs(a - _MAGNITUDES[j])
+        # strictly nearer wins; on an exact tie with code j - 1 the even one wins
+        take = (d < best) | ((d == best) & (j % 2 == 0))
+        best = np.where(take, d, best)
+        code = np.where(take, np.uint8(j), code)
+    return code | np.where(np.signbit(f), 0x20, 0).astype(np.uint8)
+
+
 def nearest_e2m3_code(t) -> np.ndarray:
     """Round each value to the nearest E2M3 code by brute-force search.
 
@@ -147,22 +165,17 @@ def nearest_e2m3_code(t) -> np.ndarray:
     even). Values beyond 7.5 are nearest to 7.5 (code 0x1F), which is the
     saturation the contract asks for. The sign bit copies the sign of t,
     negative zero included (so -0.01 gives 0x20, as IEEE rounding does).
+    Independent chunks of elements are searched on a thread pool.
     """
     t = np.asarray(t, dtype=np.float64)
     flat = t.reshape(-1)
-    out = np.empty(flat.shape, dtype=np.uint8)
-    even_bonus = np.where(np.arange(32) % 2 == 0, 2, 1)
-    chunk = 1 << 18
-    for lo in range(0, flat.size, chunk):
-        # Every |t| >= 8 has 7.5 as its nearest value, as 8 does; capping at 8
-        # keeps each distance below exact in fp64 (huge |t| would round them).
-        a = np.minimum(np.abs(flat[lo:lo + chunk]), 8.0)
-        dist = np.abs(a[:, None] - _MAGNITUDES[None, :])
-        best = dist.min(axis=1, keepdims=True)
-        candidates = dist == best
-        code = np.argmax(candidates * even_bonus[None, :], axis=1).astype(np.uint8)
-        code |= np.where(np.signbit(flat[lo:lo + chunk]), 0x20, 0).astype(np.uint8)
-        out[lo:lo + chunk] = code
+    chunk = 1 << 16
+    pieces = [flat[lo:lo + chunk] for lo in range(0, flat.size, chunk)]
+    if len(pieces) <= 1:
+        out = _nearest_chunk(flat)
+    else:
+        with ThreadPoolExecutor(max_workers=min(len(pieces), os.cpu_count() or 1)) as ex:
+            out = np.concatenate(list(ex.map(_nearest_chunk, pieces)))
     return out.reshape(t.shape)
 
 

@@ -1,0 +1,108 @@
+"""Shared helpers of the GPU parity tests: moving synthetic inputs to the device,
+reading MXFP6 results back into the oracle's plain layout, and the GEMM tolerance.
+
+The tolerance is the library's contract for every GEMM output:
+    |gpu - oracle| <= 2^-7 * |oracle| + 1e-3 * rms(oracle)
+where rms is taken over the compared elements.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+
+REL_TOL = 2.0 ** -7
+RMS_TOL = 1e-3
+
+
+def bf16_to_device(bits: np.ndarray):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16).cuda()
+
+
+def bf16_from_device(t) -> np.ndarray:
+    import torch
+
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f32_from_bf16_bits(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def mx_to_host(mxt, rows=None):
+    """MxTensor -> (codes uint8 [rows][K], plain scales uint8 [rows][K/32]) via the oracle's layout code."""
+    codes_packed = mxt.codes.cpu().numpy().reshape(mxt.rows, -1)
+    tiled = mxt.scales.cpu().numpy()
+    codes = O.unpack_codes(codes_packed, mxt.k)
+    plain = O.scales_tiled_to_plain(tiled, mxt.rows, mxt.k)
+    if rows is not None:
+        return codes[rows], plain[rows]
+    return codes, plain
+
+
+def mx_rows_to_host(mxt, rows):
+    """Only the listed rows (cheaper for big tensors)."""
+    import torch
+
+    idx = torch.as_tensor(np.asarray(rows), device=mxt.codes.device)
+    packed = mxt.codes.index_select(0, idx).cpu().numpy()
+    tiled = mxt.scales.cpu().numpy()
+    codes = O.unpack_codes(packed, mxt.k)
+    plain_all = O.scales_tiled_to_plain(tiled, mxt.rows, mxt.k)
+    return codes, plain_all[np.asarray(rows)]
+
+
+def mx_upload(codes: np.ndarray, plain_scales: np.ndarray):
+    """Oracle-made MXFP6 matrix (plain layout) -> device MxTensor in the library layout."""
+    import torch
+
+    import microscaled_precision_gemm_gb300 as mx
+
+    rows, k = codes.shape
+    packed = O.pack_codes(codes)
+    tiled = O.scales_plain_to_tiled(plain_scales, rows, k, pad_value=0)
+    return mx.MxTensor(torch.from_numpy(packed).cuda(), torch.from_numpy(tiled).cuda(), rows, k)
+
+
+def sample_rows(m: int, n_random: int = 192, seed: int = 0) -> np.ndarray:
+    """First and last row of every 128-row tile, plus seeded random rows."""
+    tiles = (m + 127) // 128
+    edge = np.concatenate([np.arange(tiles) * 128, np.minimum(np.arange(tiles) * 128 + 127, m - 1)])
+    rnd = np.random.default_rng(seed).integers(0, m, size=n_random)
+    return np.unique(np.concatenate([edge, rnd]))
+
+
+def gemm_tolerance_report(gpu: np.ndarray, ref: np.ndarray) -> dict:
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    bound = REL_TOL * np.abs(ref) + RMS_TOL * rms
+    err = np.abs(gpu - ref)
+    bad = err > bound
+    return {"rms": rms, "max_err": float(err.max()) if err.size else 0.0,
+            "n_bad": int(bad.sum()), "frac_ok": float(1 - bad.mean()) if err.size else 1.0,
+            "worst": float((err / np.maximum(bound, 1e-300)).max()) if err.size else 0.0}
+
+
+def assert_gemm_close(gpu, ref, what=""):
+    r = gemm_tolerance_report(gpu, ref)
+    assert r["n_bad"] == 0, f"{what}: {r}"
+    return r
+
+
+def assert_codes_equal(gpu_codes, ref_codes, gpu_scales, ref_scales, what=""):
+    gs, rs = np.asarray(gpu_scales), np.asarray(ref_scales)
+    if not np.array_equal(gs, rs):
+        idx = np.argwhere(gs != rs)[:8]
+        raise AssertionError(f"{what}: scales differ at {idx.tolist()}: gpu {gs[tuple(idx.T)].tolist()} "
+                             f"oracle {rs[tuple(idx.T)].tolist()}")
+    gc, rc = np.asarray(gpu_codes), np.asarray(ref_codes)
+    if not np.array_equal(gc, rc):
+        idx = np.argwhere(gc != rc)[:8]
+        raise AssertionError(f"{what}: {int((gc != rc).sum())} codes differ, first at {idx.tolist()}: "
+                             f"gpu {[hex(v) for v in gc[tuple(idx.T)].tolist()]} "
+                             f"oracle {[hex(v) for v in rc[tuple(idx.T)].tolist()]}")

@@ -1,0 +1,152 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+symbol, rejects bad arguments on the host before any launch, and its host-side
+scale-layout helpers agree with the oracle's independent layout code."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mx.h")
+
+OK, INVALID, SHAPE, MISALIGNED, WS_SMALL, DEVICE, CUDA = range(7)
+BF16, GELU = 0, 1
+A32 = 0x10000   # fake, 32-byte aligned device addresses: never dereferenced by validation
+A32b = 0x20000
+A32c = 0x30000
+A32d = 0x40000
+A32e = 0x50000
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import microscaled_precision_gemm_gb300 as pkg
+    from microscaled_precision_gemm_gb300 import _build
+
+    _build.build()
+    pkg.load()
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def lib(mx):
+    return mx.load()
+
+
+def test_exports_every_declared_symbol(lib, mx):
+    text = open(HEADER).read()
+    declared = set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(mx_\w+)\s*\(", text, flags=re.M))
+    assert declared == set(mx.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(mx):
+    assert mx.mx_version() == 100
+    for s in range(7):
+        assert mx.mx_status_string(s).startswith("MX_")
+    assert mx.mx_status_string(99) == "unknown mx_status"
+
+
+def test_size_queries(lib):
+    assert lib.mx_codes_bytes(128, 256) == 128 * 192
+    assert lib.mx_scales_bytes(128, 256) == 128 * 8
+    assert lib.mx_scales_bytes(300, 256) == 384 * 8       # rows padded to 128
+    assert lib.mx_scales_bytes(0, 256) == 0
+    assert lib.mx_codes_bytes(-1, 256) == 0
+    ws = lib.mx_mlp_workspace_bytes(20480, 3072, 12288)
+    need = 20480 * 3072 * 3 // 4 + 20480 * 96 + 20480 * 12288 * 3 // 4 + 20480 * 384
+    assert need <= ws <= need + 4 * 256
+
+
+def _q(lib, x=A32, rows=128, k=256, ld=256, codes=A32b, scales=A32c):
+    return lib.mx_quantize(x, rows, k, ld, codes, scales, None)
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    assert _q(lib, rows=-1) == INVALID
+    assert _q(lib, ld=128) == INVALID                  # ld_x < K
+    assert _q(lib, k=100, ld=100) == SHAPE             # K % 128
+    assert _q(lib, k=0, ld=0) == SHAPE
+    assert _q(lib, ld=260) == MISALIGNED               # ld_x % 8
+    assert _q(lib, x=None) == INVALID
+    assert _q(lib, codes=None) == INVALID
+    assert _q(lib, x=A32 + 8) == MISALIGNED
+    assert _q(lib, codes=A32b + 16) == MISALIGNED      # codes want 32 bytes
+    assert _q(lib, scales=A32c + 4) == MISALIGNED
+    assert _q(lib, rows=0, x=None, codes=None, scales=None) == OK   # empty input: no-op
+
+
+def _g(lib, a=A32, sa=A32b, b=A32c, sb=A32d, bias=None, M=128, N=512, K=256, epi=BF16, out=A32e,
+       out_sc=A32, dbg=None):
+    return lib.mx_gemm(a, sa, b, sb, bias, M, N, K, epi, out, out_sc, dbg, None)
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    assert _g(lib, epi=7) == INVALID
+    assert _g(lib, M=-1) == INVALID
+    assert _g(lib, N=384) == SHAPE                     # N % 256
+    assert _g(lib, K=96) == SHAPE                      # K % 128
+    assert _g(lib, K=0) == SHAPE
+    assert _g(lib, M=1 << 31) == SHAPE
+    assert _g(lib, a=None) == INVALID
+    assert _g(lib, out=None) == INVALID
+    assert _g(lib, epi=GELU, out_sc=None) == INVALID
+    assert _g(lib, a=A32 + 16) == MISALIGNED
+    assert _g(lib, sb=A32d + 8) == MISALIGNED
+    assert _g(lib, bias=A32 + 2) == MISALIGNED
+    assert _g(lib, epi=GELU, out=A32e + 16) == MISALIGNED
+    assert _g(lib, epi=GELU, dbg=A32 + 4) == MISALIGNED
+    assert _g(lib, M=0, a=None, sa=None, b=None, sb=None, out=None) == OK   # empty: no-op
+    assert _g(lib, N=0, a=None, sa=None, b=None, sb=None, out=None) == OK
+
+
+def test_mlp_rejects_bad_arguments(lib):
+    args = dict(x=A32, M=256, d=512, ff=1024, w1=A32b, w1s=A32c, b1=None, w2=A32d, w2s=A32e, b2=None,
+                y=A32, ws=0x100000, wsb=1 << 30)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.mx_mlp(a["x"], a["M"], a["d"], a["ff"], a["w1"], a["w1s"], a["b1"], a["w2"], a["w2s"],
+                          a["b2"], a["y"], a["ws"], a["wsb"], None)
+
+    assert call(M=-1) == INVALID
+    assert call(d=384) == SHAPE
+    assert call(ff=640) == SHAPE
+    assert call(x=None) == INVALID
+    assert call(ws=0x100000 + 128) == MISALIGNED
+    assert call(wsb=lib.mx_mlp_workspace_bytes(256, 512, 1024) - 1) == WS_SMALL
+    assert call(M=0, x=None, y=None, ws=None) == OK
+
+
+def test_valid_call_without_gpu_fails_loudly(lib):
+    """A well-formed call must reach the device check and fail there: no CPU fallback."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _q(lib) in (CUDA, DEVICE)
+    assert _g(lib) in (CUDA, DEVICE)
+
+
+def test_host_scale_layout_matches_oracle(mx):
+    rng = np.random.default_rng(11)
+    for rows, k in [(128, 256), (300, 384), (1, 128), (256, 1024)]:
+        plain = rng.integers(0, 256, size=(rows, k // 32)).astype(np.uint8)
+        tiled = mx.mx_scales_from_plain(plain, rows, k)
+        assert np.array_equal(tiled, O.scales_plain_to_tiled(plain, rows, k, pad_value=0))
+        assert np.array_equal(mx.mx_scales_to_plain(tiled, rows, k), plain)
+
+
+def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
+    import microscaled_precision_gemm_gb300 as pkg
+
+    monkeypatch.setattr(pkg, "_lib", None)
+    monkeypatch.setattr(pkg._build, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        pkg.load()

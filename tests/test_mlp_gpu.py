@@ -1,0 +1,84 @@
+"""MLP chain parity (K1 -> K3 -> K2 through mx_mlp).
+
+Stage-wise, each stage against the oracle given the previous stage's (already
+verified) GPU output: activations bit-exact; up-projection GELU values within
+the GEMM tolerance; requantized intermediate bit-exact given the kernel's fp32
+GELU values; down-projection within the tolerance given the GPU's intermediate.
+End to end, against a fully independent oracle run, requantization may flip a
+code where the GPU's fp32 value and the oracle's fp64 value sit on two sides of
+a rounding boundary, so that comparison asserts a 99.9% element pass rate.
+"""
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from mxutil import (assert_codes_equal, assert_gemm_close, bf16_from_device, bf16_to_device, f32_from_bf16_bits,
+                    gemm_tolerance_report, mx_rows_to_host, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lib, w, rows):
+    import torch
+
+    x = bf16_to_device(w["x"])
+    M, d = w["x"].shape
+    ff = w["w1"].shape[0]
+    w1q = lib.mx_quantize(bf16_to_device(w["w1"]))
+    w2q = lib.mx_quantize(bf16_to_device(w["w2"]))
+    b1 = bf16_to_device(w["b1"])
+    b2 = bf16_to_device(w["b2"])
+    y = lib.mx_mlp(x, w1q, b1, w2q, b2)
+
+    # the same kernels one by one, with the debug hook on the up-projection
+    xq = lib.mx_quantize(x)
+    dbg = torch.empty((M, ff), dtype=torch.float32, device="cuda")
+    hq = lib.mx_gemm(xq, w1q, b1, lib.MX_EPI_BIAS_GELU_MXFP6, debug_prequant=dbg)
+    y2 = lib.mx_gemm(hq, w2q, b2, lib.MX_EPI_BIAS_BF16)
+    assert torch.equal(y, y2), "mx_mlp differs from its three stages"
+
+    idx = torch.as_tensor(rows, device="cuda")
+    r_w1q, r_w1s = O.quantize_bf16(w["w1"])
+    r_w2q, r_w2s = O.quantize_bf16(w["w2"])
+    # stage 1: activations
+    rxq, rxs = O.quantize_bf16(w["x"][rows])
+    gxq, gxs = mx_rows_to_host(xq, rows)
+    assert_codes_equal(gxq, rxq, gxs, rxs, "xq")
+    # stage 2: up-projection + GELU (fp32 values before requantization)
+    g = dbg[idx].cpu().numpy()
+    assert_gemm_close(g, O.up_projection(rxq, rxs, r_w1q, r_w1s, w["b1"]), "gelu(x W1^T + b1)")
+    # stage 3: requantization, bit-exact given the kernel's fp32 values
+    ghq, ghs = mx_rows_to_host(hq, rows)
+    rhq, rhs = O.quantize_f32(g)
+    assert_codes_equal(ghq, rhq, ghs, rhs, "hq")
+    # stage 4: down-projection given the GPU's verified intermediate
+    got = f32_from_bf16_bits(bf16_from_device(y[idx])).astype(np.float64)
+    assert_gemm_close(got, O.down_projection(ghq, ghs, r_w2q, r_w2s, w["b2"]), "y")
+    # end to end against the independent oracle
+    y_ref, _ = O.mlp(w["x"][rows], r_w1q, r_w1s, w["b1"], r_w2q, r_w2s, w["b2"])
+    rep = gemm_tolerance_report(got, y_ref)
+    print(f"end-to-end vs independent oracle: {rep}")
+    assert rep["frac_ok"] >= 0.999, rep
+    assert lib.mx_device_error() == 0
+    return rep
+
+
+def test_small_mlp_all_rows(lib):
+    w = synth.full_mlp(M=300, d=256, ff=512)
+    _run(lib, w, np.arange(300))
+
+
+@pytest.mark.slow
+def test_full_dit_mlp_block(lib):
+    """M=20480 (16384 output + 4096 reference tokens), d=3072, ff=12288."""
+    w = synth.full_mlp()
+    _run(lib, w, sample_rows(20480, n_random=128))
+
+
+@pytest.mark.slow
+def test_outlier_heavy_wide_mlp(lib):
+    """M=20480, d=4096, ff=16384, Student-t activations, hot channels, zero blocks."""
+    w = synth.outlier_mlp()
+    _run(lib, w, sample_rows(20480, n_random=128))
