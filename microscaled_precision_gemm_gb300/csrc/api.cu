@@ -49,6 +49,7 @@ mx_status check_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, c
   if (K == 0 || K % 128 != 0 || K > kMaxDim || rows > kMaxDim || ld_x > (int64_t{1} << 40))
     return MX_ERR_UNSUPPORTED_SHAPE;
   if (ld_x % 8 != 0) return MX_ERR_MISALIGNED;
+  if (rows * (K / 32) > (int64_t{1} << 32) - (int64_t{1} << 28)) return MX_ERR_UNSUPPORTED_SHAPE;
   if (rows == 0) return MX_OK;
   if (x == nullptr || codes == nullptr || scales == nullptr) return MX_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(codes, 32) || !aligned(scales, 16)) return MX_ERR_MISALIGNED;

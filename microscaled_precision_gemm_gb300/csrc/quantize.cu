@@ -6,11 +6,9 @@
 // s = floor(log2 amax) - 2, clamped to [-127, 127]; each element rounds
 // v * 2^-s to the nearest E2M3 value, ties to even, saturating at +-7.5.
 //
-// HBM-bound: 2 bytes in, 0.75 + 1/32 bytes out per element. Each lane owns 8
-// consecutive elements (one 16-byte load, fully coalesced across the warp), four
-// lanes share a block and reduce its amax with two shuffles, lane pairs merge
-// their 6 code bytes into one 12-byte store, and 16 lanes merge four scale
-// bytes into one 32-bit store in the tiled scale layout.
+// HBM-bound: 2 bytes in, 0.75 + 1/32 bytes out per element. One lane owns one
+// 32-element block, so the amax is thread-local and the per-element work is the
+// scale multiply, the paired convert and 32-bit packing.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -22,101 +20,138 @@
 namespace mxk {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;   // 16-byte loads in flight per lane
+constexpr int kQuantUnroll = 2;   // blocks per lane per iteration (8 x 16-byte loads in flight)
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
+__device__ __forceinline__ uint4 ld_nc(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
 }
 
-// Quantize 8 BF16 values (one 16-byte chunk) whose block shares `fac` = 2^-s.
-// Returns the 8 codes packed into 48 bits (code i at bits 6i).
-__device__ __forceinline__ uint64_t encode8(const uint4 raw, float fac) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint64_t out = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(w[i] << 16) * fac;         // element 2i
-    const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * fac;  // element 2i+1
-    const uint32_t p = cvt_e2m3x2(hi, lo);
-    const uint64_t pair = (p & 0x3Fu) | (((p >> 8) & 0x3Fu) << 6);
-    out |= pair << (12 * i);
-  }
-  return out;
+// Four 6-bit codes held one per byte -> 24 bits, code i at bits 6i.
+__device__ __forceinline__ uint32_t pack4(uint32_t q) {
+  const uint32_t t = (q & 0x003F003Fu) | ((q >> 2) & 0x0FC00FC0u);  // c0 | c1<<6 | c2<<16 | c3<<22
+  return (t & 0xFFFu) | ((t >> 4) & 0xFFF000u);
 }
 
-__global__ void __launch_bounds__(kQuantThreads) quantize_bf16_kernel(
-    const uint16_t* __restrict__ x, int64_t rows, int64_t k, int64_t ld_x, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales) {
-  const int lane = threadIdx.x & 31;
-  const int64_t chunks_per_row = k / 8;
-  const int64_t total_chunks = rows * chunks_per_row;
-  const int64_t total_units = (total_chunks + 31) / 32;  // one unit = 32 chunks = 256 elements
-  const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * kQuantThreads + threadIdx.x) / 32;
-  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kQuantThreads / 32;
+// Quotient of n by an invariant divisor d with a precomputed magic number
+// (division by invariant integers using multiplication, round-up variant):
+// m = floor(2^32 (2^l - d) / d) + 1 with l = ceil(log2 d); q = (mulhi(n, m) + n) >> l.
+struct FastDiv {
+  uint32_t d, m, l;
+};
 
-  for (int64_t base = warp_global * kQuantUnroll; base < total_units; base += warps_total * kQuantUnroll) {
-    uint4 raw[kQuantUnroll];
-    int64_t chunk[kQuantUnroll];
+__host__ __device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+#ifdef __CUDA_ARCH__
+  return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(n, f.m)) + n) >> f.l);
+#else
+  return n / f.d;
+#endif
+}
+
+static FastDiv make_fast_div(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t{1} << l) < d) ++l;
+  const uint64_t m = ((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1;
+  return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+
+// One lane quantizes one 32-element block: 64 contiguous input bytes (four
+// 16-byte loads), a thread-local amax, sixteen paired E2M3 conversions, 24
+// packed code bytes. A warp owns 32 consecutive blocks of the flattened
+// [rows][K/32] block grid, so its 768 code bytes are contiguous in the packed
+// output; they are staged in shared memory and written as 16-byte stores. Four
+// consecutive lanes (4 K-blocks of one row) form one 32-bit tiled scale word.
+__global__ void __launch_bounds__(kQuantThreads) quantize_bf16_kernel(
+    const uint16_t* __restrict__ x, int rows, int k, int64_t ld_x, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, FastDiv blocks_per_row, uint32_t total_blocks) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t warp_global = (blockIdx.x * kQuantThreads + threadIdx.x) / 32;
+  const uint32_t warps_total = gridDim.x * kQuantThreads / 32;
+  __shared__ __align__(16) uint32_t stage[kQuantThreads / 32][kQuantUnroll][192];
+  uint32_t(*st)[192] = stage[threadIdx.x / 32];
+
+  for (uint32_t base = warp_global * 32 * kQuantUnroll; base < total_blocks;
+       base += warps_total * 32 * kQuantUnroll) {
+    uint4 raw[kQuantUnroll][4];
+    uint32_t row[kQuantUnroll], kb[kQuantUnroll];
+    bool valid[kQuantUnroll];
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      chunk[u] = (base + u) * 32 + lane;
-      raw[u] = make_uint4(0, 0, 0, 0);
-      if (chunk[u] < total_chunks) {
-        const int64_t r = chunk[u] / chunks_per_row;
-        const int64_t c = (chunk[u] - r * chunks_per_row) * 8;
-        raw[u] = ld_stream(x + r * ld_x + c);
-      }
+      const uint32_t b = base + 32 * u + lane;
+      valid[u] = b < total_blocks;
+      row[u] = fast_div(b, blocks_per_row);
+      kb[u] = b - row[u] * blocks_per_row.d;
+      const uint16_t* src = x + static_cast<int64_t>(row[u]) * ld_x + kb[u] * 32;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) raw[u][j] = valid[u] ? ld_nc(src + 8 * j) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
       // |v| ordering of BF16 equals unsigned ordering of (bits & 0x7FFF); NaN/Inf sort last.
-      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-      uint32_t amax = 0;
+      uint32_t m2 = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        amax = max(amax, w[i] & 0x7FFFu);
-        amax = max(amax, (w[i] >> 16) & 0x7FFFu);
+      for (int j = 0; j < 4; ++j) {
+        m2 = __vmaxu2(m2, raw[u][j].x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, raw[u][j].y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, raw[u][j].z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, raw[u][j].w & 0x7FFF7FFFu);
       }
-      amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      uint32_t scale;
-      uint64_t bits48;
+      const uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
+      uint32_t sc, w[6];
       if (amax >= 0x7F80u) {  // Inf or NaN in the block: E8M0 NaN, zero codes
-        scale = 0xFFu;
-        bits48 = 0;
+        sc = 0xFFu;
+#pragma unroll
+        for (int i = 0; i < 6; ++i) w[i] = 0;
       } else {
-        const int e = static_cast<int>(amax >> 7);         // biased exponent of amax (0 if subnormal)
-        const int sc = e > 2 ? e - 2 : 0;                   // E8M0 code = max(floor(log2 amax) - 2, -127) + 127
-        const float fac = __uint_as_float(static_cast<uint32_t>(254 - sc) << 23);  // 2^-s, exact
-        scale = static_cast<uint32_t>(sc);
-        bits48 = encode8(raw[u], fac);
-      }
-      // lane pairs: the even lane stores 16 codes = 12 bytes
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, bits48, 1);
-      // four blocks (16 lanes) -> one 32-bit scale word
-      const uint32_t s1 = __shfl_down_sync(0xffffffffu, scale, 4);
-      const uint32_t s2 = __shfl_down_sync(0xffffffffu, scale, 8);
-      const uint32_t s3 = __shfl_down_sync(0xffffffffu, scale, 12);
-      if (chunk[u] < total_chunks) {
-        if ((lane & 1) == 0) {
-          uint32_t* dst = reinterpret_cast<uint32_t*>(codes + chunk[u] * 6);
-          dst[0] = static_cast<uint32_t>(bits48);
-          dst[1] = static_cast<uint32_t>(bits48 >> 32) | static_cast<uint32_t>(other << 16);
-          dst[2] = static_cast<uint32_t>(other >> 16);
+        const uint32_t e = amax >> 7;              // biased exponent of amax (0 if subnormal)
+        sc = e > 2 ? e - 2 : 0;                    // E8M0 code = max(floor(log2 amax) - 2, -127) + 127
+        const float fac = __uint_as_float((254u - sc) << 23);  // 2^-s, exact
+        uint32_t g[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t v[4] = {raw[u][j].x, raw[u][j].y, raw[u][j].z, raw[u][j].w};
+          uint32_t p[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            p[i] = cvt_e2m3x2(__uint_as_float(v[i] & 0xFFFF0000u) * fac, __uint_as_float(v[i] << 16) * fac);
+          g[2 * j] = pack4(p[0] | (p[1] << 16));
+          g[2 * j + 1] = pack4(p[2] | (p[3] << 16));
         }
-        if ((lane & 15) == 0) {
-          const int64_t elem = chunk[u] * 8;
-          const int64_t r = elem / k;
-          const int64_t kc = (elem - r * k) / kAtomK;
-          const uint32_t word = scale | (s1 << 8) | (s2 << 16) | (s3 << 24);
-          *reinterpret_cast<uint32_t*>(scales + scale_word_offset(r, kc, k)) = word;
-        }
+        w[0] = g[0] | (g[1] << 24);
+        w[1] = (g[1] >> 8) | (g[2] << 16);
+        w[2] = (g[2] >> 16) | (g[3] << 8);
+        w[3] = g[4] | (g[5] << 24);
+        w[4] = (g[5] >> 8) | (g[6] << 16);
+        w[5] = (g[6] >> 16) | (g[7] << 8);
       }
+      uint2* s2 = reinterpret_cast<uint2*>(&st[u][6 * lane]);
+      s2[0] = make_uint2(w[0], w[1]);
+      s2[1] = make_uint2(w[2], w[3]);
+      s2[2] = make_uint2(w[4], w[5]);
+      // four consecutive blocks (K-blocks 4c..4c+3 of one row) -> one tiled scale word
+      const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
+      const uint32_t s2b = __shfl_down_sync(0xffffffffu, sc, 2);
+      const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
+      if (valid[u] && (lane & 3) == 0)
+        *reinterpret_cast<uint32_t*>(scales + scale_word_offset(row[u], kb[u] / 4, k)) =
+            sc | (s1 << 8) | (s2b << 16) | (s3 << 24);
     }
+    __syncwarp();
+    // the warp's blocks are consecutive: their codes are 24 * 32 contiguous bytes
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+      const uint32_t b0 = base + 32 * u;
+      if (b0 >= total_blocks) break;
+      const uint32_t nblk = min(32u, total_blocks - b0);  // a multiple of 4
+      const uint32_t chunks = nblk * 24 / 16;
+      uint8_t* dst = codes + static_cast<int64_t>(b0) * 24;
+      const uint4* src = reinterpret_cast<const uint4*>(st[u]);
+      for (uint32_t c = lane; c < chunks; c += 32) reinterpret_cast<uint4*>(dst)[c] = src[c];
+    }
+    __syncwarp();
   }
 
   // Zero the scale words of the padding rows (rows .. rows rounded up to 128).
@@ -132,8 +167,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_bf16_kernel(
 
 cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t ld_x, void* codes, void* scales,
                                  int num_sms, cudaStream_t stream) {
-  const int64_t units = (rows * (k / 8) + 31) / 32;
-  const int64_t warps_needed = (units + kQuantUnroll - 1) / kQuantUnroll;
+  const int64_t total_blocks = rows * (k / kBlock);
+  if (total_blocks > (int64_t{1} << 32) - (int64_t{1} << 28)) return cudaErrorInvalidValue;  // host checks first
+  const int64_t warps_needed = (total_blocks + 32 * kQuantUnroll - 1) / (32 * kQuantUnroll);
   int64_t blocks = (warps_needed * 32 + kQuantThreads - 1) / kQuantThreads;
   const int64_t pad_blocks = ((pad_rows(rows) - rows) * (k / kAtomK) + kQuantThreads - 1) / kQuantThreads;
   if (blocks < pad_blocks) blocks = pad_blocks;
@@ -141,8 +177,9 @@ cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   quantize_bf16_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(x), rows, k, ld_x, static_cast<uint8_t*>(codes),
-      static_cast<uint8_t*>(scales));
+      static_cast<const uint16_t*>(x), static_cast<int>(rows), static_cast<int>(k), ld_x,
+      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales),
+      make_fast_div(static_cast<uint32_t>(k / kBlock)), static_cast<uint32_t>(total_blocks));
   return cudaGetLastError();
 }
 
