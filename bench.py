@@ -56,7 +56,12 @@ CONFIGS = {
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the current kernels, keyed by (config, kernel); None where no
 # capture of the current kernel exists. Source summaries live in profiles/.
-NCU_TRAFFIC_BYTES: dict = {}
+# Written by hand from profiles/*_full_mlp.md (ncu on the full DiT MLP block).
+NCU_TRAFFIC_BYTES: dict = {
+    ("full_mlp", "K1 quantize"): 125870848 + 22252544,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 80438784 + 148792320,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 229895680 + 104813824,
+}
 
 
 def load_peaks() -> dict:
@@ -385,8 +390,11 @@ def run_gpu(args) -> dict | None:
 
 
 def run_e2e(mx, copies, cfg, args, world) -> dict:
-    """Same metric through mx_mlp (or the config's calls) with pinned host input
-    and output buffers; host->device and device->host copies inside the timed region."""
+    """Same metric through the public API (mx_mlp, or the configuration's calls)
+    with pinned host input and output buffers: every step copies its input
+    host->device and its result device->host inside the timed region. Steps are
+    pipelined on three streams (upload, compute, download) with two device
+    buffers, so step i+1's upload and step i-1's download overlap step i's compute."""
     import torch
 
     kind = cfg["kind"]
@@ -403,33 +411,69 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
     h_in.copy_(src)
     h_out = torch.empty(dst.shape, dtype=dst.dtype, pin_memory=True)
     steps = max(1, min(args.steps, 50))
-    stream = torch.cuda.current_stream()
+    dev = src.device
+    x_buf = [src, torch.empty_like(src)]
+    y_buf = [dst, torch.empty_like(dst)]
+    ws = None
+    if kind == "mlp":
+        ws = torch.empty(max(256, mx.mx_mlp_workspace_bytes(c.M, c.d, c.ff)), dtype=torch.uint8, device=dev)
+    s_up, s_comp, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+    up_done = [ev(), ev()]
+    comp_done = [ev(), ev()]
+    down_done = [ev(), ev()]
+    for e in comp_done + down_done:
+        e.record(torch.cuda.current_stream())
 
-    def step():
-        src.copy_(h_in, non_blocking=True)
+    def compute(slot):
         if kind == "mlp":
-            mx.mx_mlp(c.x, c.w1, c.b1, c.w2, c.b2, y=c.y)
+            mx.mx_mlp(x_buf[slot], c.w1, c.b1, c.w2, c.b2, y=y_buf[slot], workspace=ws, stream=s_comp)
+        elif kind == "down":
+            mx.mx_gemm(mx.MxTensor(x_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), c.w2, c.b2,
+                       mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp)
+        elif kind == "up":
+            mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
+            mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_GELU_MXFP6,
+                       out=mx.MxTensor(y_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), stream=s_comp)
         else:
-            for _, fn in c.stages(mx):
-                fn()
-        h_out.copy_(dst, non_blocking=True)
+            mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
+            mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp)
 
-    for _ in range(2):
-        step()
+    def step(i):
+        slot = i % 2
+        s_up.wait_event(comp_done[slot])            # x[slot] no longer read by step i-2
+        with torch.cuda.stream(s_up):
+            x_buf[slot].copy_(h_in, non_blocking=True)
+        up_done[slot].record(s_up)
+        s_comp.wait_event(up_done[slot])
+        s_comp.wait_event(down_done[slot])           # y[slot] already downloaded by step i-2
+        compute(slot)
+        comp_done[slot].record(s_comp)
+        s_down.wait_event(comp_done[slot])
+        with torch.cuda.stream(s_down):
+            h_out.copy_(y_buf[slot], non_blocking=True)
+        down_done[slot].record(s_down)
+
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize()
     barrier(world)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    a.record(s_up)
+    s_comp.wait_event(a)
+    s_down.wait_event(a)
+    for i in range(steps):
+        step(i)
+    s_down.wait_stream(s_comp)
+    b.record(s_down)
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), world) / steps
     flops = sum(w["flops"] for w in stage_work(cfg, c.M).values()) * world
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
             "h2d_bytes_per_step": int(src.numel() * src.element_size()),
-            "d2h_bytes_per_step": int(dst.numel() * dst.element_size())}
+            "d2h_bytes_per_step": int(dst.numel() * dst.element_size()),
+            "pipelining": "3 streams (upload / compute / download), 2 device buffers"}
 
 
 # ------------------------------------------------------------------ CPU oracle arm

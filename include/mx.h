@@ -145,9 +145,19 @@ mx_status mx_scales_from_plain(const void* plain_host, void* tiled_host, int64_t
  * mx_device_error -- synchronizes the current device and reads the device-side
  * error word of the library's kernels (0 = none; bit 0: a producer wait ran out,
  * bit 1: an MMA wait, bit 2: an epilogue wait, bit 3: draining after an abort ran
- * out). clear != 0 resets it. Returns MX_ERR_CUDA if the read itself fails.
+ * out, bit 4: mx_selftest_wait_timeout ran). clear != 0 resets it. Returns MX_ERR_CUDA if the read itself fails.
  */
 mx_status mx_device_error(unsigned* flags_host, int clear);
+
+/*
+ * mx_selftest_wait_timeout -- failure-detection self test. Launches a one-warp
+ * kernel whose single mbarrier wait can never complete (nothing arrives on it).
+ * The wait gives up after the kernels' bound (2 s), sets bit 4 of the device
+ * error word and returns; the CUDA context stays usable. No GPU fault, trap or
+ * hang is involved. Asynchronous on `stream`; read the result with
+ * mx_device_error().
+ */
+mx_status mx_selftest_wait_timeout(cudaStream_t stream);
 
 /* Library ABI version (major * 100 + minor). */
 int mx_version(void);

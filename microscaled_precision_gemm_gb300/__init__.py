@@ -41,6 +41,7 @@ __all__ = [
     "mx_scales_to_plain",
     "mx_scales_from_plain",
     "mx_device_error",
+    "mx_selftest_wait_timeout",
     "mx_version",
     "EXPORTED_SYMBOLS",
 ]
@@ -59,6 +60,7 @@ EXPORTED_SYMBOLS = (
     "mx_scales_to_plain",
     "mx_scales_from_plain",
     "mx_device_error",
+    "mx_selftest_wait_timeout",
     "mx_version",
 )
 
@@ -104,6 +106,7 @@ def load():
             "mx_scales_to_plain": (ctypes.c_int, [vp, vp, i64, i64]),
             "mx_scales_from_plain": (ctypes.c_int, [vp, vp, i64, i64]),
             "mx_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]),
+            "mx_selftest_wait_timeout": (ctypes.c_int, [vp]),
             "mx_version": (ctypes.c_int, []),
         }
         for name, (res, args) in sigs.items():
@@ -256,6 +259,11 @@ def mx_scales_from_plain(plain, rows: int, k: int) -> np.ndarray:
     out = np.empty(lib.mx_scales_bytes(rows, k), dtype=np.uint8)
     _check(lib.mx_scales_from_plain(p.ctypes.data, out.ctypes.data, rows, k), "mx_scales_from_plain")
     return out
+
+
+def mx_selftest_wait_timeout(stream=None) -> None:
+    """Launch the failure-detection self test (a bounded wait that must run out)."""
+    _check(load().mx_selftest_wait_timeout(_stream_handle(stream)), "mx_selftest_wait_timeout")
 
 
 def mx_device_error(clear: bool = True) -> int:

@@ -233,6 +233,13 @@ mx_status mx_device_error(unsigned* flags_host, int clear) {
   return mxk::read_device_error(flags_host, clear != 0) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+mx_status mx_selftest_wait_timeout(cudaStream_t stream) {
+  int sms = 0;
+  mx_status st = device_check(&sms);
+  if (st != MX_OK) return st;
+  return mxk::launch_wait_selftest(stream) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
 int mx_version(void) { return 100; }
 
 }  // extern "C"

@@ -465,6 +465,25 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, boo
   return launch_instance<1, false>(ta, tb, a, grid, stream);
 }
 
+// A wait that nothing will ever satisfy: it must give up after the bound, set
+// its error bit and let the kernel return with the context intact.
+__global__ void wait_selftest_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bounded(&bar, 0, &abort_flag, kErrSelfTest);
+}
+
+cudaError_t launch_wait_selftest(cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
+}
+
 cudaError_t read_device_error(unsigned* flags, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(flags, g_error_word, sizeof(unsigned));
   if (e != cudaSuccess || !clear) return e;

@@ -13,6 +13,7 @@ enum : unsigned {
   kErrWaitMma = 1u << 1,        // MMA issuer gave up waiting for operands / accumulator
   kErrWaitEpilogue = 1u << 2,   // epilogue gave up waiting for the accumulator
   kErrDrain = 1u << 3,          // copies or MMAs still in flight after an abort
+  kErrSelfTest = 1u << 4,       // the deliberate timeout of mx_selftest_wait_timeout
 };
 
 cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t ld_x, void* codes, void* scales,
@@ -34,6 +35,8 @@ struct GemmArgs {
 // Returns cudaSuccess or the first CUDA error; `encode_failed` is set when the
 // tensor-map encoder rejected the operands.
 cudaError_t launch_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream, bool* encode_failed);
+
+cudaError_t launch_wait_selftest(cudaStream_t stream);
 
 // Reads (and optionally clears) the device error word of the current device.
 cudaError_t read_device_error(unsigned* flags, bool clear);
