@@ -129,6 +129,34 @@ mx_status mx_mlp(const void* x, int64_t M, int64_t d, int64_t ff, const void* w1
                  const void* b1, const void* w2_codes, const void* w2_scales, const void* b2, void* y,
                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Capacity of the static scratch of mx_mlp_noalloc: 64 MiB per GPU. */
+#define MX_MLP_NOALLOC_WORKSPACE_BYTES ((size_t)64 << 20)
+
+/*
+ * mx_mlp_noalloc -- mx_mlp for callers that cannot allocate device memory.
+ * The paper has no counterpart for this entry point; it exists for callers such
+ * as code hosted in a runtime whose allocator owns all device memory, callers
+ * with a device-memory budget fixed at start-up, and paths that cannot afford
+ * cudaMalloc's implicit synchronization.
+ *   Same arguments and results as mx_mlp, without workspace/workspace_bytes: the
+ *   scratch (MXFP6 x and MXFP6 h) lives in a static device array of
+ *   MX_MLP_NOALLOC_WORKSPACE_BYTES inside the library, which every GPU that loads
+ *   the library holds until the process exits. The call allocates nothing.
+ *   Sizes whose mx_mlp_workspace_bytes(M, d, ff) exceeds that capacity return
+ *   MX_ERR_WORKSPACE_TOO_SMALL before anything is launched (for d = 3072,
+ *   ff = 12288 that is M > 5590 tokens).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call on a device shares the one array, and the kernels overwrite all of
+ *   it that they read, so nothing needs clearing between calls; but calls whose
+ *   executions overlap on the GPU (different streams, no ordering between them)
+ *   race on the array and must be serialized by the caller.
+ */
+mx_status mx_mlp_noalloc(const void* x, int64_t M, int64_t d, int64_t ff, const void* w1_codes,
+                         const void* w1_scales, const void* b1, const void* w2_codes, const void* w2_scales,
+                         const void* b2, void* y, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mx_status_string(mx_status status);
 

@@ -62,6 +62,7 @@ EXPORTED_SYMBOLS = (
     "mx_device_error",
     "mx_selftest_wait_timeout",
     "mx_version",
+    "mx_mlp_noalloc",
 )
 
 _lib = None

@@ -1,0 +1,58 @@
+// mx_mlp_noalloc: the MLP block for callers that cannot allocate device memory.
+//
+// mx_mlp needs scratch space for the MXFP6 activations and the MXFP6
+// intermediate. Some callers cannot provide it: code hosted inside a runtime
+// whose allocator owns all device memory (it must not call cudaMalloc behind the
+// runtime's back), callers with a fixed device-memory budget decided at start-up,
+// and paths that cannot afford cudaMalloc's implicit synchronization. For them
+// this file holds the scratch in a static device array, present on every GPU
+// that loads the library until the process exits, and runs the same three
+// kernels as mx_mlp through it. No device memory is allocated per call.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "mx.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = MX_MLP_NOALLOC_WORKSPACE_BYTES;
+constexpr int kMaxDevices = 64;
+
+// The scratch itself. Host code must not pass this name to a kernel: on the host
+// it is only a stand-in, so its device address is looked up once per device.
+static __device__ __align__(256) uint8_t g_mlp_scratch[kScratchBytes];
+
+std::mutex g_scratch_lock;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_mlp_scratch on the current device (looked up on first use).
+mx_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MX_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MX_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> guard(g_scratch_lock);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mlp_scratch) != cudaSuccess || p == nullptr) return MX_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MX_OK;
+}
+
+}  // namespace
+
+extern "C" mx_status mx_mlp_noalloc(const void* x, int64_t M, int64_t d, int64_t ff, const void* w1_codes,
+                                    const void* w1_scales, const void* b1, const void* w2_codes,
+                                    const void* w2_scales, const void* b2, void* y, cudaStream_t stream) {
+  if (M < 0 || d < 0 || ff < 0) return MX_ERR_INVALID_ARG;
+  if (M == 0) return MX_OK;
+  // sizes beyond the static scratch are refused before anything is launched
+  if (mx_mlp_workspace_bytes(M, d, ff) > kScratchBytes) return MX_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  const mx_status st = scratch_address(&scratch);
+  if (st != MX_OK) return st;
+  return mx_mlp(x, M, d, ff, w1_codes, w1_scales, b1, w2_codes, w2_scales, b2, y, scratch, kScratchBytes, stream);
+}
