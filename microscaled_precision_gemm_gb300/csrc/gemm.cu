@@ -8,19 +8,27 @@
 // Section "Fusion cut intermediate memory traffic": the up-projection's epilogue
 // writes the MXFP6 intermediate the down-projection reads directly.
 //
-// Design (sm_103a, one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: per 128-deep K step, one 16U6 tiled load for each
-//               operand (12 bytes per 16 codes in HBM, 16-byte slots in shared
-//               memory, 128-byte swizzle) and three 512-byte bulk copies of the
-//               tiled scale atoms, into a 4-stage mbarrier ring.
-//   warp 1      MMA issuer (one thread): copies the stage's scale atoms into tensor
-//               memory (tcgen05.cp) and issues four tcgen05.mma kind::mxf8f6f4
-//               block_scale (M=128, N=256, K=32, E2M3 x E2M3, E8M0 scales) into an
-//               fp32 accumulator of 256 tensor-memory columns.
-//   warps 2-9   epilogue: each warp drains 32 rows x 128 columns of the accumulator
-//               into registers, releases tensor memory to the next tile's MMAs at
-//               once, then applies bias + BF16 store (K2) or bias + tanh-GELU +
-//               MXFP6 requantization (K3), overlapping the next tile's mainloop.
+// Design (sm_103a): a CTA pair (cluster of 2) computes a 256 x 256 output tile
+// with the pair-wide MMA (tcgen05 cta_group::2). CTA r of the pair owns A rows
+// [128 r, 128 r + 128) of the tile and B rows (output columns) [128 r, 128 r + 128);
+// the tensor cores of both SMs read both halves of B, so each SM stages only half
+// of B: 33.5 KB of shared memory per 128-deep K step, which leaves room for a
+// 6-stage ring. Persistent: one pair per two SMs, walking tile pairs.
+//   warp 0      TMA producer (each CTA): one 16U6 tiled load for its A rows, one
+//               for its half of B (128-byte swizzle), and tiled loads of the scale
+//               atoms its SM's tensor memory needs (its own A rows, all 256 B rows).
+//               All four loads of both CTAs complete on the leader CTA's barrier,
+//               which expects both CTAs' bytes (cta_group::2 TMA completion).
+//   warp 1      leader CTA: issues four tcgen05.mma cta_group::2 kind::mxf8f6f4
+//               block_scale per stage (M=256, N=256, K=32, E2M3 x E2M3, E8M0) into
+//               each SM's fp32 accumulator (128 lanes x 256 columns).
+//   warp 10     leader CTA: copies each stage's scale atoms into both SMs' tensor
+//               memory (tcgen05.cp cta_group::2) in its own tcgen05 stream and
+//               signals the MMA warp, so no MMA queues behind a copy.
+//   warps 2-9   epilogue (each CTA): drain 32 rows x 128 columns of the local
+//               accumulator into registers, release tensor memory to the leader at
+//               once, then bias + BF16 store (K2) or bias + tanh-GELU + MXFP6
+//               requantization (K3).
 // Every wait is bounded (2 s on the global timer); on expiry the kernel records an
 // error bit, drains its in-flight copies and MMAs (again bounded), frees tensor
 // memory and returns.
@@ -42,11 +50,14 @@ __device__ unsigned int g_error_word;
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;
-constexpr int kStages = 4;
+constexpr int kStages = 6;
+constexpr int kPair = 2;              // CTAs per cluster (one MMA pair)
+constexpr uint16_t kPairMask = 0x3;
+constexpr int kBHalfRows = BN / kPair;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kThreads = (3 + kEpiWarps) * 32;  // + scale-copy warp
 constexpr uint32_t kABytes = BM * BK;  // 16-byte shared slot per 16 codes -> 1 byte per element
-constexpr uint32_t kBBytes = BN * BK;
+constexpr uint32_t kBBytes = kBHalfRows * BK;   // this CTA's half of the B tile
 constexpr uint32_t kSfaBytes = kAtomBytes;
 constexpr uint32_t kSfbBytes = 2 * kAtomBytes;
 // A 16U6 load writes the 12 data bytes of each 16-byte shared slot (the 4 padding
@@ -63,6 +74,7 @@ struct __align__(1024) SharedStorage {
   uint8_t sfb[kStages][kSfbBytes];
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t sfready[kStages];   // leader: the stage's scales are in both SMs' tensor memory
   uint64_t tmem_full;
   uint64_t tmem_empty;
   uint64_t drain;
@@ -87,11 +99,11 @@ __device__ __forceinline__ uint64_t desc_scale_atom(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: A, B = E2M3, K-major,
-// fp32 accumulate, E8M0 scales, M = 128, N = 256; j selects the scale byte
+// fp32 accumulate, E8M0 scales, M = 256 (the pair), N = 256; j selects the scale byte
 // (K-block) inside each 32-bit tensor-memory scale column, for A and B alike.
 __host__ __device__ constexpr uint32_t idesc_mx(uint32_t j) {
   return (j << 4) | (3u << 7) | (3u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-         (static_cast<uint32_t>(BM >> 4) << 24) | (j << 29);
+         (static_cast<uint32_t>((kPair * BM) >> 4) << 24) | (j << 29);
 }
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -101,6 +113,25 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(&g_error_word, err_bit);
+        return false;
+      }
+    }
+  }
+}
+
+// As wait_bounded, for barriers the peer CTA arrives on (acquire at cluster scope).
+__device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                     unsigned err_bit) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
     if ((i & 63) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kTimeoutNs) {
@@ -124,31 +155,41 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Tile walk shared by every role: cluster c takes tile pairs c, c + #clusters, ...
+// A pair tile is 256 rows (CTA r: row tile 2 p_m + r) x 256 columns.
+struct TileWalk {
+  int pairs, num_n, first, step, rank;
+};
+
+__device__ __forceinline__ void pair_tile(const TileWalk& w, int p, int* mb, int* nb) {
+  const int pm = p / w.num_n;
+  *nb = p - pm * w.num_n;
+  *mb = pm * kPair + w.rank;
+}
+
 __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap* ta, const CUtensorMap* tb,
-                                             const uint8_t* __restrict__ sfa_g, const uint8_t* __restrict__ sfb_g,
-                                             int num_n, int tiles, int kblocks, volatile int* abort_flag) {
+                                             const CUtensorMap* tsa, const CUtensorMap* tsb, const TileWalk& w,
+                                             int num_m, int kblocks, volatile int* abort_flag) {
   int stage = 0;
   uint32_t phase = 0;
   uint32_t filled = 0, fill_parity = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-    const int mb = tile / num_n;
-    const int nb = tile - mb * num_n;
-    const uint8_t* sfa_row = sfa_g + static_cast<int64_t>(mb) * kblocks * kAtomBytes;
-    const uint8_t* sfb_row0 = sfb_g + static_cast<int64_t>(2 * nb) * kblocks * kAtomBytes;
-    const uint8_t* sfb_row1 = sfb_row0 + static_cast<int64_t>(kblocks) * kAtomBytes;
+  for (int p = w.first; p < w.pairs && ok; p += w.step) {
+    int mb, nb;
+    pair_tile(w, p, &mb, &nb);
     for (int kb = 0; kb < kblocks; ++kb) {
       if (!wait_bounded(&s.empty[stage], phase ^ 1u, abort_flag, kErrWaitProducer)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&s.full[stage], kStageTx);
-      tma_load_2d(s.a[stage], ta, &s.full[stage], kb * BK, mb * BM);
-      tma_load_2d(s.b[stage], tb, &s.full[stage], kb * BK, nb * BN);
-      bulk_load(s.sfa[stage], sfa_row + static_cast<int64_t>(kb) * kAtomBytes, kAtomBytes, &s.full[stage]);
-      bulk_load(s.sfb[stage], sfb_row0 + static_cast<int64_t>(kb) * kAtomBytes, kAtomBytes, &s.full[stage]);
-      bulk_load(s.sfb[stage] + kAtomBytes, sfb_row1 + static_cast<int64_t>(kb) * kAtomBytes, kAtomBytes,
-                &s.full[stage]);
+      // both CTAs' stage bytes complete on the leader's full barrier, which
+      // expects them all; a row tile past M reads zeros (A and its scales)
+      const uint32_t full_leader = mapa_shared(smem_u32(&s.full[stage]), 0);
+      if (w.rank == 0) mbar_arrive_expect_tx(&s.full[stage], kPair * kStageTx);
+      tma_load_2d_pair(s.a[stage], ta, full_leader, kb * BK, mb * BM);
+      tma_load_2d_pair(s.b[stage], tb, full_leader, kb * BK, nb * BN + w.rank * kBHalfRows);
+      tma_load_2d_pair(s.sfa[stage], tsa, full_leader, 0, mb * kblocks + kb);
+      tma_load_3d_pair(s.sfb[stage], tsb, full_leader, 0, kb, 2 * nb);
       filled |= 1u << stage;
       fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == kStages) {
@@ -157,19 +198,25 @@ __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap
       }
     }
   }
-  if (!ok) {
+  if (ok) {
+    // every stage this CTA filled has been consumed by the pair's MMAs, so no
+    // completion arrival from the leader is still heading here
+    for (int st = 0; st < kStages; ++st)
+      if ((filled >> st) & 1u) wait_drain(&s.empty[st], (fill_parity >> st) & 1u);
+  } else if (w.rank == 0) {
     for (int st = 0; st < kStages; ++st)
       if ((filled >> st) & 1u) wait_drain(&s.full[st], (fill_parity >> st) & 1u);
   }
 }
 
-__device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, int tiles, int kblocks,
+__device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const TileWalk& w, int kblocks,
                                         volatile int* abort_flag) {
   int stage = 0;
   uint32_t phase = 0, acc_phase = 0;
   bool ok = true, issued = false;
-  for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-    if (!wait_bounded(&s.tmem_empty, acc_phase ^ 1u, abort_flag, kErrWaitMma)) {
+  for (int p = w.first; p < w.pairs && ok; p += w.step) {
+    // both CTAs' epilogues have drained the previous tile's accumulators
+    if (!wait_bounded_cluster(&s.tmem_empty, acc_phase ^ 1u, abort_flag, kErrWaitMma)) {
       ok = false;
       break;
     }
@@ -179,20 +226,21 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, int til
         ok = false;
         break;
       }
+      if (!wait_bounded(&s.sfready[stage], phase, abort_flag, kErrWaitMma)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const uint32_t sf_a = tmem + kSfCol0 + 16u * stage;
       const uint32_t sf_b = sf_a + 8u;
-      tc_cp_32x128b_warpx4(sf_a, desc_scale_atom(smem_u32(s.sfa[stage])));
-      tc_cp_32x128b_warpx4(sf_b, desc_scale_atom(smem_u32(s.sfb[stage])));
-      tc_cp_32x128b_warpx4(sf_b + 4u, desc_scale_atom(smem_u32(s.sfb[stage] + kAtomBytes)));
       const uint64_t ad = desc_sw128(smem_u32(s.a[stage]));
       const uint64_t bd = desc_sw128(smem_u32(s.b[stage]));
 #pragma unroll
       for (uint32_t j = 0; j < 4; ++j) {
         // K step j: 32 elements = 32 bytes further along the swizzled 128-byte row
-        tc_mma_mx(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j), sf_a, sf_b, (kb | static_cast<int>(j)) != 0);
+        tc_mma_mx_pair(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j), sf_a, sf_b, (kb | static_cast<int>(j)) != 0);
       }
-      tc_commit(&s.empty[stage]);
+      tc_commit_pair(&s.empty[stage], kPairMask);  // frees the stage in both CTAs
       issued = true;
       if (++stage == kStages) {
         stage = 0;
@@ -200,12 +248,36 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, int til
       }
     }
     if (!ok) break;
-    tc_commit(&s.tmem_full);
+    tc_commit_pair(&s.tmem_full, kPairMask);
     acc_phase ^= 1u;
   }
   if (!ok && issued) {
-    tc_commit(&s.drain);
+    tc_commit_pair(&s.drain, 0x1);
     wait_drain(&s.drain, 0);
+  }
+}
+
+// Leader CTA, scale warp: copies each stage's scale atoms into both SMs' tensor
+// memory in its own tcgen05 stream and signals sfready[stage] when they landed.
+__device__ __forceinline__ void run_scales(SharedStorage& s, uint32_t tmem, const TileWalk& w, int kblocks,
+                                           volatile int* abort_flag) {
+  const int my_pairs = w.pairs > w.first ? (w.pairs - w.first + w.step - 1) / w.step : 0;
+  const int64_t steps = static_cast<int64_t>(my_pairs) * kblocks;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int64_t g = 0; g < steps; ++g) {
+    if (!wait_bounded(&s.full[stage], phase, abort_flag, kErrWaitMma)) return;
+    tc_fence_after();
+    const uint32_t sf_a = tmem + kSfCol0 + 16u * stage;
+    const uint32_t sf_b = sf_a + 8u;
+    tc_cp_pair_32x128b_warpx4(sf_a, desc_scale_atom(smem_u32(s.sfa[stage])));
+    tc_cp_pair_32x128b_warpx4(sf_b, desc_scale_atom(smem_u32(s.sfb[stage])));
+    tc_cp_pair_32x128b_warpx4(sf_b + 4u, desc_scale_atom(smem_u32(s.sfb[stage] + kAtomBytes)));
+    tc_commit_pair(&s.sfready[stage], 0x1);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
   }
 }
 
@@ -237,17 +309,19 @@ __device__ __forceinline__ float gelu_tanh(float v) {
 }
 
 template <int EPI, bool DBG>
-__device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, int num_n,
-                                             int tiles, int m_total, int n_total,
+__device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, const TileWalk& wk,
+                                             int num_m, int m_total, int n_total,
                                              const uint16_t* __restrict__ bias, void* __restrict__ out,
                                              uint8_t* __restrict__ out_scales, float* __restrict__ dbg,
                                              volatile int* abort_flag) {
   const int q = warp & 3;           // tensor-memory lane quadrant this warp may access
   const int h = (warp - 2) >> 2;    // column half of the 256-wide tile
   uint32_t acc_phase = 0;
-  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-    const int mb = tile / num_n;
-    const int nb = tile - mb * num_n;
+  // the accumulator is released to the leader CTA's barrier (both CTAs' warps count)
+  const uint32_t tmem_empty_leader = mapa_shared(smem_u32(&s.tmem_empty), 0);
+  for (int p = wk.first; p < wk.pairs; p += wk.step) {
+    int mb, nb;
+    pair_tile(wk, p, &mb, &nb);
     int ok = 0;
     if (lane == 0) ok = wait_bounded(&s.tmem_full, acc_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -260,11 +334,11 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
     tc_wait_ld();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&s.tmem_empty);
+    if (lane == 0) mbar_arrive_remote(tmem_empty_leader);
     acc_phase ^= 1u;
 
     const int64_t row = static_cast<int64_t>(mb) * BM + 32 * q + lane;
-    const bool live = row < m_total;
+        const bool live = row < m_total;
     const int col0 = nb * BN + h * 128;
     if constexpr (EPI == 0) {
       uint16_t* y = static_cast<uint16_t*>(out);
@@ -331,9 +405,11 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
         }
         scale_word |= sc << (8 * c);
       }
-      // padding rows of the last row tile get zero scales
+      // padding rows of the last row tile get zero scales; a row tile past the
+      // last one (second half of the last pair) has no scale storage at all
       if (!live) scale_word = 0;
-      *reinterpret_cast<uint32_t*>(out_scales + scale_word_offset(row, col0 / kAtomK, n_total)) = scale_word;
+      if (mb < num_m)
+        *reinterpret_cast<uint32_t*>(out_scales + scale_word_offset(row, col0 / kAtomK, n_total)) = scale_word;
     }
   }
 }
@@ -341,7 +417,7 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
 template <int EPI, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   const uint8_t* __restrict__ sfa_g, const uint8_t* __restrict__ sfb_g,
+                   const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sb,
                    const uint16_t* __restrict__ bias, void* __restrict__ out, uint8_t* __restrict__ out_scales,
                    float* __restrict__ dbg, int m_total, int n_total, int k_total) {
   extern __shared__ uint8_t smem_raw[];
@@ -351,52 +427,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int num_n = n_total / BN;
-  const int tiles = ((m_total + BM - 1) / BM) * num_n;
+  const int num_m = (m_total + BM - 1) / BM;
   const int kblocks = k_total / BK;
+  TileWalk walk;
+  walk.num_n = num_n;
+  walk.pairs = ((num_m + kPair - 1) / kPair) * num_n;
+  walk.first = static_cast<int>(cluster_id_x());
+  walk.step = static_cast<int>(cluster_count_x());
+  walk.rank = static_cast<int>(cluster_ctarank());
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
+      mbar_init(&s.sfready[i], 1);
     }
     mbar_init(&s.tmem_full, 1);
-    mbar_init(&s.tmem_empty, kEpiWarps);
+    mbar_init(&s.tmem_empty, kPair * kEpiWarps);
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&s.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(&s.tmem_base, kTmemCols);  // both CTAs' warp 1 take part
+    tmem_relinquish_pair();
     tc_fence_before();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmap_a);
     prefetch_tensormap(&tmap_b);
+    prefetch_tensormap(&tmap_sa);
+    prefetch_tensormap(&tmap_sb);
   }
-  __syncthreads();
+  // both CTAs' barriers and tensor memory exist before either touches the other's
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
 
   if (warp == 0) {
-    if (lane == 0) run_producer(s, &tmap_a, &tmap_b, sfa_g, sfb_g, num_n, tiles, kblocks, abort_flag);
+    if (lane == 0) run_producer(s, &tmap_a, &tmap_b, &tmap_sa, &tmap_sb, walk, num_m, kblocks, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) run_mma(s, tmem, tiles, kblocks, abort_flag);
+    if (lane == 0 && walk.rank == 0) run_mma(s, tmem, walk, kblocks, abort_flag);
+  } else if (warp == 2 + kEpiWarps) {
+    if (lane == 0 && walk.rank == 0) run_scales(s, tmem, walk, kblocks, abort_flag);
   } else {
-    run_epilogue<EPI, DBG>(s, tmem, warp, lane, num_n, tiles, m_total, n_total, bias, out, out_scales, dbg,
+    run_epilogue<EPI, DBG>(s, tmem, warp, lane, walk, num_m, m_total, n_total, bias, out, out_scales, dbg,
                            abort_flag);
   }
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  // neither CTA leaves (or frees tensor memory) while its peer may still touch it
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
 // ------------------------------------------------------------------ host side
+
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -431,9 +521,36 @@ static bool make_codes_map(CUtensorMap* map, const void* codes, int64_t rows, in
   return r == CUDA_SUCCESS;
 }
 
+// Tensor maps over the tiled scales, one 512-byte atom = 128 uint32 per box row.
+// A: atoms [row tile][K step] as a 2-D [atoms][128]; box = one atom.
+// B: [row tile][K step][128] as 3-D; box = the two atoms of one 256-row N tile.
+static bool make_scale_maps(CUtensorMap* sa, CUtensorMap* sb, const void* a_scales, const void* b_scales, int64_t m,
+                            int64_t n, int64_t k) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t kblocks = static_cast<cuuint64_t>(k / BK);
+  std::memset(sa, 0, sizeof(*sa));
+  std::memset(sb, 0, sizeof(*sb));
+  cuuint64_t adims[2] = {128, static_cast<cuuint64_t>((m + BM - 1) / BM) * kblocks};
+  cuuint64_t astr[1] = {kAtomBytes};
+  cuuint32_t abox[2] = {128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(sa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(a_scales), adims, astr, abox, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  cuuint64_t bdims[3] = {128, kblocks, static_cast<cuuint64_t>(n / 128)};
+  cuuint64_t bstr[2] = {kAtomBytes, kblocks * kAtomBytes};
+  cuuint32_t bbox[3] = {128, 1, 2};
+  r = fn(sb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(b_scales), bdims, bstr, bbox, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int EPI, bool DBG>
-static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid,
-                                   cudaStream_t stream) {
+static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                                   const CUtensorMap& tsb, const GemmArgs& a, int64_t pairs, cudaStream_t stream) {
   auto kern = mx_gemm_kernel<EPI, DBG>;
   static bool configured[64] = {};
   int dev = 0;
@@ -444,25 +561,50 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(
-      ta, tb, static_cast<const uint8_t*>(a.a_scales), static_cast<const uint8_t*>(a.b_scales),
-      static_cast<const uint16_t*>(a.bias), a.out, static_cast<uint8_t*>(a.out_scales), a.debug_prequant,
-      static_cast<int>(a.m), static_cast<int>(a.n), static_cast<int>(a.k));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many CTA pairs as are co-resident (one CTA per SM), at most one per tile pair
+  static int max_clusters[64] = {};
+  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : 0;
+  if (clusters == 0) {
+    cfg.gridDim = dim3(kPair * 64, 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorLaunchOutOfResources;
+    if (dev >= 0 && dev < 64) max_clusters[dev] = clusters;
+  }
+  if (clusters > pairs) clusters = static_cast<int>(pairs);
+  cfg.gridDim = dim3(kPair * clusters, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, static_cast<const uint16_t*>(a.bias), a.out,
+                         static_cast<uint8_t*>(a.out_scales), a.debug_prequant, static_cast<int>(a.m),
+                         static_cast<int>(a.n), static_cast<int>(a.k));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, bool* encode_failed) {
   *encode_failed = false;
-  CUtensorMap ta, tb;
-  if (!make_codes_map(&ta, a.a_codes, a.m, a.k, BM) || !make_codes_map(&tb, a.b_codes, a.n, a.k, BN)) {
+  CUtensorMap ta, tb, tsa, tsb;
+  if (!make_codes_map(&ta, a.a_codes, a.m, a.k, BM) ||
+      !make_codes_map(&tb, a.b_codes, a.n, a.k, kBHalfRows) ||
+      !make_scale_maps(&tsa, &tsb, a.a_scales, a.b_scales, a.m, a.n, a.k)) {
     *encode_failed = true;
     return cudaSuccess;
   }
-  const int64_t tiles = ((a.m + BM - 1) / BM) * (a.n / BN);
-  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  if (a.epilogue == 0) return launch_instance<0, false>(ta, tb, a, grid, stream);
-  if (a.debug_prequant != nullptr) return launch_instance<1, true>(ta, tb, a, grid, stream);
-  return launch_instance<1, false>(ta, tb, a, grid, stream);
+  (void)num_sms;
+  const int64_t pairs = ((a.m + kPair * BM - 1) / (kPair * BM)) * (a.n / BN);
+  if (a.epilogue == 0) return launch_instance<0, false>(ta, tb, tsa, tsb, a, pairs, stream);
+  if (a.debug_prequant != nullptr) return launch_instance<1, true>(ta, tb, tsa, tsb, a, pairs, stream);
+  return launch_instance<1, false>(ta, tb, tsa, tsb, a, pairs, stream);
 }
 
 // A wait that nothing will ever satisfy: it must give up after the bound, set
