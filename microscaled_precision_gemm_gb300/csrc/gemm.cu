@@ -302,10 +302,16 @@ __device__ __forceinline__ void load_bias32(const uint16_t* __restrict__ bias, i
 
 // tanh-GELU as v * sigmoid(2u) = v / (1 + exp(-2u)), u = sqrt(2/pi) (v + 0.044715 v^3):
 // the same function as 0.5 v (1 + tanh(u)) without its cancellation for v < 0.
+// With u = sqrt(2/pi) (v + 0.044715 v^3), exp(-2u) = 2^t for
+// t = v (kGeluC2 + kGeluC1 v^2): kGeluC2 = -2 sqrt(2/pi) log2(e), kGeluC1 = 0.044715 kGeluC2.
+// For very negative v, 2^t is +inf and the result is v * 0 = -0 (the exact value
+// there is below 1e-37 in magnitude).
+constexpr float kGeluC2 = -2.0f * 0.7978845608028654f * 1.4426950408889634f;
+constexpr float kGeluC1 = 0.044715f * kGeluC2;
+
 __device__ __forceinline__ float gelu_tanh(float v) {
-  const float u = 0.7978845608028654f * fmaf(0.044715f * v, v * v, v);
-  const float e = __expf(fminf(-2.0f * u, 80.0f));
-  return __fdividef(v, 1.0f + e);
+  const float t = v * fmaf(kGeluC1, v * v, kGeluC2);
+  return v * rcp_approx(1.0f + ex2_approx(t));
 }
 
 template <int EPI, bool DBG>
@@ -381,27 +387,27 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
           }
         }
         uint32_t sc;
-        uint64_t w[3] = {0, 0, 0};
+        uint32_t w[6] = {0, 0, 0, 0, 0, 0};
         if (amax >= 0x7F800000u) {  // Inf or NaN: E8M0 NaN, zero codes
           sc = 0xFFu;
         } else {
           const int e = static_cast<int>(amax >> 23);
           sc = static_cast<uint32_t>(e > 2 ? e - 2 : 0);
           const float fac = __uint_as_float((254u - sc) << 23);  // 2^-s, exact
+          uint32_t grp[8];
 #pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            const uint32_t pr = cvt_e2m3x2(g[2 * p + 1] * fac, g[2 * p] * fac);
-            const uint64_t pair = (pr & 0x3Fu) | (((pr >> 8) & 0x3Fu) << 6);
-            const int bit = 12 * p;
-            w[bit / 64] |= pair << (bit % 64);
-            if (bit % 64 > 52) w[bit / 64 + 1] |= pair >> (64 - bit % 64);
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t lo = cvt_e2m3x2(g[4 * j + 1] * fac, g[4 * j] * fac);
+            const uint32_t hi = cvt_e2m3x2(g[4 * j + 3] * fac, g[4 * j + 2] * fac);
+            grp[j] = pack4(lo | (hi << 16));
           }
+          pack32(grp, w);
         }
         if (live) {
-          uint64_t* dst = reinterpret_cast<uint64_t*>(codes + row * (n_total / 4 * 3) + n / 4 * 3);
-          dst[0] = w[0];
-          dst[1] = w[1];
-          dst[2] = w[2];
+          uint2* dst = reinterpret_cast<uint2*>(codes + row * (n_total / 4 * 3) + n / 4 * 3);
+          dst[0] = make_uint2(w[0], w[1]);
+          dst[1] = make_uint2(w[2], w[3]);
+          dst[2] = make_uint2(w[4], w[5]);
         }
         scale_word |= sc << (8 * c);
       }

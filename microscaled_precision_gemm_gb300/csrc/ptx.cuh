@@ -287,6 +287,20 @@ __device__ __forceinline__ uint32_t cvt_e2m3x2(float hi, float lo) {
   return r;
 }
 
+// 2^x and 1/x on the special-function unit (PTX ex2.approx / rcp.approx, ftz):
+// relative errors of a couple of ulp; 2^x of a large x is +inf and 1/inf is 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Two fp32 -> packed bf16x2 (round-to-nearest-even); lo in the low half.
 __device__ __forceinline__ uint32_t cvt_bf16x2(float hi, float lo) {
   uint32_t r;

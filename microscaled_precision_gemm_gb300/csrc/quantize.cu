@@ -30,12 +30,6 @@ __device__ __forceinline__ uint4 ld_nc(const void* p) {
   return v;
 }
 
-// Four 6-bit codes held one per byte -> 24 bits, code i at bits 6i.
-__device__ __forceinline__ uint32_t pack4(uint32_t q) {
-  const uint32_t t = (q & 0x003F003Fu) | ((q >> 2) & 0x0FC00FC0u);  // c0 | c1<<6 | c2<<16 | c3<<22
-  return (t & 0xFFFu) | ((t >> 4) & 0xFFF000u);
-}
-
 // Quotient of n by an invariant divisor d with a precomputed magic number
 // (division by invariant integers using multiplication, round-up variant):
 // m = floor(2^32 (2^l - d) / d) + 1 with l = ceil(log2 d); q = (mulhi(n, m) + n) >> l.
@@ -120,12 +114,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_bf16_kernel(
           g[2 * j] = pack4(p[0] | (p[1] << 16));
           g[2 * j + 1] = pack4(p[2] | (p[3] << 16));
         }
-        w[0] = g[0] | (g[1] << 24);
-        w[1] = (g[1] >> 8) | (g[2] << 16);
-        w[2] = (g[2] >> 16) | (g[3] << 8);
-        w[3] = g[4] | (g[5] << 24);
-        w[4] = (g[5] >> 8) | (g[6] << 16);
-        w[5] = (g[6] >> 16) | (g[7] << 8);
+        pack32(g, w);
       }
       uint2* s2 = reinterpret_cast<uint2*>(&st[u][6 * lane]);
       s2[0] = make_uint2(w[0], w[1]);
