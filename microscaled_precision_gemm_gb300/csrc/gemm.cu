@@ -35,6 +35,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -54,7 +55,9 @@ constexpr int kStages = 6;
 constexpr int kPair = 2;              // CTAs per cluster (one MMA pair)
 constexpr uint16_t kPairMask = 0x3;
 constexpr int kBHalfRows = BN / kPair;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 8;                     // 2 per tensor-memory lane quadrant
+constexpr int kEpiCols = BN * 4 / kEpiWarps;     // accumulator columns each epilogue warp drains
+constexpr int kEpiChunks = kEpiCols / 32;        // 32-column MX blocks per epilogue thread
 constexpr int kThreads = (3 + kEpiWarps) * 32;  // + scale-copy warp
 constexpr uint32_t kABytes = BM * BK;  // 16-byte shared slot per 16 codes -> 1 byte per element
 constexpr uint32_t kBBytes = kBHalfRows * BK;   // this CTA's half of the B tile
@@ -80,8 +83,12 @@ struct __align__(1024) SharedStorage {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  alignas(16) float bias_s[kEpiWarps][kEpiCols];   // each epilogue warp's bias values (read as float4)
 };
 constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;
+static_assert(offsetof(SharedStorage, bias_s) % 16 == 0, "bias staging is read as float4");
+static_assert(offsetof(SharedStorage, sfa) % 128 == 0 && offsetof(SharedStorage, sfb) % 128 == 0,
+              "scale atoms are TMA destinations");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -222,29 +229,30 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const T
     }
     tc_fence_after();
     for (int kb = 0; kb < kblocks; ++kb) {
-      if (!wait_bounded(&s.full[stage], phase, abort_flag, kErrWaitMma)) {
-        ok = false;
-        break;
-      }
-      if (!wait_bounded(&s.sfready[stage], phase, abort_flag, kErrWaitMma)) {
+      // operands of both CTAs landed, scales copied into both SMs' tensor memory
+      if (!wait_bounded(&s.full[stage], phase, abort_flag, kErrWaitMma) ||
+          !wait_bounded(&s.sfready[stage], phase, abort_flag, kErrWaitMma)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sf_a = tmem + kSfCol0 + 16u * stage;
-      const uint32_t sf_b = sf_a + 8u;
-      const uint64_t ad = desc_sw128(smem_u32(s.a[stage]));
-      const uint64_t bd = desc_sw128(smem_u32(s.b[stage]));
+      {
+        const uint32_t sf_a = tmem + kSfCol0 + 16u * stage;
+        const uint32_t sf_b = sf_a + 8u;
+        const uint64_t ad = desc_sw128(smem_u32(s.a[stage]));
+        const uint64_t bd = desc_sw128(smem_u32(s.b[stage]));
 #pragma unroll
-      for (uint32_t j = 0; j < 4; ++j) {
-        // K step j: 32 elements = 32 bytes further along the swizzled 128-byte row
-        tc_mma_mx_pair(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j), sf_a, sf_b, (kb | static_cast<int>(j)) != 0);
-      }
-      tc_commit_pair(&s.empty[stage], kPairMask);  // frees the stage in both CTAs
-      issued = true;
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
+        for (uint32_t j = 0; j < 4; ++j) {
+          // K step j: 32 elements = 32 bytes further along the swizzled 128-byte row
+          tc_mma_mx_pair(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j), sf_a, sf_b,
+                         (kb | static_cast<int>(j)) != 0);
+        }
+        tc_commit_pair(&s.empty[stage], kPairMask);  // frees the stage in both CTAs
+        issued = true;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
     if (!ok) break;
@@ -281,27 +289,44 @@ __device__ __forceinline__ void run_scales(SharedStorage& s, uint32_t tmem, cons
   }
 }
 
-__device__ __forceinline__ void load_bias32(const uint16_t* __restrict__ bias, int n, float (&b)[32]) {
-  if (bias == nullptr) {
+// One epilogue warp stages the fp32 bias of its kEpiCols columns in shared memory
+// (lane i converts kEpiCols/32 consecutive columns); chunks then read broadcasts.
+__device__ __forceinline__ void stage_bias(float* bw, const uint16_t* __restrict__ bias, int n0, int lane) {
+  constexpr int kPer = kEpiCols / 32;
+  float f[kPer];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) b[i] = 0.0f;
-    return;
-  }
-  const uint4* p = reinterpret_cast<const uint4*>(bias + n);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint4 w = __ldg(p + v);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      b[8 * v + 2 * i] = __uint_as_float(ws[i] << 16);
-      b[8 * v + 2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+  for (int i = 0; i < kPer; ++i) f[i] = 0.f;
+  if (bias != nullptr) {
+    if constexpr (kPer == 4) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(bias + n0 + 4 * lane));
+      f[0] = __uint_as_float(w.x << 16);
+      f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+      f[2] = __uint_as_float(w.y << 16);
+      f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    } else {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(bias + n0 + 2 * lane));
+      f[0] = __uint_as_float(w << 16);
+      f[1] = __uint_as_float(w & 0xFFFF0000u);
     }
+  }
+  __syncwarp();  // the previous tile's reads are done
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) bw[kPer * lane + i] = f[i];
+  __syncwarp();
+}
+
+__device__ __forceinline__ void read_bias32(const float* bw, int c, float (&b)[32]) {
+  const float4* p = reinterpret_cast<const float4*>(bw + 32 * c);
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const float4 f = p[v];
+    b[4 * v] = f.x;
+    b[4 * v + 1] = f.y;
+    b[4 * v + 2] = f.z;
+    b[4 * v + 3] = f.w;
   }
 }
 
-// tanh-GELU as v * sigmoid(2u) = v / (1 + exp(-2u)), u = sqrt(2/pi) (v + 0.044715 v^3):
-// the same function as 0.5 v (1 + tanh(u)) without its cancellation for v < 0.
 // With u = sqrt(2/pi) (v + 0.044715 v^3), exp(-2u) = 2^t for
 // t = v (kGeluC2 + kGeluC1 v^2): kGeluC2 = -2 sqrt(2/pi) log2(e), kGeluC1 = 0.044715 kGeluC2.
 // For very negative v, 2^t is +inf and the result is v * 0 = -0 (the exact value
@@ -321,38 +346,43 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
                                              uint8_t* __restrict__ out_scales, float* __restrict__ dbg,
                                              volatile int* abort_flag) {
   const int q = warp & 3;           // tensor-memory lane quadrant this warp may access
-  const int h = (warp - 2) >> 2;    // column half of the 256-wide tile
+  const int h = (warp - 2) >> 2;    // column group (kEpiCols wide) of the 256-wide tile
   uint32_t acc_phase = 0;
   // the accumulator is released to the leader CTA's barrier (both CTAs' warps count)
   const uint32_t tmem_empty_leader = mapa_shared(smem_u32(&s.tmem_empty), 0);
   for (int p = wk.first; p < wk.pairs; p += wk.step) {
     int mb, nb;
     pair_tile(wk, p, &mb, &nb);
+    float* bw = s.bias_s[warp - 2];
+    stage_bias(bw, bias, nb * BN + h * kEpiCols, lane);
     int ok = 0;
     if (lane == 0) ok = wait_bounded(&s.tmem_full, acc_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     tc_fence_after();
-    uint32_t r[4][32];
-    const uint32_t t0 = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * 128);
+    uint32_t r[kEpiChunks][32];
+    const uint32_t t0 = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * kEpiCols);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(t0 + 32u * c, r[c]);
+    for (int c = 0; c < kEpiChunks; ++c) tc_ld_32x32b_x32(t0 + 32u * c, r[c]);
     tc_wait_ld();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive_remote(tmem_empty_leader);
+    // tcgen05.wait::ld has completed this warp's reads and the fence above orders
+    // them before the signal; no memory is handed over, so the arrive is relaxed
+    // (a release would first wait for the previous tile's global stores).
+    if (lane == 0) mbar_arrive_remote_relaxed(tmem_empty_leader);
     acc_phase ^= 1u;
 
     const int64_t row = static_cast<int64_t>(mb) * BM + 32 * q + lane;
         const bool live = row < m_total;
-    const int col0 = nb * BN + h * 128;
+    const int col0 = nb * BN + h * kEpiCols;
     if constexpr (EPI == 0) {
       uint16_t* y = static_cast<uint16_t*>(out);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kEpiChunks; ++c) {
         const int n = col0 + 32 * c;
         float b[32];
-        load_bias32(bias, n, b);
+        read_bias32(bw, c, b);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -368,17 +398,23 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
       uint8_t* codes = static_cast<uint8_t*>(out);
       uint32_t scale_word = 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kEpiChunks; ++c) {
         const int n = col0 + 32 * c;
         float b[32];
-        load_bias32(bias, n, b);
+        read_bias32(bw, c, b);
         float g[32];
-        uint32_t amax = 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          g[i] = gelu_tanh(__uint_as_float(r[c][i]) + b[i]);
-          amax = max(amax, __float_as_uint(g[i]) & 0x7FFFFFFFu);
-        }
+        for (int i = 0; i < 32; ++i) g[i] = gelu_tanh(__uint_as_float(r[c][i]) + b[i]);
+        // |g| order = unsigned order of the magnitude bits (NaN/Inf sort last); a tree keeps it shallow
+        uint32_t m[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          m[i] = max(__float_as_uint(g[2 * i]) & 0x7FFFFFFFu, __float_as_uint(g[2 * i + 1]) & 0x7FFFFFFFu);
+#pragma unroll
+        for (int w2 = 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int i = 0; i < w2; ++i) m[i] = max(m[i], m[i + w2]);
+        const uint32_t amax = m[0];
         if constexpr (DBG) {
           if (live) {
             float4* d = reinterpret_cast<float4*>(dbg + row * n_total + n);
@@ -414,8 +450,13 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
       // padding rows of the last row tile get zero scales; a row tile past the
       // last one (second half of the last pair) has no scale storage at all
       if (!live) scale_word = 0;
-      if (mb < num_m)
-        *reinterpret_cast<uint32_t*>(out_scales + scale_word_offset(row, col0 / kAtomK, n_total)) = scale_word;
+      if (mb < num_m) {
+        uint8_t* sw = out_scales + scale_word_offset(row, col0 / kAtomK, n_total) + (col0 % kAtomK) / 32;
+        if constexpr (kEpiChunks == 4)
+          *reinterpret_cast<uint32_t*>(sw) = scale_word;
+        else
+          *reinterpret_cast<uint16_t*>(sw) = static_cast<uint16_t>(scale_word);
+      }
     }
   }
 }
