@@ -58,9 +58,9 @@ CONFIGS = {
 # capture of the current kernel exists. Source summaries live in profiles/.
 # Written by hand from profiles/*_full_mlp.md (ncu on the full DiT MLP block).
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", "K1 quantize"): 125870848 + 22252544,
-    ("full_mlp", "K3 up GEMM+GELU+requant"): 80438784 + 148792320,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 229895680 + 104813824,
+    ("full_mlp", "K1 quantize"): 125852416 + 22633728,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 80900096 + 148366080,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 237485312 + 105883392,
 }
 
 

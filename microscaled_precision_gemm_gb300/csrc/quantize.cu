@@ -20,7 +20,7 @@
 namespace mxk {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 2;   // blocks per lane per iteration (8 x 16-byte loads in flight)
+constexpr int kQuantUnroll = 1;   // blocks per lane per iteration (4 x 16-byte loads in flight)
 
 __device__ __forceinline__ uint4 ld_nc(const void* p) {
   uint4 v;
@@ -162,7 +162,17 @@ cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t
   int64_t blocks = (warps_needed * 32 + kQuantThreads - 1) / kQuantThreads;
   const int64_t pad_blocks = ((pad_rows(rows) - rows) * (k / kAtomK) + kQuantThreads - 1) / kQuantThreads;
   if (blocks < pad_blocks) blocks = pad_blocks;
-  const int64_t cap = static_cast<int64_t>(num_sms) * (2048 / kQuantThreads);
+  // every block resident at once (grid-stride), so no second partial wave
+  static int resident_per_sm[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  int per_sm = (dev >= 0 && dev < 64) ? resident_per_sm[dev] : 0;
+  if (per_sm == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_bf16_kernel, kQuantThreads, 0);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    if (dev >= 0 && dev < 64) resident_per_sm[dev] = per_sm;
+  }
+  const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   quantize_bf16_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
