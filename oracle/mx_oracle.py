@@ -28,6 +28,11 @@ and it is the one of the OCP Microscaling Formats (MX) v1.0 specification:
 Each function below says which of these steps it follows. Readings taken where
 the pages and the contract are silent are listed in each docstring.
 
+The neighbouring fusions of the same section -- the gate and up projections
+stacked with the SwiGLU activation, modulation merged with RMSNorm before the
+quantizer, and an output projection merged with its gate and the residual add
+-- are restated at the end of the module ("Fused neighbours").
+
 Parity pins (tests/test_oracle.py): every function here is pinned against
 something other than itself -- the OCP MX value table typed in by hand, CUDA's
 own host-side fp6 conversion routine, brute-force integer GEMMs, mpmath, and
@@ -65,6 +70,12 @@ __all__ = [
     "up_projection",
     "down_projection",
     "mlp",
+    "silu",
+    "swiglu_up_projection",
+    "gated_mlp",
+    "rms_norm_modulate",
+    "gate_residual",
+    "dit_mlp_block",
 ]
 
 BLOCK = 32          # elements sharing one scale (OCP MX v1.0, block size k = 32)
@@ -357,3 +368,113 @@ def mlp(x_bits, w1_codes, w1_scales, b1_bits, w2_codes, w2_scales, b2_bits):
     hq, hs = quantize_f32(g.astype(np.float32))
     y = down_projection(hq, hs, w2_codes, w2_scales, b2_bits)
     return y, {"xq": xq, "xs": xs, "g": g, "hq": hq, "hs": hs}
+
+
+# --------------------------------------------------------------------------
+# Fused neighbours of the MLP
+#
+# "Optimizing Krea 3 on AMD Instinct MI355X", section "Fusion cut intermediate
+# memory traffic": the MLP's gate and up projections merge with the SwiGLU
+# activation; modulation merges with RMSNorm; an output projection merges with
+# its gate and the residual add. "Creating Custom Kernels for the AMD MI300",
+# sections "Fused RMS Norm Kernel" and "Fused SwiGLU Kernel": row-wise RMS
+# normalisation and the SwiGLU activation, each followed by the quantization of
+# its output in the same kernel.
+# --------------------------------------------------------------------------
+
+def silu(v) -> np.ndarray:
+    """SiLU in fp64: v * sigmoid(v) = v / (1 + exp(-v)).
+
+    For v below about -709, exp(-v) overflows to +inf and the quotient is -0,
+    the correctly rounded value of a number below 1e-300 in magnitude.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def swiglu_up_projection(xq_codes, xq_scales, wgu_codes, wgu_scales, bgu_bits):
+    """Gate and up projections as one stacked GEMM, SwiGLU epilogue, fp64.
+
+    The stacked weight holds the F gate rows first and the F up rows after them
+    (N = 2F rows of K, each row quantized on its own, so stacking is a plain
+    concatenation of the two MXFP6 weights); the stacked bias likewise [b_g; b_u].
+      g = x W_g^T + b_g,  u = x W_u^T + b_u,  h = silu(g) * u.
+    Returns h [M][F] in fp64. As for the GELU epilogue, parity requantizes the
+    GPU's own fp32 h (quantize_f32).
+    """
+    c = gemm(xq_codes, xq_scales, wgu_codes, wgu_scales, bgu_bits)
+    f = c.shape[1] // 2
+    return silu(c[:, :f]) * c[:, f:]
+
+
+def gated_mlp(x_bits, wgu_codes, wgu_scales, bgu_bits, w2_codes, w2_scales, b2_bits):
+    """The SwiGLU MLP, independent of any GPU value.
+
+    x (BF16) -> MXFP6 -> stacked gate/up projection + SwiGLU -> rounded to fp32
+    -> MXFP6 -> down-projection + bias. Same readings as mlp().
+    Returns (y fp64 [M][d], intermediate dict).
+    """
+    xq, xs = quantize_bf16(x_bits)
+    h = swiglu_up_projection(xq, xs, wgu_codes, wgu_scales, bgu_bits)
+    hq, hs = quantize_f32(h.astype(np.float32))
+    y = down_projection(hq, hs, w2_codes, w2_scales, b2_bits)
+    return y, {"xq": xq, "xs": xs, "h": h, "hq": hq, "hs": hs}
+
+
+def rms_norm_modulate(x_bits, shift_bits, scale_bits, eps: float) -> np.ndarray:
+    """Row-wise RMS normalisation followed by modulation, fp64.
+
+      y[m][k] = x[m][k] / sqrt(mean_k' x[m][k']^2 + eps) * (1 + scale[k]) + shift[k]
+
+    x is BF16 [M][K]; shift and scale are BF16 [K] (one conditioning vector per
+    sample; this library's workloads are one sample). Readings: the norm carries
+    no learned weight of its own (the modulation is its affine part) and eps is
+    added to the mean square inside the root. The quantizer that follows rounds
+    y to fp32 first (the precision the fused kernel keeps), so parity
+    requantizes the GPU's own fp32 y (quantize_f32).
+    """
+    x = bf16_bits_to_f64(x_bits)
+    shift = bf16_bits_to_f64(shift_bits)
+    scale = bf16_bits_to_f64(scale_bits)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * (1.0 + scale) + shift
+
+
+def gate_residual(c, gate_bits, residual_bits) -> np.ndarray:
+    """Output-projection epilogue with gate and residual, fp64.
+
+      y[m][n] = residual[m][n] + gate[n] * c[m][n]
+
+    c is the projection with its bias already added (gemm(..., bias)); gate is
+    BF16 [N] (one conditioning vector per sample), residual BF16 [M][N]. The BF16
+    store of y is compared with tolerance.
+    """
+    c = np.asarray(c, dtype=np.float64)
+    return bf16_bits_to_f64(residual_bits) + bf16_bits_to_f64(gate_bits)[None, :] * c
+
+
+def dit_mlp_block(x_bits, shift_bits, scale_bits, gate_bits, eps: float, w_up_codes, w_up_scales, b_up_bits,
+                  w2_codes, w2_scales, b2_bits, activation: str = "gelu"):
+    """The MLP half of a diffusion-transformer block, independent of any GPU value.
+
+      y = x + gate * (MLP(MXFP6(rms_norm_modulate(x))) + b2)
+
+    with MLP = up-projection + activation ("gelu": tanh-GELU, w_up is W1 [F][d];
+    "swiglu": w_up is the stacked [W_g; W_u] [2F][d]), the intermediate rounded
+    to fp32 and requantized, then the down-projection. Each rounding to fp32
+    before a quantization is the reading the fused kernels take.
+    Returns (y fp64 [M][d], intermediate dict).
+    """
+    a = rms_norm_modulate(x_bits, shift_bits, scale_bits, eps)
+    xq, xs = quantize_f32(a.astype(np.float32))
+    if activation == "gelu":
+        h = up_projection(xq, xs, w_up_codes, w_up_scales, b_up_bits)
+    elif activation == "swiglu":
+        h = swiglu_up_projection(xq, xs, w_up_codes, w_up_scales, b_up_bits)
+    else:
+        raise ValueError(f"unknown activation {activation!r}")
+    hq, hs = quantize_f32(h.astype(np.float32))
+    c = down_projection(hq, hs, w2_codes, w2_scales, b2_bits)
+    y = gate_residual(c, gate_bits, x_bits)
+    return y, {"a": a, "xq": xq, "xs": xs, "h": h, "hq": hq, "hs": hs, "c": c}

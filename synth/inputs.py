@@ -16,11 +16,18 @@ full_mlp       x[20480][3072] ~ N(0,1); W1[12288][3072], W2[3072][12288] ~ N(0,0
 outlier_mlp    x[20480][4096] ~ Student-t(3); 41 channels (1%, seeded permutation)
                scaled x100; 1% of (row, 32-block) pairs set to +0 (Bernoulli 0.01);
                W1[16384][4096], W2[4096][16384] ~ N(0,0.02); b1, b2 ~ N(0,0.01)
+gated_mlp      x[20480][3072] ~ N(0,1); stacked [W_g; W_u][2*8192][3072] ~ N(0,0.02),
+               [b_g; b_u][16384] ~ N(0,0.01); W2[3072][8192] ~ N(0,0.02); b2 ~ N(0,0.01)
+qkv_proj       x[20480][3072] ~ N(0,1); stacked [W_q; W_k; W_v; W_gate][12288][3072]
+               ~ N(0,0.02); b[12288] ~ N(0,0.01)
+dit_block      as full_mlp (or gated_mlp's weights), plus the conditioning vectors
+               shift, scale, gate [3072] ~ N(0,0.5) and eps = 1e-6
 =============  ======================================================================
 
 Every workload uses seed 0 by default. Each tensor draws from its own child of
 SeedSequence(seed), spawned in the fixed order x, W1, b1, W2, b2, channel
-scales, masks, so that shrinking one tensor never changes another. Values are
+scales, masks, shift, scale, gate, so that shrinking one tensor never changes
+another (stacked weights draw all their rows from the W1 / b1 child). Values are
 drawn in fp32 and rounded to BF16 with round-to-nearest-even; BF16 tensors are
 returned as uint16 bit patterns.
 """
@@ -38,10 +45,13 @@ __all__ = [
     "dit_down",
     "full_mlp",
     "outlier_mlp",
+    "gated_mlp",
+    "qkv_proj",
+    "dit_block",
     "WORKLOADS",
 ]
 
-_ORDER = ("x", "w1", "b1", "w2", "b2", "chan", "mask")
+_ORDER = ("x", "w1", "b1", "w2", "b2", "chan", "mask", "shift", "scale", "gate")
 
 
 def bf16_round(x) -> np.ndarray:
@@ -154,12 +164,62 @@ def outlier_mlp(seed: int = 0, M: int = 20480, d: int = 4096, ff: int = 16384) -
     }
 
 
+def gated_mlp(seed: int = 0, M: int = 20480, d: int = 3072, ff: int = 8192) -> dict:
+    """SwiGLU MLP: x, stacked gate/up weight wgu [2 ff][d] (gate rows first) and
+    bias bgu [2 ff], W2 [d][ff], b2 (BF16 bits). ff = 8192 is 2/3 of 4d, so the
+    three GEMMs do the same work as the GELU MLP's two at ff = 4d."""
+    r = _rngs(seed)
+    return {
+        "x": _normal_bf16(r["x"], (M, d), 1.0),
+        "wgu": _normal_bf16(r["w1"], (2 * ff, d), 0.02),
+        "bgu": _normal_bf16(r["b1"], (2 * ff,), 0.01),
+        "w2": _normal_bf16(r["w2"], (d, ff), 0.02),
+        "b2": _normal_bf16(r["b2"], (d,), 0.01),
+    }
+
+
+def qkv_proj(seed: int = 0, M: int = 20480, d: int = 3072, stack: int = 4) -> dict:
+    """Stacked query/key/value/attention-gate projection: x [M][d], w [4d][d], b [4d]."""
+    r = _rngs(seed)
+    return {
+        "x": _normal_bf16(r["x"], (M, d), 1.0),
+        "w": _normal_bf16(r["w1"], (stack * d, d), 0.02),
+        "b": _normal_bf16(r["b1"], (stack * d,), 0.01),
+    }
+
+
+def dit_block(seed: int = 0, M: int = 20480, d: int = 3072, ff: int | None = None,
+              activation: str = "gelu") -> dict:
+    """MLP half of a DiT block: x, conditioning shift/scale/gate [d], eps, the up
+    weight w_up (W1 [ff][d] for "gelu", stacked [W_g; W_u] [2 ff][d] for "swiglu"),
+    b_up, W2 [d][ff], b2. ff defaults to 4d (gelu) or 8d/3 (swiglu)."""
+    if ff is None:
+        ff = 4 * d if activation == "gelu" else (8 * d) // 3
+    r = _rngs(seed)
+    rows_up = ff if activation == "gelu" else 2 * ff
+    return {
+        "x": _normal_bf16(r["x"], (M, d), 1.0),
+        "w_up": _normal_bf16(r["w1"], (rows_up, d), 0.02),
+        "b_up": _normal_bf16(r["b1"], (rows_up,), 0.01),
+        "w2": _normal_bf16(r["w2"], (d, ff), 0.02),
+        "b2": _normal_bf16(r["b2"], (d,), 0.01),
+        "shift": _normal_bf16(r["shift"], (d,), 0.5),
+        "scale": _normal_bf16(r["scale"], (d,), 0.5),
+        "gate": _normal_bf16(r["gate"], (d,), 0.5),
+        "eps": 1e-6,
+        "activation": activation,
+    }
+
+
 WORKLOADS = {
     "pr1": pr1,
     "dit_up": dit_up,
     "dit_down": dit_down,
     "full_mlp": full_mlp,
     "outlier_mlp": outlier_mlp,
+    "gated_mlp": gated_mlp,
+    "qkv_proj": qkv_proj,
+    "dit_block": dit_block,
 }
 
 
