@@ -62,9 +62,15 @@ typedef enum {
 } mx_status;
 
 typedef enum {
-  MX_EPI_BIAS_BF16 = 0,        /* out = bf16_rne(acc + bias): the down-projection (K2)      */
-  MX_EPI_BIAS_GELU_MXFP6 = 1   /* out = MXFP6(gelu_tanh(acc + bias)): the up-projection (K3) */
+  MX_EPI_BIAS_BF16 = 0,          /* out = bf16_rne(acc + bias): the down-projection (K2)       */
+  MX_EPI_BIAS_GELU_MXFP6 = 1,    /* out = MXFP6(gelu_tanh(acc + bias)): the up-projection (K3)  */
+  MX_EPI_BIAS_SWIGLU_MXFP6 = 2   /* stacked gate/up weight: out = MXFP6(silu(g) * u)            */
 } mx_epilogue;
+
+typedef enum {
+  MX_ACT_GELU_TANH = 0,   /* up-projection W1 [ff][d], h = gelu_tanh(x W1^T + b1)                 */
+  MX_ACT_SWIGLU = 1       /* stacked [W_g; W_u] [2ff][d], h = silu(x W_g^T + b_g) * (x W_u^T + b_u) */
+} mx_activation;
 
 /* Bytes of the packed codes of a rows x K MXFP6 tensor: rows * 3K/4. */
 size_t mx_codes_bytes(int64_t rows, int64_t K);
@@ -90,6 +96,27 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, void
                       cudaStream_t stream);
 
 /*
+ * mx_quantize_rmsnorm_modulate -- K1 with the step before it fused in: row-wise
+ * RMS normalisation, modulation, then MXFP6 quantization of the result
+ * ("Optimizing Krea 3 on AMD Instinct MI355X", section "Fusion cut intermediate
+ * memory traffic": modulation merged with RMSNorm; "Creating Custom Kernels for
+ * the AMD MI300", section "Fused RMS Norm Kernel").
+ *   y[m][k] = x[m][k] / sqrt(mean_k' x[m][k']^2 + eps) * (1 + scale[k]) + shift[k]
+ * in fp32 (sum of squares in fp32, 1/sqrt correctly rounded, then
+ * fma(x * rstd, 1 + scale, shift)); codes/scales = MXFP6(y) by the mx_quantize rule.
+ *   x, rows, K, ld_x, codes, scales : as mx_quantize, and K <= 8192
+ *   shift, scale : device BF16 [K] (one conditioning vector for all rows), 16-byte
+ *                  aligned, or NULL for zeros
+ *   eps          : >= 0 and finite (with eps = 0 an all-zero row gives NaN, whose
+ *                  blocks get scale 0xFF and zero codes)
+ *   debug_y      : NULL, or device fp32 [rows][K] (16-byte aligned) that receives y,
+ *                  the exact values the quantization rounded (test hook)
+ */
+mx_status mx_quantize_rmsnorm_modulate(const void* x, int64_t rows, int64_t K, int64_t ld_x, const void* shift,
+                                       const void* scale, float eps, void* codes, void* scales, float* debug_y,
+                                       cudaStream_t stream);
+
+/*
  * mx_gemm -- K2/K3: C = A * B^T on MXFP6 operands, fp32 accumulation in tensor
  * memory, then the fused epilogue `epi`:
  *   MX_EPI_BIAS_BF16      : out = BF16 [M][N] row-major, bf16_rne(C + bias)
@@ -97,21 +124,52 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, void
  *                           gelu_tanh(v) = 0.5 v (1 + tanh(sqrt(2/pi)(v + 0.044715 v^3)));
  *                           out = MXFP6 codes of g [M][N] (same rule as mx_quantize,
  *                           blocks of 32 along N), out_scales = its tiled scales.
+ *   MX_EPI_BIAS_SWIGLU_MXFP6: the gate and up projections of a SwiGLU MLP as one
+ *                           GEMM ("Optimizing Krea 3 on AMD Instinct MI355X", section
+ *                           "Fusion cut intermediate memory traffic"; "Creating Custom
+ *                           Kernels for the AMD MI300", section "Fused SwiGLU Kernel").
+ *                           B is the stacked weight [W_g; W_u]: its first F = N/2 rows
+ *                           are the gate rows, the next F the up rows (quantize W_g and
+ *                           W_u into the two halves of one buffer); bias likewise
+ *                           [b_g; b_u] (2F values). With C = [G | U]:
+ *                           h = silu(G + b_g) * (U + b_u) in fp32, silu(v) = v/(1+e^-v);
+ *                           out = MXFP6 codes of h [M][F], out_scales its tiled
+ *                           scales (mx_scales_bytes(M, F)).
  *   a_codes/a_scales : A, M x K MXFP6 (activations)
  *   b_codes/b_scales : B, N x K MXFP6 (weights, nn.Linear layout)
  *   bias             : device BF16 [N], 16-byte aligned, or NULL (no bias)
  *   M >= 0 (any value; 0 is a no-op), N % 256 == 0, K % 128 == 0 and K > 0,
  *   M, N, K < 2^31.
- *   out              : BF16 [M][N] (16-byte aligned) or codes mx_codes_bytes(M, N)
- *   out_scales       : MXFP6 epilogue only: mx_scales_bytes(M, N) bytes; else ignored
- *   debug_prequant   : MXFP6 epilogue only, may be NULL: fp32 [M][N] receives g,
- *                      the exact value the requantization rounded (test hook).
+ *   out              : BF16 [M][N] (16-byte aligned) or codes mx_codes_bytes(M, W),
+ *                      W = N (GELU) or N/2 (SwiGLU), 32-byte aligned
+ *   out_scales       : MXFP6 epilogues only: mx_scales_bytes(M, W) bytes; else ignored
+ *   debug_prequant   : MXFP6 epilogues only, may be NULL: fp32 [M][W] receives g
+ *                      (or h), the exact value the requantization rounded (test hook).
  */
 mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
                   const void* bias, int64_t M, int64_t N, int64_t K, mx_epilogue epi, void* out,
                   void* out_scales, float* debug_prequant, cudaStream_t stream);
 
-/* Workspace bytes mx_mlp needs for M tokens: MXFP6 x (M x d) and MXFP6 h (M x ff). */
+/*
+ * mx_gemm_gate_residual -- an output projection fused with its gate and the
+ * residual add ("Optimizing Krea 3 on AMD Instinct MI355X", section "Fusion cut
+ * intermediate memory traffic"):
+ *   out[m][n] = bf16_rne(residual[m][n] + gate[n] * (C[m][n] + bias[n])),  C = A * B^T
+ * computed in fp32 as fma(gate, C + bias, residual).
+ *   A, B, bias, M, N, K : as mx_gemm (MXFP6 operands, N % 256 == 0, K % 128 == 0)
+ *   gate     : device BF16 [N] (one conditioning vector for all rows), 16-byte
+ *              aligned, or NULL for a gate of 1 (plain residual add)
+ *   residual : device BF16 [M][N] row-major, 16-byte aligned; required
+ *   out      : device BF16 [M][N] row-major, 16-byte aligned (written). It may be
+ *              residual itself (in-place update: each element is read before it
+ *              is written, by the same thread); any other overlap returns
+ *              MX_ERR_INVALID_ARG.
+ */
+mx_status mx_gemm_gate_residual(const void* a_codes, const void* a_scales, const void* b_codes,
+                                const void* b_scales, const void* bias, const void* gate, const void* residual,
+                                int64_t M, int64_t N, int64_t K, void* out, cudaStream_t stream);
+
+/* Workspace bytes mx_mlp and mx_gated_mlp need for M tokens: MXFP6 x (M x d) and MXFP6 h (M x ff). */
 size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff);
 
 /*
@@ -128,6 +186,40 @@ size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff);
 mx_status mx_mlp(const void* x, int64_t M, int64_t d, int64_t ff, const void* w1_codes, const void* w1_scales,
                  const void* b1, const void* w2_codes, const void* w2_scales, const void* b2, void* y,
                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * mx_gated_mlp -- the SwiGLU MLP block in three launches on `stream`:
+ *   K1 xq = MXFP6(x); up hq = MXFP6(silu(xq W_g^T + b_g) * (xq W_u^T + b_u));
+ *   K2 y = bf16(hq W2^T + b2).
+ *   wgu_*    : the stacked [W_g; W_u] as MXFP6, 2ff x d (gate rows first)
+ *   bgu      : BF16 [2ff] = [b_g; b_u], or NULL
+ *   w2_*     : W2 as MXFP6, d x ff;  b2: BF16 [d] or NULL
+ *   d % 256 == 0, ff % 128 == 0; workspace as mx_mlp (mx_mlp_workspace_bytes(M, d, ff)).
+ */
+mx_status mx_gated_mlp(const void* x, int64_t M, int64_t d, int64_t ff, const void* wgu_codes,
+                       const void* wgu_scales, const void* bgu, const void* w2_codes, const void* w2_scales,
+                       const void* b2, void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * mx_dit_mlp_block -- the MLP half of a diffusion-transformer block, with both
+ * neighbouring fusions of "Optimizing Krea 3 on AMD Instinct MI355X", section
+ * "Fusion cut intermediate memory traffic", in three launches on `stream`:
+ *   1. xq = MXFP6(x / rms(x) * (1 + scale) + shift)    (mx_quantize_rmsnorm_modulate)
+ *   2. hq = MXFP6(act(xq W_up^T + b_up))                (GELU, or SwiGLU on [W_g; W_u])
+ *   3. y  = bf16(x + gate * (hq W2^T + b2))             (mx_gemm_gate_residual, residual x)
+ *   x          : BF16 [M][d]; y: BF16 [M][d], may be x itself (in place), no other overlap
+ *   shift, scale, gate : BF16 [d] conditioning vectors (one sample), or NULL (0, 0, 1)
+ *   eps        : as mx_quantize_rmsnorm_modulate
+ *   activation : MX_ACT_GELU_TANH (w_up = W1, ff x d; b_up [ff]) or MX_ACT_SWIGLU
+ *                (w_up = [W_g; W_u], 2ff x d; b_up [2ff])
+ *   w2_*, b2   : W2 as MXFP6, d x ff; BF16 [d] or NULL
+ *   d % 256 == 0, d <= 8192, ff % 128 == 0 (ff % 256 == 0 for GELU);
+ *   workspace  : >= mx_mlp_workspace_bytes(M, d, ff), 256-byte aligned.
+ */
+mx_status mx_dit_mlp_block(const void* x, int64_t M, int64_t d, int64_t ff, const void* shift, const void* scale,
+                           const void* gate, float eps, mx_activation activation, const void* w_up_codes,
+                           const void* w_up_scales, const void* b_up, const void* w2_codes, const void* w2_scales,
+                           const void* b2, void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Capacity of the static scratch of mx_mlp_noalloc: 64 MiB per GPU. */
 #define MX_MLP_NOALLOC_WORKSPACE_BYTES ((size_t)64 << 20)

@@ -10,6 +10,9 @@ Entry points keep the C names:
 * ``mx_quantize(x)`` -- BF16 [rows][K] -> (codes uint8 [rows][3K/4], tiled scales uint8)
 * ``mx_gemm(a, b, bias, epilogue)`` -- block-scaled MXFP6 GEMM with a fused epilogue
 * ``mx_mlp(x, w1, b1, w2, b2)`` -- quantize -> up-proj + GELU + requant -> down-proj
+* ``mx_gated_mlp(x, wgu, bgu, w2, b2)`` -- the same with a SwiGLU up-projection on the
+  stacked [W_g; W_u] weight (``mx_quantize_stacked`` builds it)
+* ``mx_gemm_gate_residual(a, b, bias, gate, residual)`` -- residual + gate * (A B^T + bias)
 * ``mx_scales_to_plain`` / ``mx_scales_from_plain`` -- host-side scale layout helpers
 """
 
@@ -28,6 +31,7 @@ __all__ = [
     "MxError",
     "MX_EPI_BIAS_BF16",
     "MX_EPI_BIAS_GELU_MXFP6",
+    "MX_EPI_BIAS_SWIGLU_MXFP6",
     "MxTensor",
     "load",
     "library_path",
@@ -35,8 +39,15 @@ __all__ = [
     "mx_scales_bytes",
     "mx_mlp_workspace_bytes",
     "mx_quantize",
+    "mx_quantize_rmsnorm_modulate",
+    "mx_quantize_stacked",
     "mx_gemm",
+    "mx_gemm_gate_residual",
     "mx_mlp",
+    "mx_gated_mlp",
+    "mx_dit_mlp_block",
+    "MX_ACT_GELU_TANH",
+    "MX_ACT_SWIGLU",
     "mx_status_string",
     "mx_scales_to_plain",
     "mx_scales_from_plain",
@@ -48,6 +59,9 @@ __all__ = [
 
 MX_EPI_BIAS_BF16 = 0
 MX_EPI_BIAS_GELU_MXFP6 = 1
+MX_EPI_BIAS_SWIGLU_MXFP6 = 2
+MX_ACT_GELU_TANH = 0
+MX_ACT_SWIGLU = 1
 
 EXPORTED_SYMBOLS = (
     "mx_codes_bytes",
@@ -63,6 +77,10 @@ EXPORTED_SYMBOLS = (
     "mx_selftest_wait_timeout",
     "mx_version",
     "mx_mlp_noalloc",
+    "mx_gemm_gate_residual",
+    "mx_gated_mlp",
+    "mx_quantize_rmsnorm_modulate",
+    "mx_dit_mlp_block",
 )
 
 _lib = None
@@ -103,6 +121,12 @@ def load():
             "mx_gemm": (ctypes.c_int, [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]),
             "mx_mlp_workspace_bytes": (sz, [i64, i64, i64]),
             "mx_mlp": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "mx_gated_mlp": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "mx_gemm_gate_residual": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]),
+            "mx_quantize_rmsnorm_modulate": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, ctypes.c_float, vp, vp, vp,
+                                                            vp]),
+            "mx_dit_mlp_block": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, ctypes.c_float, ctypes.c_int, vp, vp,
+                                                vp, vp, vp, vp, vp, vp, sz, vp]),
             "mx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "mx_scales_to_plain": (ctypes.c_int, [vp, vp, i64, i64]),
             "mx_scales_from_plain": (ctypes.c_int, [vp, vp, i64, i64]),
@@ -190,13 +214,60 @@ def mx_quantize(x, out: MxTensor | None = None, stream=None) -> MxTensor:
     return out
 
 
+def mx_quantize_rmsnorm_modulate(x, shift=None, scale=None, eps: float = 1e-6, out: MxTensor | None = None,
+                                 debug_y=None, stream=None) -> MxTensor:
+    """RMSNorm + modulation + K1: MXFP6(x / rms(x) * (1 + scale) + shift) of a BF16 [rows][K] tensor."""
+    torch = _torch()
+    lib = load()
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("mx_quantize_rmsnorm_modulate wants a CUDA bfloat16 [rows][K] tensor")
+    rows, k = x.shape
+    for name, v in (("shift", shift), ("scale", scale)):
+        if v is not None and (v.dtype != torch.bfloat16 or v.numel() != k):
+            raise ValueError(f"{name} must be bfloat16 [K]")
+    if out is None:
+        codes = _empty_u8(lib.mx_codes_bytes(rows, k), x.device).view(rows, -1) if rows else \
+            _empty_u8(0, x.device).view(0, k // 4 * 3)
+        out = MxTensor(codes, _empty_u8(lib.mx_scales_bytes(rows, k), x.device), rows, k)
+    st = lib.mx_quantize_rmsnorm_modulate(_ptr(x), rows, k, x.stride(0), _ptr(shift), _ptr(scale), float(eps),
+                                          _ptr(out.codes), _ptr(out.scales), _ptr(debug_y), _stream_handle(stream))
+    _check(st, "mx_quantize_rmsnorm_modulate")
+    return out
+
+
+def mx_quantize_stacked(parts, stream=None) -> MxTensor:
+    """Quantize BF16 matrices [R_i][K] into one stacked MXFP6 tensor [sum R_i][K].
+
+    Rows are quantized independently, so the result is the concatenation of the
+    parts' MXFP6 forms; every part but the last needs R_i % 128 == 0 (its tiled
+    scales then end on an atom boundary). Builds the [W_g; W_u] weight of
+    mx_gated_mlp and the stacked query/key/value/gate weight of one projection.
+    """
+    lib = load()
+    k = parts[0].shape[1]
+    rows = sum(int(p.shape[0]) for p in parts)
+    if any(p.shape[1] != k for p in parts) or any(p.shape[0] % 128 for p in parts[:-1]):
+        raise ValueError("parts need equal K and all but the last a multiple of 128 rows")
+    dev = parts[0].device
+    codes = _empty_u8(lib.mx_codes_bytes(rows, k), dev).view(rows, -1)
+    scales = _empty_u8(lib.mx_scales_bytes(rows, k), dev)
+    r0 = 0
+    for p in parts:
+        r = int(p.shape[0])
+        s0 = lib.mx_scales_bytes(r0, k)
+        mx_quantize(p, MxTensor(codes[r0:r0 + r], scales[s0:s0 + lib.mx_scales_bytes(r, k)], r, k), stream)
+        r0 += r
+    return MxTensor(codes, scales, rows, k)
+
+
 def mx_gemm(a: MxTensor, b: MxTensor, bias=None, epilogue: int = MX_EPI_BIAS_BF16, out=None,
             debug_prequant=None, stream=None):
     """K2/K3: a [M][K] x b [N][K]^T on MXFP6 with the fused epilogue.
 
-    Returns a BF16 [M][N] tensor (MX_EPI_BIAS_BF16) or an MxTensor of [M][N]
-    (MX_EPI_BIAS_GELU_MXFP6). ``debug_prequant`` (fp32 [M][N]) receives the
-    GELU output the requantization rounds.
+    Returns a BF16 [M][N] tensor (MX_EPI_BIAS_BF16) or an MxTensor of [M][W]
+    (W = N for MX_EPI_BIAS_GELU_MXFP6, N/2 for MX_EPI_BIAS_SWIGLU_MXFP6, where b
+    is the stacked [W_g; W_u]). ``debug_prequant`` (fp32 [M][W]) receives the
+    activation output the requantization rounds.
     """
     torch = _torch()
     lib = load()
@@ -209,10 +280,11 @@ def mx_gemm(a: MxTensor, b: MxTensor, bias=None, epilogue: int = MX_EPI_BIAS_BF1
             out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
         out_ptr, out_sc = _ptr(out), None
     else:
+        w = n // 2 if epilogue == MX_EPI_BIAS_SWIGLU_MXFP6 else n
         if out is None:
-            out = MxTensor(_empty_u8(lib.mx_codes_bytes(m, n), dev).view(m, -1) if m else
-                           _empty_u8(0, dev).view(0, n // 4 * 3),
-                           _empty_u8(lib.mx_scales_bytes(m, n), dev), m, n)
+            out = MxTensor(_empty_u8(lib.mx_codes_bytes(m, w), dev).view(m, -1) if m else
+                           _empty_u8(0, dev).view(0, w // 4 * 3),
+                           _empty_u8(lib.mx_scales_bytes(m, w), dev), m, w)
         out_ptr, out_sc = _ptr(out.codes), _ptr(out.scales)
     if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != n):
         raise ValueError("bias must be bfloat16 [N]")
@@ -239,6 +311,69 @@ def mx_mlp(x, w1: MxTensor, b1, w2: MxTensor, b2, y=None, workspace=None, stream
                     _ptr(w2.scales), _ptr(b2), _ptr(y), _ptr(workspace), workspace.numel(),
                     _stream_handle(stream))
     _check(st, "mx_mlp")
+    return y
+
+
+def mx_gemm_gate_residual(a: MxTensor, b: MxTensor, bias, gate, residual, out=None, stream=None):
+    """out = bf16(residual + gate * (a b^T + bias)); out may be residual (in place)."""
+    torch = _torch()
+    lib = load()
+    if a.k != b.k:
+        raise ValueError("inner dimensions differ")
+    m, n, k = a.rows, b.rows, a.k
+    if residual.dtype != torch.bfloat16 or tuple(residual.shape) != (m, n) or not residual.is_contiguous():
+        raise ValueError("residual must be a contiguous bfloat16 [M][N] tensor")
+    for name, v in (("bias", bias), ("gate", gate)):
+        if v is not None and (v.dtype != torch.bfloat16 or v.numel() != n):
+            raise ValueError(f"{name} must be bfloat16 [N]")
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=residual.device)
+    st = lib.mx_gemm_gate_residual(_ptr(a.codes), _ptr(a.scales), _ptr(b.codes), _ptr(b.scales), _ptr(bias),
+                                   _ptr(gate), _ptr(residual), m, n, k, _ptr(out), _stream_handle(stream))
+    _check(st, "mx_gemm_gate_residual")
+    return out
+
+
+def mx_gated_mlp(x, wgu: MxTensor, bgu, w2: MxTensor, b2, y=None, workspace=None, stream=None):
+    """K1 + SwiGLU up-projection + K2: y = bf16(MXFP6(silu(g) * u) W2^T + b2),
+    [g | u] = MXFP6(x) [W_g; W_u]^T + [b_g; b_u]."""
+    torch = _torch()
+    lib = load()
+    m, d = x.shape
+    ff = wgu.rows // 2
+    if wgu.k != d or wgu.rows != 2 * ff or w2.rows != d or w2.k != ff:
+        raise ValueError("weight shapes do not match x")
+    if y is None:
+        y = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
+    need = lib.mx_mlp_workspace_bytes(m, d, ff)
+    if workspace is None:
+        workspace = _empty_u8(max(need, 256), x.device)
+    st = lib.mx_gated_mlp(_ptr(x), m, d, ff, _ptr(wgu.codes), _ptr(wgu.scales), _ptr(bgu), _ptr(w2.codes),
+                          _ptr(w2.scales), _ptr(b2), _ptr(y), _ptr(workspace), workspace.numel(),
+                          _stream_handle(stream))
+    _check(st, "mx_gated_mlp")
+    return y
+
+
+def mx_dit_mlp_block(x, shift, scale, gate, w_up: MxTensor, b_up, w2: MxTensor, b2, eps: float = 1e-6,
+                     activation: int = MX_ACT_GELU_TANH, y=None, workspace=None, stream=None):
+    """y = x + gate * MLP(MXFP6(rmsnorm(x) * (1 + scale) + shift)); y may be x (in place)."""
+    torch = _torch()
+    lib = load()
+    m, d = x.shape
+    ff = w2.k
+    rows_up = 2 * ff if activation == MX_ACT_SWIGLU else ff
+    if w_up.k != d or w_up.rows != rows_up or w2.rows != d:
+        raise ValueError("weight shapes do not match x")
+    if y is None:
+        y = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
+    need = lib.mx_mlp_workspace_bytes(m, d, ff)
+    if workspace is None:
+        workspace = _empty_u8(max(need, 256), x.device)
+    st = lib.mx_dit_mlp_block(_ptr(x), m, d, ff, _ptr(shift), _ptr(scale), _ptr(gate), float(eps), int(activation),
+                              _ptr(w_up.codes), _ptr(w_up.scales), _ptr(b_up), _ptr(w2.codes), _ptr(w2.scales),
+                              _ptr(b2), _ptr(y), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st, "mx_dit_mlp_block")
     return y
 
 

@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG_DIR, "_lib")
 LIB_NAME = "libmxfp6.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "mlp_noalloc.cu"]
+SOURCES = ["api.cu", "quantize.cu", "norm_quantize.cu", "gemm.cu", "mlp_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -56,10 +56,30 @@ mx_status check_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, c
   return MX_OK;
 }
 
+mx_status check_norm_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, const void* shift,
+                              const void* scale, float eps, const void* codes, const void* scales, const float* dbg) {
+  if (!(eps >= 0.0f) || eps > 3.0e38f) return MX_ERR_INVALID_ARG;   // negative, NaN or infinite
+  mx_status st = check_quantize(x, rows, K, ld_x, codes, scales);
+  if (st != MX_OK) return st;
+  if (K > mxk::norm_quantize_max_k()) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return MX_OK;
+  if ((shift != nullptr && !aligned(shift, 16)) || (scale != nullptr && !aligned(scale, 16)) ||
+      (dbg != nullptr && !aligned(dbg, 16)))
+    return MX_ERR_MISALIGNED;
+  return MX_OK;
+}
+
+// epi: an mx_epilogue value, or kEpiGateResidual for mx_gemm_gate_residual.
+constexpr int kEpiGateResidual = 3;
+
+bool mxfp6_out(int epi) { return epi == MX_EPI_BIAS_GELU_MXFP6 || epi == MX_EPI_BIAS_SWIGLU_MXFP6; }
+
 mx_status check_gemm(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
                      const void* bias, int64_t M, int64_t N, int64_t K, int epi, const void* out,
                      const void* out_scales, const float* dbg) {
-  if (epi != MX_EPI_BIAS_BF16 && epi != MX_EPI_BIAS_GELU_MXFP6) return MX_ERR_INVALID_ARG;
+  if (epi != MX_EPI_BIAS_BF16 && epi != MX_EPI_BIAS_GELU_MXFP6 && epi != MX_EPI_BIAS_SWIGLU_MXFP6 &&
+      epi != kEpiGateResidual)
+    return MX_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return MX_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N % 256 != 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return MX_ERR_UNSUPPORTED_SHAPE;
@@ -67,14 +87,13 @@ mx_status check_gemm(const void* a_codes, const void* a_scales, const void* b_co
   if (M == 0 || N == 0) return MX_OK;
   if (a_codes == nullptr || a_scales == nullptr || b_codes == nullptr || b_scales == nullptr || out == nullptr)
     return MX_ERR_INVALID_ARG;
-  if (epi == MX_EPI_BIAS_GELU_MXFP6 && out_scales == nullptr) return MX_ERR_INVALID_ARG;
+  if (mxfp6_out(epi) && out_scales == nullptr) return MX_ERR_INVALID_ARG;
   if (!aligned(a_codes, 32) || !aligned(b_codes, 32) || !aligned(a_scales, 16) || !aligned(b_scales, 16))
     return MX_ERR_MISALIGNED;
   if (bias != nullptr && !aligned(bias, 16)) return MX_ERR_MISALIGNED;
-  if (epi == MX_EPI_BIAS_BF16 && !aligned(out, 16)) return MX_ERR_MISALIGNED;
-  if (epi == MX_EPI_BIAS_GELU_MXFP6 && (!aligned(out, 32) || !aligned(out_scales, 16)))
-    return MX_ERR_MISALIGNED;
-  if (epi == MX_EPI_BIAS_GELU_MXFP6 && dbg != nullptr && !aligned(dbg, 16)) return MX_ERR_MISALIGNED;
+  if (!mxfp6_out(epi) && !aligned(out, 16)) return MX_ERR_MISALIGNED;
+  if (mxfp6_out(epi) && (!aligned(out, 32) || !aligned(out_scales, 16))) return MX_ERR_MISALIGNED;
+  if (mxfp6_out(epi) && dbg != nullptr && !aligned(dbg, 16)) return MX_ERR_MISALIGNED;
   return MX_OK;
 }
 
@@ -94,7 +113,8 @@ MlpLayout mlp_layout(int64_t M, int64_t d, int64_t ff) {
 
 mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
                       const void* bias, int64_t M, int64_t N, int64_t K, int epi, void* out, void* out_scales,
-                      float* dbg, int num_sms, cudaStream_t stream) {
+                      float* dbg, int num_sms, cudaStream_t stream, const void* gate = nullptr,
+                      const void* residual = nullptr) {
   if (M == 0 || N == 0) return MX_OK;
   mxk::GemmArgs a;
   a.a_codes = a_codes;
@@ -102,9 +122,11 @@ mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_c
   a.b_codes = b_codes;
   a.b_scales = b_scales;
   a.bias = bias;
+  a.gate = gate;
+  a.residual = residual;
   a.out = out;
   a.out_scales = out_scales;
-  a.debug_prequant = (epi == MX_EPI_BIAS_GELU_MXFP6) ? dbg : nullptr;
+  a.debug_prequant = mxfp6_out(epi) ? dbg : nullptr;
   a.m = M;
   a.n = N;
   a.k = K;
@@ -113,6 +135,88 @@ mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_c
   cudaError_t e = mxk::launch_gemm(a, num_sms, stream, &encode_failed);
   if (encode_failed) return MX_ERR_CUDA;
   return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+// K1 -> up-projection (GELU, or SwiGLU on the stacked gate/up weight) -> K2.
+mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, const void* w_up_codes,
+                   const void* w_up_scales, const void* b_up, const void* w2_codes, const void* w2_scales,
+                   const void* b2, void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (M < 0 || d < 0 || ff < 0) return MX_ERR_INVALID_ARG;
+  const int64_t n_up = up_epi == MX_EPI_BIAS_SWIGLU_MXFP6 ? 2 * ff : ff;
+  if (d == 0 || ff == 0 || d % 256 != 0 || ff % 128 != 0 || n_up % 256 != 0 || M > kMaxDim || d > kMaxDim ||
+      n_up > kMaxDim)
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MX_OK;
+  if (x == nullptr || w_up_codes == nullptr || w_up_scales == nullptr || w2_codes == nullptr ||
+      w2_scales == nullptr || y == nullptr || workspace == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
+  const MlpLayout l = mlp_layout(M, d, ff);
+  if (workspace_bytes < l.total) return MX_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* xq = ws + l.xq;
+  void* xs = ws + l.xs;
+  void* hq = ws + l.hq;
+  void* hs = ws + l.hs;
+  mx_status st = check_quantize(x, M, d, d, xq, xs);
+  if (st != MX_OK) return st;
+  st = check_gemm(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr);
+  if (st != MX_OK) return st;
+  st = check_gemm(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr);
+  if (st != MX_OK) return st;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  if (mxk::launch_quantize_bf16(x, M, d, d, xq, xs, sms, stream) != cudaSuccess) return MX_ERR_CUDA;
+  st = gemm_launch(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr, sms, stream);
+  if (st != MX_OK) return st;
+  return gemm_launch(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr, sms,
+                     stream);
+}
+
+// The MLP half of a DiT block: fused norm quantizer -> up-projection -> down-projection
+// with gate and residual (the residual is x itself).
+mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const void* shift, const void* scale,
+                         const void* gate, float eps, int activation, const void* w_up_codes, const void* w_up_scales,
+                         const void* b_up, const void* w2_codes, const void* w2_scales, const void* b2, void* y,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (M < 0 || d < 0 || ff < 0) return MX_ERR_INVALID_ARG;
+  if (activation != MX_ACT_GELU_TANH && activation != MX_ACT_SWIGLU) return MX_ERR_INVALID_ARG;
+  const int up_epi = activation == MX_ACT_SWIGLU ? MX_EPI_BIAS_SWIGLU_MXFP6 : MX_EPI_BIAS_GELU_MXFP6;
+  const int64_t n_up = activation == MX_ACT_SWIGLU ? 2 * ff : ff;
+  if (d == 0 || ff == 0 || d % 256 != 0 || ff % 128 != 0 || n_up % 256 != 0 || M > kMaxDim || d > kMaxDim ||
+      n_up > kMaxDim)
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MX_OK;
+  if (x == nullptr || w_up_codes == nullptr || w_up_scales == nullptr || w2_codes == nullptr ||
+      w2_scales == nullptr || y == nullptr || workspace == nullptr)
+    return MX_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
+  const MlpLayout l = mlp_layout(M, d, ff);
+  if (workspace_bytes < l.total) return MX_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* xq = ws + l.xq;
+  void* xs = ws + l.xs;
+  void* hq = ws + l.hq;
+  void* hs = ws + l.hs;
+  mx_status st = check_norm_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr);
+  if (st != MX_OK) return st;
+  st = check_gemm(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr);
+  if (st != MX_OK) return st;
+  st = check_gemm(hq, hs, w2_codes, w2_scales, b2, M, d, ff, kEpiGateResidual, y, nullptr, nullptr);
+  if (st != MX_OK) return st;
+  if (gate != nullptr && !aligned(gate, 16)) return MX_ERR_MISALIGNED;
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), y0 = reinterpret_cast<uintptr_t>(y);
+  const uintptr_t bytes = static_cast<uintptr_t>(M) * static_cast<uintptr_t>(d) * 2u;
+  if (x0 != y0 && x0 < y0 + bytes && y0 < x0 + bytes) return MX_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  if (mxk::launch_norm_modulate_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr, sms, stream) !=
+      cudaSuccess)
+    return MX_ERR_CUDA;
+  st = gemm_launch(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr, sms, stream);
+  if (st != MX_OK) return st;
+  return gemm_launch(hq, hs, w2_codes, w2_scales, b2, M, d, ff, kEpiGateResidual, y, nullptr, nullptr, sms, stream,
+                     gate, x);
 }
 
 }  // namespace
@@ -139,9 +243,23 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, void
                                                                                                 : MX_ERR_CUDA;
 }
 
+mx_status mx_quantize_rmsnorm_modulate(const void* x, int64_t rows, int64_t K, int64_t ld_x, const void* shift,
+                                       const void* scale, float eps, void* codes, void* scales, float* debug_y,
+                                       cudaStream_t stream) {
+  mx_status st = check_norm_quantize(x, rows, K, ld_x, shift, scale, eps, codes, scales, debug_y);
+  if (st != MX_OK || rows == 0) return st;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  return mxk::launch_norm_modulate_quantize(x, rows, K, ld_x, shift, scale, eps, codes, scales, debug_y, sms,
+                                            stream) == cudaSuccess
+             ? MX_OK
+             : MX_ERR_CUDA;
+}
+
 mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
                   const void* bias, int64_t M, int64_t N, int64_t K, mx_epilogue epi, void* out,
                   void* out_scales, float* debug_prequant, cudaStream_t stream) {
+  if (static_cast<int>(epi) == kEpiGateResidual) return MX_ERR_INVALID_ARG;  // needs mx_gemm_gate_residual
   mx_status st = check_gemm(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, static_cast<int>(epi), out,
                             out_scales, debug_prequant);
   if (st != MX_OK || M == 0 || N == 0) return st;
@@ -149,6 +267,24 @@ mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes
   if ((st = device_check(&sms)) != MX_OK) return st;
   return gemm_launch(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, static_cast<int>(epi), out, out_scales,
                      debug_prequant, sms, stream);
+}
+
+mx_status mx_gemm_gate_residual(const void* a_codes, const void* a_scales, const void* b_codes,
+                                const void* b_scales, const void* bias, const void* gate, const void* residual,
+                                int64_t M, int64_t N, int64_t K, void* out, cudaStream_t stream) {
+  mx_status st = check_gemm(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, kEpiGateResidual, out, nullptr,
+                            nullptr);
+  if (st != MX_OK || M == 0 || N == 0) return st;
+  if (residual == nullptr) return MX_ERR_INVALID_ARG;
+  if (!aligned(residual, 16) || (gate != nullptr && !aligned(gate, 16))) return MX_ERR_MISALIGNED;
+  // the residual may be the output itself (in-place update), but not overlap it otherwise
+  const uintptr_t r0 = reinterpret_cast<uintptr_t>(residual), o0 = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t bytes = static_cast<uintptr_t>(M) * static_cast<uintptr_t>(N) * 2u;
+  if (r0 != o0 && r0 < o0 + bytes && o0 < r0 + bytes) return MX_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  return gemm_launch(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, kEpiGateResidual, out, nullptr, nullptr,
+                     sms, stream, gate, residual);
 }
 
 size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff) {
@@ -159,35 +295,23 @@ size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff) {
 mx_status mx_mlp(const void* x, int64_t M, int64_t d, int64_t ff, const void* w1_codes, const void* w1_scales,
                  const void* b1, const void* w2_codes, const void* w2_scales, const void* b2, void* y,
                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (M < 0 || d < 0 || ff < 0) return MX_ERR_INVALID_ARG;
-  if (d == 0 || ff == 0 || d % 256 != 0 || ff % 256 != 0 || M > kMaxDim || d > kMaxDim || ff > kMaxDim)
-    return MX_ERR_UNSUPPORTED_SHAPE;
-  if (M == 0) return MX_OK;
-  if (x == nullptr || w1_codes == nullptr || w1_scales == nullptr || w2_codes == nullptr ||
-      w2_scales == nullptr || y == nullptr || workspace == nullptr)
-    return MX_ERR_INVALID_ARG;
-  if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
-  const MlpLayout l = mlp_layout(M, d, ff);
-  if (workspace_bytes < l.total) return MX_ERR_WORKSPACE_TOO_SMALL;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* xq = ws + l.xq;
-  void* xs = ws + l.xs;
-  void* hq = ws + l.hq;
-  void* hs = ws + l.hs;
-  mx_status st = check_quantize(x, M, d, d, xq, xs);
-  if (st != MX_OK) return st;
-  st = check_gemm(xq, xs, w1_codes, w1_scales, b1, M, ff, d, MX_EPI_BIAS_GELU_MXFP6, hq, hs, nullptr);
-  if (st != MX_OK) return st;
-  st = check_gemm(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr);
-  if (st != MX_OK) return st;
-  int sms = 0;
-  if ((st = device_check(&sms)) != MX_OK) return st;
-  if (mxk::launch_quantize_bf16(x, M, d, d, xq, xs, sms, stream) != cudaSuccess) return MX_ERR_CUDA;
-  st = gemm_launch(xq, xs, w1_codes, w1_scales, b1, M, ff, d, MX_EPI_BIAS_GELU_MXFP6, hq, hs, nullptr, sms,
-                   stream);
-  if (st != MX_OK) return st;
-  return gemm_launch(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr, sms,
-                     stream);
+  return mlp_impl(x, M, d, ff, MX_EPI_BIAS_GELU_MXFP6, w1_codes, w1_scales, b1, w2_codes, w2_scales, b2, y,
+                  workspace, workspace_bytes, stream);
+}
+
+mx_status mx_gated_mlp(const void* x, int64_t M, int64_t d, int64_t ff, const void* wgu_codes,
+                       const void* wgu_scales, const void* bgu, const void* w2_codes, const void* w2_scales,
+                       const void* b2, void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return mlp_impl(x, M, d, ff, MX_EPI_BIAS_SWIGLU_MXFP6, wgu_codes, wgu_scales, bgu, w2_codes, w2_scales, b2, y,
+                  workspace, workspace_bytes, stream);
+}
+
+mx_status mx_dit_mlp_block(const void* x, int64_t M, int64_t d, int64_t ff, const void* shift, const void* scale,
+                           const void* gate, float eps, mx_activation activation, const void* w_up_codes,
+                           const void* w_up_scales, const void* b_up, const void* w2_codes, const void* w2_scales,
+                           const void* b2, void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return dit_block_impl(x, M, d, ff, shift, scale, gate, eps, static_cast<int>(activation), w_up_codes, w_up_scales,
+                        b_up, w2_codes, w2_scales, b2, y, workspace, workspace_bytes, stream);
 }
 
 const char* mx_status_string(mx_status status) {

@@ -27,8 +27,16 @@
 //               signals the MMA warp, so no MMA queues behind a copy.
 //   warps 2-9   epilogue (each CTA): drain 32 rows x 128 columns of the local
 //               accumulator into registers, release tensor memory to the leader at
-//               once, then bias + BF16 store (K2) or bias + tanh-GELU + MXFP6
-//               requantization (K3).
+//               once, then one of the fused epilogues:
+//                 kEpiBf16      bias + BF16 store (the down-projection, K2)
+//                 kEpiGelu      bias + tanh-GELU + MXFP6 requantization (K3)
+//                 kEpiSwiglu    stacked gate/up weight: CTA 0 of the pair stages gate
+//                               rows, CTA 1 the matching up rows, so accumulator
+//                               columns c and 128 + c are gate and up of one output
+//                               column; bias + silu(gate) * up + MXFP6 requantization
+//                 kEpiGateRes   bias, times a per-column gate, plus a BF16 residual,
+//                               BF16 store (an output projection with its gate and
+//                               residual add)
 // Every wait is bounded (2 s on the global timer); on expiry the kernel records an
 // error bit, drains its in-flight copies and MMAs (again bounded), frees tensor
 // memory and returns.
@@ -42,11 +50,14 @@
 
 #include "internal.h"
 #include "mx_layout.cuh"
+#include "mx_quant.cuh"
 #include "ptx.cuh"
 
 namespace mxk {
 
 __device__ unsigned int g_error_word;
+
+enum : int { kEpiBf16 = 0, kEpiGelu = 1, kEpiSwiglu = 2, kEpiGateRes = 3 };
 
 constexpr int BM = 128;
 constexpr int BN = 256;
@@ -84,9 +95,11 @@ struct __align__(1024) SharedStorage {
   uint32_t tmem_base;
   int abort_flag;
   alignas(16) float bias_s[kEpiWarps][kEpiCols];   // each epilogue warp's bias values (read as float4)
+  alignas(16) float gate_s[kEpiWarps][kEpiCols];   // kEpiGateRes: each epilogue warp's gate values
 };
 constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;
-static_assert(offsetof(SharedStorage, bias_s) % 16 == 0, "bias staging is read as float4");
+static_assert(offsetof(SharedStorage, bias_s) % 16 == 0 && offsetof(SharedStorage, gate_s) % 16 == 0,
+              "bias and gate staging are read as float4");
 static_assert(offsetof(SharedStorage, sfa) % 128 == 0 && offsetof(SharedStorage, sfb) % 128 == 0,
               "scale atoms are TMA destinations");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -174,9 +187,13 @@ __device__ __forceinline__ void pair_tile(const TileWalk& w, int p, int* mb, int
   *mb = pm * kPair + w.rank;
 }
 
+// gated: B is the stacked [gate; up] weight of 2 * n_out rows; CTA 0 of the pair
+// stages gate rows [128 nb, 128 nb + 128) and CTA 1 the up rows n_out rows further,
+// and both SMs' tensor memory gets the scale atoms of both row groups.
 __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap* ta, const CUtensorMap* tb,
                                              const CUtensorMap* tsa, const CUtensorMap* tsb, const TileWalk& w,
-                                             int num_m, int kblocks, volatile int* abort_flag) {
+                                             int num_m, int kblocks, bool gated, int n_out,
+                                             volatile int* abort_flag) {
   int stage = 0;
   uint32_t phase = 0;
   uint32_t filled = 0, fill_parity = 0;
@@ -194,9 +211,15 @@ __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap
       const uint32_t full_leader = mapa_shared(smem_u32(&s.full[stage]), 0);
       if (w.rank == 0) mbar_arrive_expect_tx(&s.full[stage], kPair * kStageTx);
       tma_load_2d_pair(s.a[stage], ta, full_leader, kb * BK, mb * BM);
-      tma_load_2d_pair(s.b[stage], tb, full_leader, kb * BK, nb * BN + w.rank * kBHalfRows);
+      const int b_row = gated ? w.rank * n_out + nb * kBHalfRows : nb * BN + w.rank * kBHalfRows;
+      tma_load_2d_pair(s.b[stage], tb, full_leader, kb * BK, b_row);
       tma_load_2d_pair(s.sfa[stage], tsa, full_leader, 0, mb * kblocks + kb);
-      tma_load_3d_pair(s.sfb[stage], tsb, full_leader, 0, kb, 2 * nb);
+      if (gated) {
+        tma_load_3d_pair(s.sfb[stage], tsb, full_leader, 0, kb, nb);
+        tma_load_3d_pair(s.sfb[stage] + kAtomBytes, tsb, full_leader, 0, kb, n_out / kBHalfRows + nb);
+      } else {
+        tma_load_3d_pair(s.sfb[stage], tsb, full_leader, 0, kb, 2 * nb);
+      }
       filled |= 1u << stage;
       fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == kStages) {
@@ -289,42 +312,30 @@ __device__ __forceinline__ void run_scales(SharedStorage& s, uint32_t tmem, cons
   }
 }
 
-// One epilogue warp stages the fp32 bias of its kEpiCols columns in shared memory
-// (lane i converts kEpiCols/32 consecutive columns); chunks then read broadcasts.
-__device__ __forceinline__ void stage_bias(float* bw, const uint16_t* __restrict__ bias, int n0, int lane) {
-  constexpr int kPer = kEpiCols / 32;
-  float f[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) f[i] = 0.f;
-  if (bias != nullptr) {
-    if constexpr (kPer == 4) {
-      const uint2 w = __ldg(reinterpret_cast<const uint2*>(bias + n0 + 4 * lane));
-      f[0] = __uint_as_float(w.x << 16);
-      f[1] = __uint_as_float(w.x & 0xFFFF0000u);
-      f[2] = __uint_as_float(w.y << 16);
-      f[3] = __uint_as_float(w.y & 0xFFFF0000u);
-    } else {
-      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(bias + n0 + 2 * lane));
-      f[0] = __uint_as_float(w << 16);
-      f[1] = __uint_as_float(w & 0xFFFF0000u);
-    }
+// One epilogue warp stages kEpiCols fp32 values of a BF16 vector in shared memory:
+// lanes 0-15 convert 4 consecutive values each from src[n_lo ...], lanes 16-31 from
+// src[n_hi ...] (n_hi = n_lo + 64 for a contiguous range); a null src stages `fill`.
+// Chunks then read them as broadcasts.
+__device__ __forceinline__ void stage_vec(float* bw, const uint16_t* __restrict__ src, int n_lo, int n_hi, int lane,
+                                          float fill) {
+  static_assert(kEpiCols == 128, "two halves of 64 values, 4 per lane");
+  float f[4] = {fill, fill, fill, fill};
+  if (src != nullptr) {
+    const int n = (lane < 16 ? n_lo : n_hi) + 4 * (lane & 15);
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src + n));
+    f[0] = __uint_as_float(w.x << 16);
+    f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(w.y << 16);
+    f[3] = __uint_as_float(w.y & 0xFFFF0000u);
   }
   __syncwarp();  // the previous tile's reads are done
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) bw[kPer * lane + i] = f[i];
+  *reinterpret_cast<float4*>(bw + 4 * lane) = make_float4(f[0], f[1], f[2], f[3]);
   __syncwarp();
 }
 
-__device__ __forceinline__ void read_bias32(const float* bw, int c, float (&b)[32]) {
-  const float4* p = reinterpret_cast<const float4*>(bw + 32 * c);
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    const float4 f = p[v];
-    b[4 * v] = f.x;
-    b[4 * v + 1] = f.y;
-    b[4 * v + 2] = f.z;
-    b[4 * v + 3] = f.w;
-  }
+// Values 4 v .. 4 v + 3 of staged chunk c (32 values per chunk).
+__device__ __forceinline__ float4 staged4(const float* bw, int c, int v) {
+  return reinterpret_cast<const float4*>(bw + 32 * c)[v];
 }
 
 // With u = sqrt(2/pi) (v + 0.044715 v^3), exp(-2u) = 2^t for
@@ -339,31 +350,70 @@ __device__ __forceinline__ float gelu_tanh(float v) {
   return v * rcp_approx(1.0f + ex2_approx(t));
 }
 
+// silu(v) = v / (1 + e^-v) = v / (1 + 2^(-v log2 e)). For very negative v, 2^.. is
+// +inf and the result is v * 0 = -0 (the exact value is below 1e-37 in magnitude).
+constexpr float kNegLog2e = -1.4426950408889634f;
+
+__device__ __forceinline__ float silu(float v) { return v * rcp_approx(1.0f + ex2_approx(v * kNegLog2e)); }
+
+__device__ __forceinline__ void store_block_codes(uint8_t* dst_bytes, const uint32_t (&w)[6]) {
+  uint2* dst = reinterpret_cast<uint2*>(dst_bytes);
+  dst[0] = make_uint2(w[0], w[1]);
+  dst[1] = make_uint2(w[2], w[3]);
+  dst[2] = make_uint2(w[4], w[5]);
+}
+
+__device__ __forceinline__ void store_dbg32(float* d, const float (&g)[32]) {
+  float4* p = reinterpret_cast<float4*>(d);
+#pragma unroll
+  for (int v = 0; v < 8; ++v) p[v] = make_float4(g[4 * v], g[4 * v + 1], g[4 * v + 2], g[4 * v + 3]);
+}
+
+// Accumulator column (inside the 256-column tile) of epilogue chunk c of column group h.
+// kEpiSwiglu: chunks 0, 1 are gate columns 64 h + 32 c, chunks 2, 3 the up columns 128 further.
+template <int EPI>
+__device__ __forceinline__ uint32_t chunk_col(int h, int c) {
+  if constexpr (EPI == kEpiSwiglu)
+    return static_cast<uint32_t>((c >> 1) * kBHalfRows + 64 * h + 32 * (c & 1));
+  else
+    return static_cast<uint32_t>(h * kEpiCols + 32 * c);
+}
+
+// n_total: the GEMM's N (rows of B; stacked 2 F for kEpiSwiglu). Output width:
+// F = n_total / 2 for kEpiSwiglu, else n_total.
 template <int EPI, bool DBG>
 __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, const TileWalk& wk,
                                              int num_m, int m_total, int n_total,
-                                             const uint16_t* __restrict__ bias, void* __restrict__ out,
-                                             uint8_t* __restrict__ out_scales, float* __restrict__ dbg,
-                                             volatile int* abort_flag) {
+                                             const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate,
+                                             const uint16_t* residual, void* out, uint8_t* __restrict__ out_scales,
+                                             float* __restrict__ dbg, volatile int* abort_flag) {
   const int q = warp & 3;           // tensor-memory lane quadrant this warp may access
-  const int h = (warp - 2) >> 2;    // column group (kEpiCols wide) of the 256-wide tile
+  const int h = (warp - 2) >> 2;    // column group of the 256-wide tile
+  const int n_out = (EPI == kEpiSwiglu) ? n_total / 2 : n_total;
   uint32_t acc_phase = 0;
   // the accumulator is released to the leader CTA's barrier (both CTAs' warps count)
   const uint32_t tmem_empty_leader = mapa_shared(smem_u32(&s.tmem_empty), 0);
+  float* bw = s.bias_s[warp - 2];
+  float* gw = s.gate_s[warp - 2];
   for (int p = wk.first; p < wk.pairs; p += wk.step) {
     int mb, nb;
     pair_tile(wk, p, &mb, &nb);
-    float* bw = s.bias_s[warp - 2];
-    stage_bias(bw, bias, nb * BN + h * kEpiCols, lane);
+    // first output column of this warp: 64 of them (kEpiSwiglu) or 128
+    const int col0 = (EPI == kEpiSwiglu) ? nb * kBHalfRows + 64 * h : nb * BN + h * kEpiCols;
+    if constexpr (EPI == kEpiSwiglu)
+      stage_vec(bw, bias, col0, n_out + col0, lane, 0.f);
+    else
+      stage_vec(bw, bias, col0, col0 + 64, lane, 0.f);
+    if constexpr (EPI == kEpiGateRes) stage_vec(gw, gate, col0, col0 + 64, lane, 1.f);
     int ok = 0;
     if (lane == 0) ok = wait_bounded(&s.tmem_full, acc_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     tc_fence_after();
     uint32_t r[kEpiChunks][32];
-    const uint32_t t0 = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * kEpiCols);
+    const uint32_t t0 = tmem + (static_cast<uint32_t>(32 * q) << 16);
 #pragma unroll
-    for (int c = 0; c < kEpiChunks; ++c) tc_ld_32x32b_x32(t0 + 32u * c, r[c]);
+    for (int c = 0; c < kEpiChunks; ++c) tc_ld_32x32b_x32(t0 + chunk_col<EPI>(h, c), r[c]);
     tc_wait_ld();
     tc_fence_before();
     __syncwarp();
@@ -374,85 +424,91 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
     acc_phase ^= 1u;
 
     const int64_t row = static_cast<int64_t>(mb) * BM + 32 * q + lane;
-        const bool live = row < m_total;
-    const int col0 = nb * BN + h * kEpiCols;
-    if constexpr (EPI == 0) {
+    const bool live = row < m_total;
+    if constexpr (EPI == kEpiBf16 || EPI == kEpiGateRes) {
       uint16_t* y = static_cast<uint16_t*>(out);
 #pragma unroll
       for (int c = 0; c < kEpiChunks; ++c) {
         const int n = col0 + 32 * c;
-        float b[32];
-        read_bias32(bw, c, b);
+        uint32_t rw[16];  // kEpiGateRes: the residual's 32 BF16 values, two per word
+        if constexpr (EPI == kEpiGateRes) {
+          uint4 res[4] = {};
+          if (live) {
+            const uint4* src = reinterpret_cast<const uint4*>(residual + row * n_total + n);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) res[j] = __ldg(src + j);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            rw[4 * j] = res[j].x;
+            rw[4 * j + 1] = res[j].y;
+            rw[4 * j + 2] = res[j].z;
+            rw[4 * j + 3] = res[j].w;
+          }
+        }
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = cvt_bf16x2(__uint_as_float(r[c][2 * i + 1]) + b[2 * i + 1],
-                             __uint_as_float(r[c][2 * i]) + b[2 * i]);
+        for (int v = 0; v < 8; ++v) {
+          const float4 b4 = staged4(bw, c, v);
+          float x0 = __uint_as_float(r[c][4 * v]) + b4.x;
+          float x1 = __uint_as_float(r[c][4 * v + 1]) + b4.y;
+          float x2 = __uint_as_float(r[c][4 * v + 2]) + b4.z;
+          float x3 = __uint_as_float(r[c][4 * v + 3]) + b4.w;
+          if constexpr (EPI == kEpiGateRes) {
+            const float4 g4 = staged4(gw, c, v);
+            x0 = fmaf(g4.x, x0, __uint_as_float(rw[2 * v] << 16));
+            x1 = fmaf(g4.y, x1, __uint_as_float(rw[2 * v] & 0xFFFF0000u));
+            x2 = fmaf(g4.z, x2, __uint_as_float(rw[2 * v + 1] << 16));
+            x3 = fmaf(g4.w, x3, __uint_as_float(rw[2 * v + 1] & 0xFFFF0000u));
+          }
+          pk[2 * v] = cvt_bf16x2(x1, x0);
+          pk[2 * v + 1] = cvt_bf16x2(x3, x2);
+        }
         if (live) {
           uint4* dst = reinterpret_cast<uint4*>(y + row * n_total + n);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
     } else {
+      // MXFP6 requantization along the output columns, one 32-column block at a time
+      constexpr int kBlocks = (EPI == kEpiSwiglu) ? kEpiChunks / 2 : kEpiChunks;
       uint8_t* codes = static_cast<uint8_t*>(out);
       uint32_t scale_word = 0;
 #pragma unroll
-      for (int c = 0; c < kEpiChunks; ++c) {
+      for (int c = 0; c < kBlocks; ++c) {
         const int n = col0 + 32 * c;
-        float b[32];
-        read_bias32(bw, c, b);
         float g[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = gelu_tanh(__uint_as_float(r[c][i]) + b[i]);
-        // |g| order = unsigned order of the magnitude bits (NaN/Inf sort last); a tree keeps it shallow
-        uint32_t m[16];
+        for (int v = 0; v < 8; ++v) {
+          const float4 b4 = staged4(bw, c, v);
+          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+          if constexpr (EPI == kEpiGelu) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          m[i] = max(__float_as_uint(g[2 * i]) & 0x7FFFFFFFu, __float_as_uint(g[2 * i + 1]) & 0x7FFFFFFFu);
+            for (int t = 0; t < 4; ++t) g[4 * v + t] = gelu_tanh(__uint_as_float(r[c][4 * v + t]) + bb[t]);
+          } else {
+            const float4 u4 = staged4(bw, 2 + c, v);
+            const float bu[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-        for (int w2 = 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-          for (int i = 0; i < w2; ++i) m[i] = max(m[i], m[i + w2]);
-        const uint32_t amax = m[0];
+            for (int t = 0; t < 4; ++t)
+              g[4 * v + t] = silu(__uint_as_float(r[c][4 * v + t]) + bb[t]) *
+                             (__uint_as_float(r[2 + c][4 * v + t]) + bu[t]);
+          }
+        }
         if constexpr (DBG) {
-          if (live) {
-            float4* d = reinterpret_cast<float4*>(dbg + row * n_total + n);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) d[v] = make_float4(g[4 * v], g[4 * v + 1], g[4 * v + 2], g[4 * v + 3]);
-          }
+          if (live) store_dbg32(dbg + row * n_out + n, g);
         }
-        uint32_t sc;
-        uint32_t w[6] = {0, 0, 0, 0, 0, 0};
-        if (amax >= 0x7F800000u) {  // Inf or NaN: E8M0 NaN, zero codes
-          sc = 0xFFu;
-        } else {
-          const int e = static_cast<int>(amax >> 23);
-          sc = static_cast<uint32_t>(e > 2 ? e - 2 : 0);
-          const float fac = __uint_as_float((254u - sc) << 23);  // 2^-s, exact
-          uint32_t grp[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t lo = cvt_e2m3x2(g[4 * j + 1] * fac, g[4 * j] * fac);
-            const uint32_t hi = cvt_e2m3x2(g[4 * j + 3] * fac, g[4 * j + 2] * fac);
-            grp[j] = pack4(lo | (hi << 16));
-          }
-          pack32(grp, w);
-        }
-        if (live) {
-          uint2* dst = reinterpret_cast<uint2*>(codes + row * (n_total / 4 * 3) + n / 4 * 3);
-          dst[0] = make_uint2(w[0], w[1]);
-          dst[1] = make_uint2(w[2], w[3]);
-          dst[2] = make_uint2(w[4], w[5]);
-        }
+        uint32_t w[6];
+        const uint32_t sc = quant_block32(g, w);
+        if (live) store_block_codes(codes + row * (n_out / 4 * 3) + n / 4 * 3, w);
         scale_word |= sc << (8 * c);
       }
       // padding rows of the last row tile get zero scales; a row tile past the
       // last one (second half of the last pair) has no scale storage at all
       if (!live) scale_word = 0;
       if (mb < num_m) {
-        uint8_t* sw = out_scales + scale_word_offset(row, col0 / kAtomK, n_total) + (col0 % kAtomK) / 32;
-        if constexpr (kEpiChunks == 4)
+        uint8_t* sw = out_scales + scale_word_offset(row, col0 / kAtomK, n_out) + (col0 % kAtomK) / 32;
+        if constexpr (kBlocks == 4)
           *reinterpret_cast<uint32_t*>(sw) = scale_word;
         else
           *reinterpret_cast<uint16_t*>(sw) = static_cast<uint16_t>(scale_word);
@@ -465,8 +521,9 @@ template <int EPI, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sb,
-                   const uint16_t* __restrict__ bias, void* __restrict__ out, uint8_t* __restrict__ out_scales,
-                   float* __restrict__ dbg, int m_total, int n_total, int k_total) {
+                   const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate, const uint16_t* residual,
+                   void* out, uint8_t* __restrict__ out_scales, float* __restrict__ dbg, int m_total, int n_total,
+                   int k_total) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   SharedStorage& s =
@@ -513,14 +570,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &s.abort_flag;
 
   if (warp == 0) {
-    if (lane == 0) run_producer(s, &tmap_a, &tmap_b, &tmap_sa, &tmap_sb, walk, num_m, kblocks, abort_flag);
+    if (lane == 0)
+      run_producer(s, &tmap_a, &tmap_b, &tmap_sa, &tmap_sb, walk, num_m, kblocks, EPI == kEpiSwiglu, n_total / 2,
+                   abort_flag);
   } else if (warp == 1) {
     if (lane == 0 && walk.rank == 0) run_mma(s, tmem, walk, kblocks, abort_flag);
   } else if (warp == 2 + kEpiWarps) {
     if (lane == 0 && walk.rank == 0) run_scales(s, tmem, walk, kblocks, abort_flag);
   } else {
-    run_epilogue<EPI, DBG>(s, tmem, warp, lane, walk, num_m, m_total, n_total, bias, out, out_scales, dbg,
-                           abort_flag);
+    run_epilogue<EPI, DBG>(s, tmem, warp, lane, walk, num_m, m_total, n_total, bias, gate, residual, out,
+                           out_scales, dbg, abort_flag);
   }
   __syncwarp();
   tc_fence_before();
@@ -570,9 +629,10 @@ static bool make_codes_map(CUtensorMap* map, const void* codes, int64_t rows, in
 
 // Tensor maps over the tiled scales, one 512-byte atom = 128 uint32 per box row.
 // A: atoms [row tile][K step] as a 2-D [atoms][128]; box = one atom.
-// B: [row tile][K step][128] as 3-D; box = the two atoms of one 256-row N tile.
+// B: [row tile][K step][128] as 3-D; box = the two atoms of one 256-row N tile, or
+// (stacked gate/up weight) one atom, loaded once for the gate and once for the up rows.
 static bool make_scale_maps(CUtensorMap* sa, CUtensorMap* sb, const void* a_scales, const void* b_scales, int64_t m,
-                            int64_t n, int64_t k) {
+                            int64_t n, int64_t k, uint32_t b_box_groups) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t kblocks = static_cast<cuuint64_t>(k / BK);
@@ -588,7 +648,7 @@ static bool make_scale_maps(CUtensorMap* sa, CUtensorMap* sb, const void* a_scal
   if (r != CUDA_SUCCESS) return false;
   cuuint64_t bdims[3] = {128, kblocks, static_cast<cuuint64_t>(n / 128)};
   cuuint64_t bstr[2] = {kAtomBytes, kblocks * kAtomBytes};
-  cuuint32_t bbox[3] = {128, 1, 2};
+  cuuint32_t bbox[3] = {128, 1, b_box_groups};
   r = fn(sb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(b_scales), bdims, bstr, bbox, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -631,7 +691,8 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   }
   if (clusters > pairs) clusters = static_cast<int>(pairs);
   cfg.gridDim = dim3(kPair * clusters, 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, static_cast<const uint16_t*>(a.bias), a.out,
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, static_cast<const uint16_t*>(a.bias),
+                         static_cast<const uint16_t*>(a.gate), static_cast<const uint16_t*>(a.residual), a.out,
                          static_cast<uint8_t*>(a.out_scales), a.debug_prequant, static_cast<int>(a.m),
                          static_cast<int>(a.n), static_cast<int>(a.k));
   if (e != cudaSuccess) return e;
@@ -643,15 +704,24 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, boo
   CUtensorMap ta, tb, tsa, tsb;
   if (!make_codes_map(&ta, a.a_codes, a.m, a.k, BM) ||
       !make_codes_map(&tb, a.b_codes, a.n, a.k, kBHalfRows) ||
-      !make_scale_maps(&tsa, &tsb, a.a_scales, a.b_scales, a.m, a.n, a.k)) {
+      !make_scale_maps(&tsa, &tsb, a.a_scales, a.b_scales, a.m, a.n, a.k, a.epilogue == kEpiSwiglu ? 1u : 2u)) {
     *encode_failed = true;
     return cudaSuccess;
   }
   (void)num_sms;
   const int64_t pairs = ((a.m + kPair * BM - 1) / (kPair * BM)) * (a.n / BN);
-  if (a.epilogue == 0) return launch_instance<0, false>(ta, tb, tsa, tsb, a, pairs, stream);
-  if (a.debug_prequant != nullptr) return launch_instance<1, true>(ta, tb, tsa, tsb, a, pairs, stream);
-  return launch_instance<1, false>(ta, tb, tsa, tsb, a, pairs, stream);
+  const bool dbg = a.debug_prequant != nullptr;
+  switch (a.epilogue) {
+    case kEpiBf16: return launch_instance<kEpiBf16, false>(ta, tb, tsa, tsb, a, pairs, stream);
+    case kEpiGelu:
+      return dbg ? launch_instance<kEpiGelu, true>(ta, tb, tsa, tsb, a, pairs, stream)
+                 : launch_instance<kEpiGelu, false>(ta, tb, tsa, tsb, a, pairs, stream);
+    case kEpiSwiglu:
+      return dbg ? launch_instance<kEpiSwiglu, true>(ta, tb, tsa, tsb, a, pairs, stream)
+                 : launch_instance<kEpiSwiglu, false>(ta, tb, tsa, tsb, a, pairs, stream);
+    case kEpiGateRes: return launch_instance<kEpiGateRes, false>(ta, tb, tsa, tsb, a, pairs, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // A wait that nothing will ever satisfy: it must give up after the bound, set

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "mx.h")
 
 OK, INVALID, SHAPE, MISALIGNED, WS_SMALL, DEVICE, CUDA = range(7)
-BF16, GELU = 0, 1
+BF16, GELU, SWIGLU = 0, 1, 2
 A32 = 0x10000   # fake, 32-byte aligned device addresses: never dereferenced by validation
 A32b = 0x20000
 A32c = 0x30000
@@ -124,6 +124,39 @@ def test_mlp_rejects_bad_arguments(lib):
     assert call(M=0, x=None, y=None, ws=None) == OK
 
 
+def test_swiglu_gemm_arguments(lib):
+    assert _g(lib, epi=SWIGLU, out_sc=None) == INVALID
+    assert _g(lib, epi=SWIGLU, N=384) == SHAPE         # stacked N = 2F needs N % 256
+    assert _g(lib, epi=SWIGLU, out=A32e + 16) == MISALIGNED
+    assert _g(lib, epi=SWIGLU, dbg=A32 + 4) == MISALIGNED
+    assert _g(lib, epi=3) == INVALID                   # the gate/residual epilogue has its own entry point
+
+
+def _gr(lib, bias=None, gate=None, res=0x200000, M=128, N=512, K=256, out=0x400000):
+    return lib.mx_gemm_gate_residual(A32, A32b, A32c, A32d, bias, gate, res, M, N, K, out, None)
+
+
+def test_gate_residual_rejects_bad_arguments(lib):
+    assert _gr(lib, res=None) == INVALID
+    assert _gr(lib, N=384) == SHAPE
+    assert _gr(lib, gate=A32 + 2) == MISALIGNED
+    assert _gr(lib, res=0x200000 + 8) == MISALIGNED
+    assert _gr(lib, out=0x200000 + 1024) == INVALID    # partial overlap with the residual
+    assert _gr(lib, M=0, res=None, out=None) == OK
+
+
+def test_gated_mlp_rejects_bad_arguments(lib):
+    def call(M=256, d=512, ff=1024, ws=0x100000, wsb=1 << 30, x=A32):
+        return lib.mx_gated_mlp(x, M, d, ff, A32b, A32c, None, A32d, A32e, None, A32, ws, wsb, None)
+
+    assert call(M=-1) == INVALID
+    assert call(d=384) == SHAPE
+    assert call(ff=192) == SHAPE                       # ff % 128
+    assert call(x=None) == INVALID
+    assert call(wsb=lib.mx_mlp_workspace_bytes(256, 512, 1024) - 1) == WS_SMALL
+    assert call(M=0, x=None) == OK
+
+
 def test_valid_call_without_gpu_fails_loudly(lib):
     """A well-formed call must reach the device check and fail there: no CPU fallback."""
     import torch
@@ -132,6 +165,8 @@ def test_valid_call_without_gpu_fails_loudly(lib):
         pytest.skip("a GPU is present")
     assert _q(lib) in (CUDA, DEVICE)
     assert _g(lib) in (CUDA, DEVICE)
+    assert _g(lib, epi=SWIGLU) in (CUDA, DEVICE)
+    assert _gr(lib) in (CUDA, DEVICE)
 
 
 def test_host_scale_layout_matches_oracle(mx):
