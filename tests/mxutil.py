@@ -14,6 +14,7 @@ import oracle as O
 
 REL_TOL = 2.0 ** -7
 RMS_TOL = 1e-3
+SILU_LIP = 1.1      # max |silu'(v)| is 1.0998
 
 
 def bf16_to_device(bits: np.ndarray):
@@ -106,3 +107,18 @@ def assert_codes_equal(gpu_codes, ref_codes, gpu_scales, ref_scales, what=""):
         raise AssertionError(f"{what}: {int((gc != rc).sum())} codes differ, first at {idx.tolist()}: "
                              f"gpu {[hex(v) for v in gc[tuple(idx.T)].tolist()]} "
                              f"oracle {[hex(v) for v in rc[tuple(idx.T)].tolist()]}")
+
+
+def assert_swiglu_close(h_gpu, c_ref, what):
+    """h_gpu [M][F] against the oracle's stacked accumulators c_ref [M][2F] (bias included)."""
+    f = c_ref.shape[1] // 2
+    g, u = c_ref[:, :f], c_ref[:, f:]
+    tg = REL_TOL * np.abs(g) + RMS_TOL * np.sqrt(np.mean(g * g))
+    tu = REL_TOL * np.abs(u) + RMS_TOL * np.sqrt(np.mean(u * u))
+    ref = O.silu(g) * u
+    bound = SILU_LIP * tg * (np.abs(u) + tu) + np.abs(O.silu(g)) * tu + 1e-6 * np.abs(ref) + 1e-30
+    err = np.abs(np.asarray(h_gpu, np.float64) - ref)
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, (f"{what}: {len(bad)} of {err.size} outside, first {bad[:4].tolist()}, "
+                           f"worst ratio {float((err / bound).max()):.3g}")
+    return float((err / bound).max())

@@ -157,6 +157,40 @@ def test_gated_mlp_rejects_bad_arguments(lib):
     assert call(M=0, x=None) == OK
 
 
+def _nq(lib, x=A32, rows=128, k=256, ld=256, shift=None, scale=None, eps=1e-6, codes=A32b, scales=A32c, dbg=None):
+    return lib.mx_quantize_rmsnorm_modulate(x, rows, k, ld, shift, scale, eps, codes, scales, dbg, None)
+
+
+def test_norm_quantize_rejects_bad_arguments(lib):
+    assert _nq(lib, eps=-1.0) == INVALID
+    assert _nq(lib, eps=float("nan")) == INVALID
+    assert _nq(lib, eps=float("inf")) == INVALID
+    assert _nq(lib, k=8320, ld=8320) == SHAPE          # above the 8192 columns one CTA holds
+    assert _nq(lib, k=100, ld=100) == SHAPE
+    assert _nq(lib, shift=A32 + 8) == MISALIGNED
+    assert _nq(lib, scale=A32 + 2) == MISALIGNED
+    assert _nq(lib, dbg=A32 + 4) == MISALIGNED
+    assert _nq(lib, x=None) == INVALID
+    assert _nq(lib, rows=0, x=None, codes=None, scales=None) == OK
+
+
+def test_dit_block_rejects_bad_arguments(lib):
+    def call(M=256, d=512, ff=1024, act=0, x=A32, y=0x800000, ws=0x100000, wsb=1 << 30, eps=1e-6, gate=None):
+        return lib.mx_dit_mlp_block(x, M, d, ff, None, None, gate, eps, act, A32b, A32c, None, A32d, A32e, None, y,
+                                    ws, wsb, None)
+
+    assert call(act=2) == INVALID
+    assert call(M=-1) == INVALID
+    assert call(d=384) == SHAPE
+    assert call(ff=384, act=0) == SHAPE                # GELU: ff is N of the up-projection
+    assert call(d=8448) == SHAPE                       # fused quantizer holds at most 8192 columns
+    assert call(eps=-1.0) == INVALID
+    assert call(y=A32 + 512) == INVALID                # partial overlap of y and x
+    assert call(gate=A32 + 2) == MISALIGNED
+    assert call(wsb=lib.mx_mlp_workspace_bytes(256, 512, 1024) - 1) == WS_SMALL
+    assert call(M=0, x=None, y=None) == OK
+
+
 def test_valid_call_without_gpu_fails_loudly(lib):
     """A well-formed call must reach the device check and fail there: no CPU fallback."""
     import torch
@@ -167,6 +201,7 @@ def test_valid_call_without_gpu_fails_loudly(lib):
     assert _g(lib) in (CUDA, DEVICE)
     assert _g(lib, epi=SWIGLU) in (CUDA, DEVICE)
     assert _gr(lib) in (CUDA, DEVICE)
+    assert _nq(lib) in (CUDA, DEVICE)
 
 
 def test_host_scale_layout_matches_oracle(mx):

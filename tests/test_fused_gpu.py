@@ -22,34 +22,16 @@ import pytest
 
 import oracle as O
 import synth
-from mxutil import (REL_TOL, RMS_TOL, assert_codes_equal, assert_gemm_close, bf16_from_device, bf16_to_device,
-                    f32_from_bf16_bits, gemm_tolerance_report, mx_rows_to_host, mx_to_host, mx_upload,
-                    sample_rows)
+from mxutil import (REL_TOL, RMS_TOL, assert_codes_equal, assert_gemm_close, assert_swiglu_close,
+                    bf16_from_device, bf16_to_device, f32_from_bf16_bits, gemm_tolerance_report, mx_rows_to_host,
+                    mx_to_host, mx_upload, sample_rows)
 
 pytestmark = pytest.mark.gpu
-
-SILU_LIP = 1.1
-
 
 def _random_mx(rng, rows, k, lo=118, hi=124):
     codes = rng.integers(0, 64, size=(rows, k)).astype(np.uint8)
     scales = rng.integers(lo, hi, size=(rows, k // 32)).astype(np.uint8)
     return codes, scales
-
-
-def assert_swiglu_close(h_gpu, c_ref, what):
-    """h_gpu [M][F] against the oracle's stacked accumulators c_ref [M][2F] (bias included)."""
-    f = c_ref.shape[1] // 2
-    g, u = c_ref[:, :f], c_ref[:, f:]
-    tg = REL_TOL * np.abs(g) + RMS_TOL * np.sqrt(np.mean(g * g))
-    tu = REL_TOL * np.abs(u) + RMS_TOL * np.sqrt(np.mean(u * u))
-    ref = O.silu(g) * u
-    bound = SILU_LIP * tg * (np.abs(u) + tu) + np.abs(O.silu(g)) * tu + 1e-6 * np.abs(ref) + 1e-30
-    err = np.abs(np.asarray(h_gpu, np.float64) - ref)
-    bad = np.argwhere(err > bound)
-    assert bad.size == 0, (f"{what}: {len(bad)} of {err.size} outside, first {bad[:4].tolist()}, "
-                           f"worst ratio {float((err / bound).max()):.3g}")
-    return float((err / bound).max())
 
 
 def _swiglu(lib, a, b, bias_bits, m, f):

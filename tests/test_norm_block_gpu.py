@@ -1,0 +1,208 @@
+"""Parity of the fused RMSNorm + modulation quantizer and of the DiT MLP sub-block.
+
+Fused quantizer: the kernel's fp32 y (debug hook) against the oracle's fp64
+rms_norm_modulate, and the codes/scales bit-exact given that y. Tolerance of y:
+the fp32 sum of K positive squares (32 sequential terms per lane, then a tree)
+is within (32 + log2(K/32) + 2) 2^-24 < 3e-6 relative, the root halves that and
+the mean, the root and the reciprocal add three roundings; x rstd and the fma
+add one rounding each, 1 + scale one more relative to (1 + scale). So
+|dy| <= 5e-6 |x rstd (1 + scale)| + 2^-23 |y|.
+
+DiT MLP sub-block: mx_dit_mlp_block equals its three stages run one by one
+(fused quantizer, up-projection with the debug hook, gate/residual GEMM), each
+stage is checked against the oracle given the previous stage's GPU output, and
+the whole block against an independent oracle run: >= 99.9% of elements within
+the gate/residual tolerance, over the rows whose quantized normalised
+activations agree with the oracle's (a code may flip where the GPU's fp32 value
+and the oracle's sit on two sides of a rounding boundary; such rows are counted
+and bounded, 1% of the sampled rows at most).
+"""
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from mxutil import (REL_TOL, RMS_TOL, assert_codes_equal, assert_gemm_close, assert_swiglu_close,
+                    bf16_from_device, bf16_to_device, f32_from_bf16_bits, mx_rows_to_host, mx_to_host, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def _norm_ref_parts(x_bits, shift_bits, scale_bits, eps):
+    x = f32_from_bf16_bits(x_bits).astype(np.float64)
+    rstd = 1.0 / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps)
+    opp = 1.0 + f32_from_bf16_bits(scale_bits).astype(np.float64)
+    return np.abs(x * rstd * opp[None, :])
+
+
+def assert_norm_close(y_gpu, x_bits, shift_bits, scale_bits, eps, what):
+    ref = O.rms_norm_modulate(x_bits, shift_bits, scale_bits, eps)
+    bound = 5e-6 * _norm_ref_parts(x_bits, shift_bits, scale_bits, eps) + 2.0 ** -23 * np.abs(ref) + 1e-30
+    err = np.abs(np.asarray(y_gpu, np.float64) - ref)
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, f"{what}: {len(bad)} outside, first {bad[:4].tolist()}, worst {float((err / bound).max())}"
+
+
+def _norm_quant(lib, x_bits, shift_bits, scale_bits, eps, use_vectors=True):
+    import torch
+
+    x = bf16_to_device(x_bits)
+    sh = bf16_to_device(shift_bits) if use_vectors else None
+    sc = bf16_to_device(scale_bits) if use_vectors else None
+    rows, k = x_bits.shape
+    dbg = torch.full((rows, k), float("nan"), dtype=torch.float32, device="cuda")
+    out_dbg = lib.mx_quantize_rmsnorm_modulate(x, sh, sc, eps, debug_y=dbg)
+    out = lib.mx_quantize_rmsnorm_modulate(x, sh, sc, eps)
+    assert torch.equal(out.codes, out_dbg.codes) and torch.equal(out.scales, out_dbg.scales)
+    return out, dbg
+
+
+def _inputs(rng, rows, k):
+    # rows of very different magnitudes: the normalisation must remove them
+    mag = np.exp2(rng.integers(-10, 12, size=(rows, 1))).astype(np.float32)
+    x = synth.bf16_round(rng.standard_normal((rows, k)).astype(np.float32) * mag)
+    shift = synth.bf16_round((rng.standard_normal(k) * 0.5).astype(np.float32))
+    scale = synth.bf16_round((rng.standard_normal(k) * 0.5).astype(np.float32))
+    return x, shift, scale
+
+
+@pytest.mark.parametrize("rows,k", [(300, 3072), (129, 128), (64, 640), (200, 8192), (1, 4096)])
+def test_norm_quantize_random(lib, rows, k):
+    rng = np.random.default_rng(rows + k)
+    x, shift, scale = _inputs(rng, rows, k)
+    out, dbg = _norm_quant(lib, x, shift, scale, 1e-6)
+    y = dbg.cpu().numpy()
+    assert np.isfinite(y).all()
+    assert_norm_close(y, x, shift, scale, 1e-6, f"y {rows}x{k}")
+    codes, scales = mx_to_host(out)
+    rc, rs = O.quantize_f32(y)
+    assert_codes_equal(codes, rc, scales, rs, f"codes {rows}x{k}")
+    tiled = out.scales.cpu().numpy()
+    assert np.count_nonzero(tiled) == np.count_nonzero(O.scales_plain_to_tiled(rs, rows, k))
+
+
+def test_norm_quantize_without_modulation_and_zero_rows(lib):
+    rng = np.random.default_rng(77)
+    rows, k = 130, 1024
+    x, shift, scale = _inputs(rng, rows, k)
+    x[5] = 0          # an all-zero row: y = shift exactly (eps keeps the root finite)
+    out, dbg = _norm_quant(lib, x, shift, scale, 1e-6)
+    y = dbg.cpu().numpy()
+    np.testing.assert_array_equal(y[5], f32_from_bf16_bits(shift))
+    zero = np.zeros(k, np.uint16)
+    out0, dbg0 = _norm_quant(lib, x, shift, scale, 1e-6, use_vectors=False)
+    y0 = dbg0.cpu().numpy()
+    assert_norm_close(y0, x, zero, zero, 1e-6, "plain RMSNorm")
+    assert np.all(y0[5] == 0)
+    codes, scales = mx_to_host(out0)
+    rc, rs = O.quantize_f32(y0)
+    assert_codes_equal(codes, rc, scales, rs, "plain RMSNorm codes")
+
+
+@pytest.mark.slow
+def test_norm_quantize_full_size(lib):
+    """M=20480, d=3072 with the DiT block's conditioning vectors, sampled rows."""
+    import torch
+
+    w = synth.dit_block()
+    out, dbg = _norm_quant(lib, w["x"], w["shift"], w["scale"], w["eps"])
+    rows = sample_rows(20480)
+    y = dbg[torch.as_tensor(rows, device="cuda")].cpu().numpy()
+    assert_norm_close(y, w["x"][rows], w["shift"], w["scale"], w["eps"], "full-size y")
+    codes, scales = mx_rows_to_host(out, rows)
+    rc, rs = O.quantize_f32(y)
+    assert_codes_equal(codes, rc, scales, rs, "full-size codes")
+    assert lib.mx_device_error() == 0
+
+
+# ---------------------------------------------------------------- DiT MLP sub-block
+
+def _gate_res_report(y_gpu, c_ref, gate_f, y_ref):
+    rms = np.sqrt(np.mean(c_ref * c_ref))
+    bound = np.abs(gate_f)[None, :] * (REL_TOL * np.abs(c_ref) + RMS_TOL * rms) + 2.0 ** -8 * np.abs(y_ref) + 1e-30
+    bad = np.abs(y_gpu - y_ref) > bound
+    return {"n_bad": int(bad.sum()), "frac_ok": float(1 - bad.mean())}
+
+
+def _run_block(lib, w, rows, in_place=False):
+    import torch
+
+    act = lib.MX_ACT_SWIGLU if w["activation"] == "swiglu" else lib.MX_ACT_GELU_TANH
+    up_epi = lib.MX_EPI_BIAS_SWIGLU_MXFP6 if w["activation"] == "swiglu" else lib.MX_EPI_BIAS_GELU_MXFP6
+    x = bf16_to_device(w["x"])
+    M, d = w["x"].shape
+    ff = w["w2"].shape[1]
+    vec = {k: bf16_to_device(w[k]) for k in ("shift", "scale", "gate", "b_up", "b2")}
+    wup = lib.mx_quantize(bf16_to_device(w["w_up"]))
+    w2q = lib.mx_quantize(bf16_to_device(w["w2"]))
+    x_keep = x.clone()
+    y = lib.mx_dit_mlp_block(x, vec["shift"], vec["scale"], vec["gate"], wup, vec["b_up"], w2q, vec["b2"],
+                             eps=w["eps"], activation=act, y=x if in_place else None)
+    if in_place:
+        assert y.data_ptr() == x.data_ptr()
+
+    # the same kernels one by one, with the debug hooks
+    ydbg = torch.empty((M, d), dtype=torch.float32, device="cuda")
+    xq = lib.mx_quantize_rmsnorm_modulate(x_keep, vec["shift"], vec["scale"], w["eps"], debug_y=ydbg)
+    hdbg = torch.empty((M, ff), dtype=torch.float32, device="cuda")
+    hq = lib.mx_gemm(xq, wup, vec["b_up"], up_epi, debug_prequant=hdbg)
+    y2 = lib.mx_gemm_gate_residual(hq, w2q, vec["b2"], vec["gate"], x_keep)
+    assert torch.equal(y, y2), "mx_dit_mlp_block differs from its three stages"
+
+    idx = torch.as_tensor(rows, device="cuda")
+    r_wq, r_ws = O.quantize_bf16(w["w_up"])
+    r_w2q, r_w2s = O.quantize_bf16(w["w2"])
+    xr = w["x"][rows]
+    # stage 1: fused norm quantizer
+    a = ydbg[idx].cpu().numpy()
+    assert_norm_close(a, xr, w["shift"], w["scale"], w["eps"], "normalised x")
+    gxq, gxs = mx_rows_to_host(xq, rows)
+    rxq, rxs = O.quantize_f32(a)
+    assert_codes_equal(gxq, rxq, gxs, rxs, "xq")
+    # stage 2: up-projection + activation, given the GPU's xq
+    h = hdbg[idx].cpu().numpy()
+    if w["activation"] == "gelu":
+        assert_gemm_close(h, O.up_projection(gxq, gxs, r_wq, r_ws, w["b_up"]), "gelu")
+    else:
+        assert_swiglu_close(h, O.gemm(gxq, gxs, r_wq, r_ws, w["b_up"]), "swiglu")
+    ghq, ghs = mx_rows_to_host(hq, rows)
+    rhq, rhs = O.quantize_f32(h)
+    assert_codes_equal(ghq, rhq, ghs, rhs, "hq")
+    # stage 3: down-projection with gate and residual, given the GPU's hq
+    got = f32_from_bf16_bits(bf16_from_device(y[idx])).astype(np.float64)
+    c = O.down_projection(ghq, ghs, r_w2q, r_w2s, w["b2"])
+    gate_f = f32_from_bf16_bits(w["gate"]).astype(np.float64)
+    rep = _gate_res_report(got, c, gate_f, O.gate_residual(c, w["gate"], xr))
+    assert rep["n_bad"] == 0, rep
+    # the whole block against an independent oracle run. The normalised activations
+    # are rounded to fp32 before quantization on both sides, in different operation
+    # orders, so a code may legitimately differ where a value sits within an ulp of a
+    # rounding boundary; one such code moves a whole output row. Those rows are
+    # counted (both results are correct) and the rest are compared element-wise.
+    y_ref, mid = O.dit_mlp_block(xr, w["shift"], w["scale"], w["gate"], w["eps"], r_wq, r_ws, w["b_up"],
+                                 r_w2q, r_w2s, w["b2"], activation=w["activation"])
+    same = np.all(mid["xq"] == gxq, axis=1) & np.all(mid["xs"] == gxs, axis=1)
+    assert (~same).sum() <= max(2, 0.01 * len(rows)), f"{(~same).sum()} rows with a differing activation code"
+    rep = _gate_res_report(got[same], mid["c"][same], gate_f, y_ref[same])
+    rep["rows_with_differing_xq"] = int((~same).sum())
+    print(f"DiT block ({w['activation']}) end-to-end vs independent oracle: {rep}")
+    assert rep["frac_ok"] >= 0.999, rep
+    assert lib.mx_device_error() == 0
+
+
+@pytest.mark.parametrize("activation", ["gelu", "swiglu"])
+def test_small_dit_block(lib, activation):
+    _run_block(lib, synth.dit_block(M=300, d=256, ff=512 if activation == "gelu" else 384, activation=activation),
+               np.arange(300))
+
+
+def test_small_dit_block_in_place(lib):
+    _run_block(lib, synth.dit_block(M=257, d=512, ff=1024), np.arange(257), in_place=True)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("activation", ["gelu", "swiglu"])
+def test_full_dit_block(lib, activation):
+    """M=20480, d=3072; ff=12288 (GELU) or 8192 (SwiGLU)."""
+    _run_block(lib, synth.dit_block(activation=activation), sample_rows(20480, n_random=96))
