@@ -8,6 +8,12 @@ down-projection + bias + BF16 store. The weights are quantized once, before
 timing (they are inference weights). `value` is MLP GEMM TFLOP/s over the whole
 step (2*M*d*ff*2 flops per step, quantizer time included).
 
+Other --config values measure the smaller single-GEMM workloads (pr1, dit_up,
+dit_down), the outlier-heavy wide MLP, and the neighbouring fusions: the SwiGLU
+MLP (gated_mlp), the stacked query/key/value/gate projection (qkv_proj) and the
+MLP half of a DiT block with the fused RMSNorm quantizer and the gate/residual
+epilogue (dit_block, dit_block_swiglu).
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 
 Timing: CUDA events on the launching stream around exactly K steps, after W
@@ -51,7 +57,28 @@ CONFIGS = {
                      workload="DiT MLP down-projection (M=16384, K=12288, N=3072, bias+BF16 store)"),
     "pr1": dict(kind="gemm", M=128, d=256, ff=512,
                 workload="single MXFP6 GEMM (M=128, K=256, N=512, bias+BF16)"),
+    "gated_mlp": dict(kind="gated_mlp", M=20480, d=3072, ff=8192,
+                      workload="SwiGLU DiT MLP (M=20480, d=3072, ff=8192: stacked gate/up GEMM N=16384 + "
+                               "silu(g)*u + MXFP6 requant, down-projection K=8192)"),
+    "qkv_proj": dict(kind="qkv", M=20480, d=3072, ff=4 * 3072,
+                     workload="stacked query/key/value/gate projection (M=20480, K=3072, N=4*3072, bias+BF16)"),
+    "dit_block": dict(kind="block", M=20480, d=3072, ff=12288, activation="gelu",
+                      workload="DiT MLP sub-block (M=20480, d=3072, ff=12288: RMSNorm+modulation+MXFP6 quantize "
+                               "-> up+GELU+requant -> down + gate x output + residual)"),
+    "dit_block_swiglu": dict(kind="block", M=20480, d=3072, ff=8192, activation="swiglu",
+                             workload="DiT MLP sub-block, SwiGLU (M=20480, d=3072, ff=8192: RMSNorm+modulation+"
+                                      "MXFP6 quantize -> stacked gate/up+SwiGLU+requant -> down + gate + residual)"),
 }
+
+# names of the launches of one step
+S_K1 = "K1 quantize"
+S_K1N = "K1 RMSNorm+modulate+quantize"
+S_UP = "K3 up GEMM+GELU+requant"
+S_GU = "K3 gate/up GEMM+SwiGLU+requant"
+S_DOWN = "K2 down GEMM+bias+BF16"
+S_DOWNR = "K2 down GEMM+bias+gate+residual"
+S_GEMM = "K2 GEMM+bias+BF16"
+S_QKV = "QKV+gate GEMM+bias+BF16"
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the current kernels, keyed by (config, kernel); None where no
@@ -183,30 +210,46 @@ class Workload:
         kind = cfg["kind"]
         M, d, ff = m_rows, cfg["d"], cfg["ff"]
         self.M, self.d, self.ff = M, d, ff
-        if kind in ("mlp",):
-            gen = synth.outlier_mlp if cfg is CONFIGS["outlier_mlp"] else synth.full_mlp
-            w = gen(seed=seed, M=M, d=d, ff=ff)
+
+        def mx_empty(rows, k):
+            return mx.MxTensor(torch.empty((rows, k * 3 // 4), dtype=torch.uint8, device=dev),
+                               torch.empty(mx.mx_scales_bytes(rows, k), dtype=torch.uint8, device=dev), rows, k)
+
+        if kind in ("mlp", "gated_mlp", "block"):
+            if kind == "mlp":
+                gen = synth.outlier_mlp if cfg is CONFIGS["outlier_mlp"] else synth.full_mlp
+                w = gen(seed=seed, M=M, d=d, ff=ff)
+                w_up, b_up = w["w1"], w["b1"]
+            elif kind == "gated_mlp":
+                w = synth.gated_mlp(seed=seed, M=M, d=d, ff=ff)
+                w_up, b_up = w["wgu"], w["bgu"]
+            else:
+                w = synth.dit_block(seed=seed, M=M, d=d, ff=ff, activation=cfg["activation"])
+                w_up, b_up = w["w_up"], w["b_up"]
+                self.shift, self.scale, self.gate = (_bf16_dev(w[k], dev) for k in ("shift", "scale", "gate"))
+                self.eps = w["eps"]
             self.x = _bf16_dev(w["x"], dev)
-            self.w1 = mx.mx_quantize(_bf16_dev(w["w1"], dev))
+            self.w1 = mx.mx_quantize(_bf16_dev(w_up, dev))
             self.w2 = mx.mx_quantize(_bf16_dev(w["w2"], dev))
-            self.b1 = _bf16_dev(w["b1"], dev)
+            self.b1 = _bf16_dev(b_up, dev)
             self.b2 = _bf16_dev(w["b2"], dev)
-            self.xq = mx.MxTensor(torch.empty((M, d * 3 // 4), dtype=torch.uint8, device=dev),
-                                  torch.empty(mx.mx_scales_bytes(M, d), dtype=torch.uint8, device=dev), M, d)
-            self.hq = mx.MxTensor(torch.empty((M, ff * 3 // 4), dtype=torch.uint8, device=dev),
-                                  torch.empty(mx.mx_scales_bytes(M, ff), dtype=torch.uint8, device=dev), M, ff)
+            self.xq = mx_empty(M, d)
+            self.hq = mx_empty(M, ff)
             self.y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
             self.host = w
-        elif kind in ("up", "gemm"):
-            w = synth.dit_up(seed=seed, M=M, d=d, ff=ff) if kind == "up" else synth.pr1(seed=seed, M=M, K=d, N=ff)
+        elif kind in ("up", "gemm", "qkv"):
+            if kind == "up":
+                w = synth.dit_up(seed=seed, M=M, d=d, ff=ff)
+            elif kind == "qkv":
+                w = synth.qkv_proj(seed=seed, M=M, d=d, stack=ff // d)
+            else:
+                w = synth.pr1(seed=seed, M=M, K=d, N=ff)
             self.x = _bf16_dev(w["x"], dev)
             self.w1 = mx.mx_quantize(_bf16_dev(w["w"], dev))
             self.b1 = _bf16_dev(w["b"], dev)
-            self.xq = mx.MxTensor(torch.empty((M, d * 3 // 4), dtype=torch.uint8, device=dev),
-                                  torch.empty(mx.mx_scales_bytes(M, d), dtype=torch.uint8, device=dev), M, d)
+            self.xq = mx_empty(M, d)
             if kind == "up":
-                self.hq = mx.MxTensor(torch.empty((M, ff * 3 // 4), dtype=torch.uint8, device=dev),
-                                      torch.empty(mx.mx_scales_bytes(M, ff), dtype=torch.uint8, device=dev), M, ff)
+                self.hq = mx_empty(M, ff)
             else:
                 self.y = torch.empty((M, ff), dtype=torch.bfloat16, device=dev)
             self.host = w
@@ -226,36 +269,51 @@ class Workload:
     def stages(self, mx):
         """The step's launches as (name, callable) in stream order."""
         kind = self.cfg["kind"]
+        swiglu = kind == "gated_mlp" or (kind == "block" and self.cfg["activation"] == "swiglu")
         out = []
-        if kind in ("mlp", "up", "gemm"):
-            out.append(("K1 quantize", lambda: mx.mx_quantize(self.x, out=self.xq)))
-        if kind in ("mlp", "up"):
-            out.append(("K3 up GEMM+GELU+requant",
-                        lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_GELU_MXFP6, out=self.hq)))
-        if kind == "gemm":
-            out.append(("K2 GEMM+bias+BF16", lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16,
-                                                                   out=self.y)))
-        if kind in ("mlp", "down"):
-            out.append(("K2 down GEMM+bias+BF16",
-                        lambda: mx.mx_gemm(self.hq, self.w2, self.b2, mx.MX_EPI_BIAS_BF16, out=self.y)))
+        if kind in ("mlp", "gated_mlp", "up", "gemm", "qkv"):
+            out.append((S_K1, lambda: mx.mx_quantize(self.x, out=self.xq)))
+        if kind == "block":
+            out.append((S_K1N, lambda: mx.mx_quantize_rmsnorm_modulate(self.x, self.shift, self.scale, self.eps,
+                                                                       out=self.xq)))
+        if kind in ("mlp", "gated_mlp", "up", "block"):
+            epi = mx.MX_EPI_BIAS_SWIGLU_MXFP6 if swiglu else mx.MX_EPI_BIAS_GELU_MXFP6
+            out.append((S_GU if swiglu else S_UP, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, epi, out=self.hq)))
+        if kind in ("gemm", "qkv"):
+            out.append((S_QKV if kind == "qkv" else S_GEMM,
+                        lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y)))
+        if kind in ("mlp", "gated_mlp", "down"):
+            out.append((S_DOWN, lambda: mx.mx_gemm(self.hq, self.w2, self.b2, mx.MX_EPI_BIAS_BF16, out=self.y)))
+        if kind == "block":
+            out.append((S_DOWNR, lambda: mx.mx_gemm_gate_residual(self.hq, self.w2, self.b2, self.gate, self.x,
+                                                                  out=self.y)))
         return out
 
 
 def stage_work(cfg: dict, M: int) -> dict:
-    """Algorithmic flops / bytes per launch of each stage."""
+    """Algorithmic flops / bytes per launch of each stage (0.78125 = 0.75 code +
+    1/32 scale bytes per MXFP6 element)."""
     d, ff = cfg["d"], cfg["ff"]
     kind = cfg["kind"]
+    swiglu = kind == "gated_mlp" or (kind == "block" and cfg.get("activation") == "swiglu")
+    q = 0.78125
     out = {}
-    if kind in ("mlp", "up", "gemm"):
-        out["K1 quantize"] = {"bytes": M * d * (2 + 0.75 + 1 / 32), "flops": 0.0}
-    if kind in ("mlp", "up"):
-        out["K3 up GEMM+GELU+requant"] = {"flops": 2.0 * M * d * ff,
-                                          "bytes": M * d * 0.78125 + ff * d * 0.78125 + M * ff * 0.78125}
+    if kind in ("mlp", "gated_mlp", "up", "gemm", "qkv"):
+        out[S_K1] = {"bytes": M * d * (2 + q), "flops": 0.0}
+    if kind == "block":
+        out[S_K1N] = {"bytes": M * d * (2 + q), "flops": 0.0}
+    if kind in ("mlp", "up", "block") and not swiglu:
+        out[S_UP] = {"flops": 2.0 * M * d * ff, "bytes": M * d * q + ff * d * q + M * ff * q}
+    if swiglu:
+        out[S_GU] = {"flops": 2.0 * M * d * 2 * ff, "bytes": M * d * q + 2 * ff * d * q + M * ff * q}
     if kind == "gemm":
-        out["K2 GEMM+bias+BF16"] = {"flops": 2.0 * M * d * ff, "bytes": (M + ff) * d * 0.78125 + M * ff * 2}
-    if kind in ("mlp", "down"):
-        out["K2 down GEMM+bias+BF16"] = {"flops": 2.0 * M * d * ff,
-                                         "bytes": M * ff * 0.78125 + d * ff * 0.78125 + M * d * 2}
+        out[S_GEMM] = {"flops": 2.0 * M * d * ff, "bytes": (M + ff) * d * q + M * ff * 2}
+    if kind == "qkv":
+        out[S_QKV] = {"flops": 2.0 * M * d * ff, "bytes": (M + ff) * d * q + M * ff * 2}
+    if kind in ("mlp", "gated_mlp", "down"):
+        out[S_DOWN] = {"flops": 2.0 * M * d * ff, "bytes": M * ff * q + d * ff * q + M * d * 2}
+    if kind == "block":
+        out[S_DOWNR] = {"flops": 2.0 * M * d * ff, "bytes": M * ff * q + d * ff * q + M * d * 4}
     return out
 
 
@@ -373,7 +431,7 @@ def run_gpu(args) -> dict | None:
                          "each step's working set exceeds the 129 MB L2, so no step reads operands the "
                          "previous step left in L2" if args.copies > 1 else "single copy (profiling run)",
                    "parallelism": f"token-sharded x{world}, weights replicated, no collective"},
-        "ms_per_mlp": ms_step if cfg["kind"] == "mlp" else None,
+        "ms_per_mlp": ms_step if cfg["kind"] in ("mlp", "gated_mlp", "block") else None,
         "stages": stage_report,
         "roofline": roof,
         "pct_fp6_peak_spec_5pf": value / FP6_SPEC_PEAK_TFLOPS,
@@ -381,9 +439,10 @@ def run_gpu(args) -> dict | None:
         "clocks": clk,
         "e2e": e2e,
     }
-    if "K1 quantize" in stage_report:
-        line["quantize_gbs"] = stage_report["K1 quantize"]["gbs"]
-        line["quantize_frac_hbm"] = stage_report["K1 quantize"]["gbs"] / peaks["hbm_gbs"]
+    k1 = S_K1 if S_K1 in stage_report else (S_K1N if S_K1N in stage_report else None)
+    if k1 is not None:
+        line["quantize_gbs"] = stage_report[k1]["gbs"]
+        line["quantize_frac_hbm"] = stage_report[k1]["gbs"] / peaks["hbm_gbs"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_budget)
     return line
@@ -399,7 +458,7 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
 
     kind = cfg["kind"]
     c = copies[0]
-    if kind == "mlp":
+    if kind in ("mlp", "gated_mlp", "block"):
         src, dst = c.x, c.y
     elif kind == "down":
         src, dst = c.hq.codes, c.y
@@ -415,7 +474,7 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
     x_buf = [src, torch.empty_like(src)]
     y_buf = [dst, torch.empty_like(dst)]
     ws = None
-    if kind == "mlp":
+    if kind in ("mlp", "gated_mlp", "block"):
         ws = torch.empty(max(256, mx.mx_mlp_workspace_bytes(c.M, c.d, c.ff)), dtype=torch.uint8, device=dev)
     s_up, s_comp, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
     ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
@@ -428,6 +487,12 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
     def compute(slot):
         if kind == "mlp":
             mx.mx_mlp(x_buf[slot], c.w1, c.b1, c.w2, c.b2, y=y_buf[slot], workspace=ws, stream=s_comp)
+        elif kind == "gated_mlp":
+            mx.mx_gated_mlp(x_buf[slot], c.w1, c.b1, c.w2, c.b2, y=y_buf[slot], workspace=ws, stream=s_comp)
+        elif kind == "block":
+            act = mx.MX_ACT_SWIGLU if cfg["activation"] == "swiglu" else mx.MX_ACT_GELU_TANH
+            mx.mx_dit_mlp_block(x_buf[slot], c.shift, c.scale, c.gate, c.w1, c.b1, c.w2, c.b2, eps=c.eps,
+                                activation=act, y=y_buf[slot], workspace=ws, stream=s_comp)
         elif kind == "down":
             mx.mx_gemm(mx.MxTensor(x_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), c.w2, c.b2,
                        mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp)
@@ -495,13 +560,27 @@ class OracleWorkload:
         self.cfg = cfg
         kind = cfg["kind"]
         M = cfg["M"]
-        if kind == "mlp":
-            gen = synth.outlier_mlp if cfg is CONFIGS["outlier_mlp"] else synth.full_mlp
-            w = gen(M=M, d=cfg["d"], ff=cfg["ff"])
-            self.w1q, self.w1s = O.quantize_bf16(w["w1"])
+        d, ff = cfg["d"], cfg["ff"]
+        if kind in ("mlp", "gated_mlp", "block"):
+            if kind == "mlp":
+                gen = synth.outlier_mlp if cfg is CONFIGS["outlier_mlp"] else synth.full_mlp
+                w = gen(M=M, d=d, ff=ff)
+                w_up = w["w1"]
+            elif kind == "gated_mlp":
+                w = synth.gated_mlp(M=M, d=d, ff=ff)
+                w_up = w["wgu"]
+            else:
+                w = synth.dit_block(M=M, d=d, ff=ff, activation=cfg["activation"])
+                w_up = w["w_up"]
+            self.w1q, self.w1s = O.quantize_bf16(w_up)
             self.w2q, self.w2s = O.quantize_bf16(w["w2"])
-        elif kind in ("up", "gemm"):
-            w = synth.dit_up(M=M) if kind == "up" else synth.pr1()
+        elif kind in ("up", "gemm", "qkv"):
+            if kind == "up":
+                w = synth.dit_up(M=M)
+            elif kind == "qkv":
+                w = synth.qkv_proj(M=M, d=d, stack=ff // d)
+            else:
+                w = synth.pr1()
             self.w1q, self.w1s = O.quantize_bf16(w["w"])
         else:
             w = synth.dit_down(M=min(M, sample_rows * 8))
@@ -516,12 +595,19 @@ class OracleWorkload:
         if kind == "mlp":
             O.mlp(w["x"][rows], self.w1q, self.w1s, w["b1"], self.w2q, self.w2s, w["b2"])
             return 4.0 * len(rows) * d * ff
+        if kind == "gated_mlp":
+            O.gated_mlp(w["x"][rows], self.w1q, self.w1s, w["bgu"], self.w2q, self.w2s, w["b2"])
+            return 6.0 * len(rows) * d * ff
+        if kind == "block":
+            O.dit_mlp_block(w["x"][rows], w["shift"], w["scale"], w["gate"], w["eps"], self.w1q, self.w1s,
+                            w["b_up"], self.w2q, self.w2s, w["b2"], activation=self.cfg["activation"])
+            return (6.0 if self.cfg["activation"] == "swiglu" else 4.0) * len(rows) * d * ff
         if kind == "up":
             xq, xs = O.quantize_bf16(w["x"][rows])
             g = O.up_projection(xq, xs, self.w1q, self.w1s, w["b"])
             O.quantize_f32(g.astype(np.float32))
             return 2.0 * len(rows) * d * ff
-        if kind == "gemm":
+        if kind in ("gemm", "qkv"):
             xq, xs = O.quantize_bf16(w["x"][rows])
             O.gemm(xq, xs, self.w1q, self.w1s, w["b"])
             return 2.0 * len(rows) * d * ff

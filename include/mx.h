@@ -102,7 +102,7 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, void
  * memory traffic": modulation merged with RMSNorm; "Creating Custom Kernels for
  * the AMD MI300", section "Fused RMS Norm Kernel").
  *   y[m][k] = x[m][k] / sqrt(mean_k' x[m][k']^2 + eps) * (1 + scale[k]) + shift[k]
- * in fp32 (sum of squares in fp32, 1/sqrt correctly rounded, then
+ * in fp32 (sum of squares in fp32, rstd = rsqrtf(sum / K + eps) within 2 ulp, then
  * fma(x * rstd, 1 + scale, shift)); codes/scales = MXFP6(y) by the mx_quantize rule.
  *   x, rows, K, ld_x, codes, scales : as mx_quantize, and K <= 8192
  *   shift, scale : device BF16 [K] (one conditioning vector for all rows), 16-byte

@@ -37,20 +37,4 @@ __host__ __device__ __forceinline__ int64_t scale_word_offset(int64_t row, int64
   return ((row / kAtomRows) * (k / kAtomK) + kc) * kAtomBytes + (row % 32) * 16 + ((row % 128) / 32) * 4;
 }
 
-// Four 6-bit codes held one per byte -> 24 bits, code i at bits 6i.
-__device__ __forceinline__ uint32_t pack4(uint32_t q) {
-  const uint32_t t = (q & 0x003F003Fu) | ((q >> 2) & 0x0FC00FC0u);  // c0 | c1<<6 | c2<<16 | c3<<22
-  return (t & 0xFFFu) | ((t >> 4) & 0xFFF000u);
-}
-
-// Eight 24-bit groups (32 codes) -> the six little-endian words of their 24 bytes.
-__device__ __forceinline__ void pack32(const uint32_t (&g)[8], uint32_t (&w)[6]) {
-  w[0] = g[0] | (g[1] << 24);
-  w[1] = (g[1] >> 8) | (g[2] << 16);
-  w[2] = (g[2] >> 16) | (g[3] << 8);
-  w[3] = g[4] | (g[5] << 24);
-  w[4] = (g[5] >> 8) | (g[6] << 16);
-  w[5] = (g[6] >> 16) | (g[7] << 8);
-}
-
 }  // namespace mxk

@@ -12,19 +12,61 @@
 
 namespace mxk {
 
+// max(a, b, c), NaN if any is NaN (PTX three-input max.NaN).
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Block amax of 32 fp32 values as magnitude bits: +0 .. 0x7F7FFFFF finite, 0x7F800000
+// Inf, above that NaN (max.NaN returns the canonical NaN 0x7FFFFFFF). A tree of
+// three-input maxima: 32 -> 11 -> 4 -> 2 -> 1.
+__device__ __forceinline__ uint32_t amax_bits32(const float (&g)[32]) {
+  float m[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) m[i] = max3_nan(fabsf(g[3 * i]), fabsf(g[3 * i + 1]), fabsf(g[3 * i + 2]));
+  m[10] = max_nan(fabsf(g[30]), fabsf(g[31]));
+  const float n0 = max3_nan(m[0], m[1], m[2]);
+  const float n1 = max3_nan(m[3], m[4], m[5]);
+  const float n2 = max3_nan(m[6], m[7], m[8]);
+  const float n3 = max_nan(m[9], m[10]);
+  return __float_as_uint(max_nan(max3_nan(n0, n1, n2), n3));
+}
+
+// Two E2M3 codes held one per byte (c0 | c1 << 8, as the paired convert returns
+// them) -> the 12-bit group c0 | c1 << 6, as c0 + 256 c1 - 192 c1.
+__device__ __forceinline__ uint32_t pack2(uint32_t v) { return v - 192u * (v >> 8); }
+
+// Four codes from two paired converts -> their 24-bit group c0 | c1 << 6 | c2 << 12 | c3 << 18.
+__device__ __forceinline__ uint32_t pack4_pairs(uint32_t lo_pair, uint32_t hi_pair) {
+  return pack2(lo_pair) + 4096u * pack2(hi_pair);
+}
+
+// Eight 24-bit groups (32 codes) -> the six little-endian words of their 24 bytes
+// (group j at bits [24 j, 24 j + 24) of the block's bit string).
+__device__ __forceinline__ void pack_groups(const uint32_t (&grp)[8], uint32_t (&w)[6]) {
+  w[0] = grp[0] + (grp[1] << 24);
+  w[1] = (grp[1] >> 8) + (grp[2] << 16);
+  w[2] = (grp[2] >> 16) + (grp[3] << 8);
+  w[3] = grp[4] + (grp[5] << 24);
+  w[4] = (grp[5] >> 8) + (grp[6] << 16);
+  w[5] = (grp[6] >> 16) + (grp[7] << 8);
+}
+
 // MXFP6 encoding of one 32-value block: returns the E8M0 code and the block's 24
 // code bytes as six little-endian words (the quantizer's rule, on fp32 values).
+// The code bits are assembled with multiply-adds of disjoint fields, which keeps
+// the integer ALU (also busy with the maxima and the converts) from being the
+// bottleneck.
 __device__ __forceinline__ uint32_t quant_block32(const float (&g)[32], uint32_t (&w)[6]) {
-  // |g| order = unsigned order of the magnitude bits (NaN/Inf sort last); a tree keeps it shallow
-  uint32_t m[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    m[i] = max(__float_as_uint(g[2 * i]) & 0x7FFFFFFFu, __float_as_uint(g[2 * i + 1]) & 0x7FFFFFFFu);
-#pragma unroll
-  for (int w2 = 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-    for (int i = 0; i < w2; ++i) m[i] = max(m[i], m[i + w2]);
-  const uint32_t amax = m[0];
+  const uint32_t amax = amax_bits32(g);
   if (amax >= 0x7F800000u) {  // Inf or NaN: E8M0 NaN, zero codes
 #pragma unroll
     for (int i = 0; i < 6; ++i) w[i] = 0;
@@ -33,14 +75,12 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&g)[32], uint32_t
   const int e = static_cast<int>(amax >> 23);
   const uint32_t sc = static_cast<uint32_t>(e > 2 ? e - 2 : 0);
   const float fac = __uint_as_float((254u - sc) << 23);  // 2^-s, exact
-  uint32_t grp[8];
+  uint32_t grp[8];   // 24-bit groups of four codes
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t lo = cvt_e2m3x2(g[4 * j + 1] * fac, g[4 * j] * fac);
-    const uint32_t hi = cvt_e2m3x2(g[4 * j + 3] * fac, g[4 * j + 2] * fac);
-    grp[j] = pack4(lo | (hi << 16));
-  }
-  pack32(grp, w);
+  for (int j = 0; j < 8; ++j)
+    grp[j] = pack4_pairs(cvt_e2m3x2(g[4 * j + 1] * fac, g[4 * j] * fac),
+                         cvt_e2m3x2(g[4 * j + 3] * fac, g[4 * j + 2] * fac));
+  pack_groups(grp, w);
   return sc;
 }
 

@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_
   const int blocks_per_row = k / kBlock;
   const int kb = warp * 32 + lane;            // this lane's K-block
   const bool active = kb < blocks_per_row;
-  const float kf = static_cast<float>(k);
+  const float inv_k = 1.0f / static_cast<float>(k);
   __shared__ float partial[2][kNormMaxWarps];
   __shared__ __align__(16) uint32_t stage[kNormMaxWarps][192];
 
@@ -106,20 +106,22 @@ __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_
     }
     const uint32_t xw[16] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y, cur[1].z, cur[1].w,
                              cur[2].x, cur[2].y, cur[2].z, cur[2].w, cur[3].x, cur[3].y, cur[3].z, cur[3].w};
-    float ss = 0.f;
+    // four interleaved partial sums keep the dependent chain 8 deep
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float a = bf16_lo(xw[i]), b = bf16_hi(xw[i]);
-      ss = fmaf(a, a, ss);
-      ss = fmaf(b, b, ss);
+      s4[i & 3] = fmaf(a, a, s4[i & 3]);
+      s4[i & 3] = fmaf(b, b, s4[i & 3]);
     }
+    float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) partial[parity][warp] = ss;
     __syncthreads();
-    float tot = 0.f;
-    for (int w = 0; w < nwarps; ++w) tot += partial[parity][w];   // same order in every thread
-    const float rstd = 1.0f / sqrtf(tot / kf + eps);
+    float tot = partial[parity][0];
+    for (int w = 1; w < nwarps; ++w) tot += partial[parity][w];   // same order in every thread
+    const float rstd = rsqrtf(fmaf(tot, inv_k, eps));   // CUDA's rsqrtf: within 2 ulp
 
     uint32_t sc = 0;
     if (active) {

@@ -15,6 +15,7 @@
 
 #include "internal.h"
 #include "mx_layout.cuh"
+#include "mx_quant.cuh"
 #include "ptx.cuh"
 
 namespace mxk {
@@ -111,10 +112,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_bf16_kernel(
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             p[i] = cvt_e2m3x2(__uint_as_float(v[i] & 0xFFFF0000u) * fac, __uint_as_float(v[i] << 16) * fac);
-          g[2 * j] = pack4(p[0] | (p[1] << 16));
-          g[2 * j + 1] = pack4(p[2] | (p[3] << 16));
+          g[2 * j] = pack4_pairs(p[0], p[1]);
+          g[2 * j + 1] = pack4_pairs(p[2], p[3]);
         }
-        pack32(g, w);
+        pack_groups(g, w);
       }
       uint2* s2 = reinterpret_cast<uint2*>(&st[u][6 * lane]);
       s2[0] = make_uint2(w[0], w[1]);

@@ -2,10 +2,11 @@
 
 Fused quantizer: the kernel's fp32 y (debug hook) against the oracle's fp64
 rms_norm_modulate, and the codes/scales bit-exact given that y. Tolerance of y:
-the fp32 sum of K positive squares (32 sequential terms per lane, then a tree)
-is within (32 + log2(K/32) + 2) 2^-24 < 3e-6 relative, the root halves that and
-the mean, the root and the reciprocal add three roundings; x rstd and the fma
-add one rounding each, 1 + scale one more relative to (1 + scale). So
+the fp32 sum of K positive squares (four interleaved partial sums of 8 terms per
+lane, then trees) is within (8 + 2 + log2(K/32) + 2) 2^-24 < 2e-6 relative, the
+root halves that; the multiply by the fp32 1/K and the fma with eps add two
+roundings and rsqrtf at most 2 ulp; x rstd and the fma add one rounding each,
+1 + scale one more relative to (1 + scale). So
 |dy| <= 5e-6 |x rstd (1 + scale)| + 2^-23 |y|.
 
 DiT MLP sub-block: mx_dit_mlp_block equals its three stages run one by one
