@@ -350,11 +350,31 @@ __device__ __forceinline__ float gelu_tanh(float v) {
   return v * rcp_approx(1.0f + ex2_approx(t));
 }
 
+// gelu_tanh of a packed pair, rounding exactly as the scalar form: the multiplies,
+// the fma and the add run two-wide, 2^t and the reciprocal per lane.
+__device__ __forceinline__ void gelu_tanh2(uint64_t v, float& g0, float& g1) {
+  const uint64_t t = f2_mul(v, f2_fma(f2_mul(v, v), f2_pack(kGeluC1, kGeluC1), f2_pack(kGeluC2, kGeluC2)));
+  float t0, t1;
+  f2_unpack(t, t0, t1);
+  float d0, d1;
+  f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), f2_pack(1.0f, 1.0f)), d0, d1);
+  f2_unpack(f2_mul(v, f2_pack(rcp_approx(d0), rcp_approx(d1))), g0, g1);
+}
+
 // silu(v) = v / (1 + e^-v) = v / (1 + 2^(-v log2 e)). For very negative v, 2^.. is
 // +inf and the result is v * 0 = -0 (the exact value is below 1e-37 in magnitude).
 constexpr float kNegLog2e = -1.4426950408889634f;
 
 __device__ __forceinline__ float silu(float v) { return v * rcp_approx(1.0f + ex2_approx(v * kNegLog2e)); }
+
+// silu(g) * u of packed pairs, rounding exactly as the scalar form.
+__device__ __forceinline__ void silu_mul2(uint64_t g, uint64_t u, float& h0, float& h1) {
+  float t0, t1;
+  f2_unpack(f2_mul(g, f2_pack(kNegLog2e, kNegLog2e)), t0, t1);
+  float d0, d1;
+  f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), f2_pack(1.0f, 1.0f)), d0, d1);
+  f2_unpack(f2_mul(f2_mul(g, f2_pack(rcp_approx(d0), rcp_approx(d1))), u), h0, h1);
+}
 
 __device__ __forceinline__ void store_block_codes(uint8_t* dst_bytes, const uint32_t (&w)[6]) {
   uint2* dst = reinterpret_cast<uint2*>(dst_bytes);
@@ -450,17 +470,20 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const float4 b4 = staged4(bw, c, v);
-          float x0 = __uint_as_float(r[c][4 * v]) + b4.x;
-          float x1 = __uint_as_float(r[c][4 * v + 1]) + b4.y;
-          float x2 = __uint_as_float(r[c][4 * v + 2]) + b4.z;
-          float x3 = __uint_as_float(r[c][4 * v + 3]) + b4.w;
+          uint64_t x01 = f2_add(f2_pack(__uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1])),
+                                f2_pack(b4.x, b4.y));
+          uint64_t x23 = f2_add(f2_pack(__uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3])),
+                                f2_pack(b4.z, b4.w));
           if constexpr (EPI == kEpiGateRes) {
             const float4 g4 = staged4(gw, c, v);
-            x0 = fmaf(g4.x, x0, __uint_as_float(rw[2 * v] << 16));
-            x1 = fmaf(g4.y, x1, __uint_as_float(rw[2 * v] & 0xFFFF0000u));
-            x2 = fmaf(g4.z, x2, __uint_as_float(rw[2 * v + 1] << 16));
-            x3 = fmaf(g4.w, x3, __uint_as_float(rw[2 * v + 1] & 0xFFFF0000u));
+            x01 = f2_fma(f2_pack(g4.x, g4.y), x01,
+                         f2_pack(__uint_as_float(rw[2 * v] << 16), __uint_as_float(rw[2 * v] & 0xFFFF0000u)));
+            x23 = f2_fma(f2_pack(g4.z, g4.w), x23,
+                         f2_pack(__uint_as_float(rw[2 * v + 1] << 16), __uint_as_float(rw[2 * v + 1] & 0xFFFF0000u)));
           }
+          float x0, x1, x2, x3;
+          f2_unpack(x01, x0, x1);
+          f2_unpack(x23, x2, x3);
           pk[2 * v] = cvt_bf16x2(x1, x0);
           pk[2 * v + 1] = cvt_bf16x2(x3, x2);
         }
@@ -482,17 +505,19 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const float4 b4 = staged4(bw, c, v);
-          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
-          if constexpr (EPI == kEpiGelu) {
+          const uint64_t bb[2] = {f2_pack(b4.x, b4.y), f2_pack(b4.z, b4.w)};
 #pragma unroll
-            for (int t = 0; t < 4; ++t) g[4 * v + t] = gelu_tanh(__uint_as_float(r[c][4 * v + t]) + bb[t]);
-          } else {
-            const float4 u4 = staged4(bw, 2 + c, v);
-            const float bu[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              g[4 * v + t] = silu(__uint_as_float(r[c][4 * v + t]) + bb[t]) *
-                             (__uint_as_float(r[2 + c][4 * v + t]) + bu[t]);
+          for (int t = 0; t < 2; ++t) {
+            const int i = 4 * v + 2 * t;
+            const uint64_t x = f2_add(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), bb[t]);
+            if constexpr (EPI == kEpiGelu) {
+              gelu_tanh2(x, g[i], g[i + 1]);
+            } else {
+              const float4 u4 = staged4(bw, 2 + c, v);
+              const uint64_t bu = t == 0 ? f2_pack(u4.x, u4.y) : f2_pack(u4.z, u4.w);
+              const uint64_t u = f2_add(f2_pack(__uint_as_float(r[2 + c][i]), __uint_as_float(r[2 + c][i + 1])), bu);
+              silu_mul2(x, u, g[i], g[i + 1]);
+            }
           }
         }
         if constexpr (DBG) {

@@ -12,41 +12,68 @@
 
 namespace mxk {
 
-// max(a, b, c), NaN if any is NaN (PTX three-input max.NaN).
+// Three- and two-input maxima / minima, NaN if any input is NaN (PTX max.NaN / min.NaN).
 __device__ __forceinline__ float max3_nan(float a, float b, float c) {
   float d;
   asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-
+__device__ __forceinline__ float min3_nan(float a, float b, float c) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ float max_nan(float a, float b) {
   float d;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
   return d;
 }
-
-// Block amax of 32 fp32 values as magnitude bits: +0 .. 0x7F7FFFFF finite, 0x7F800000
-// Inf, above that NaN (max.NaN returns the canonical NaN 0x7FFFFFFF). A tree of
-// three-input maxima: 32 -> 11 -> 4 -> 2 -> 1.
-__device__ __forceinline__ uint32_t amax_bits32(const float (&g)[32]) {
-  float m[11];
-#pragma unroll
-  for (int i = 0; i < 10; ++i) m[i] = max3_nan(fabsf(g[3 * i]), fabsf(g[3 * i + 1]), fabsf(g[3 * i + 2]));
-  m[10] = max_nan(fabsf(g[30]), fabsf(g[31]));
-  const float n0 = max3_nan(m[0], m[1], m[2]);
-  const float n1 = max3_nan(m[3], m[4], m[5]);
-  const float n2 = max3_nan(m[6], m[7], m[8]);
-  const float n3 = max_nan(m[9], m[10]);
-  return __float_as_uint(max_nan(max3_nan(n0, n1, n2), n3));
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
-// Two E2M3 codes held one per byte (c0 | c1 << 8, as the paired convert returns
-// them) -> the 12-bit group c0 | c1 << 6, as c0 + 256 c1 - 192 c1.
-__device__ __forceinline__ uint32_t pack2(uint32_t v) { return v - 192u * (v >> 8); }
+// Block amax of 32 fp32 values as magnitude bits: +0 .. 0x7F7FFFFF finite, 0x7F800000
+// Inf, above that NaN (max.NaN returns the canonical NaN 0x7FFFFFFF). The largest
+// and the smallest value by three-input trees (32 -> 11 -> 4 -> 2 -> 1, no per-value
+// absolute value), then max(hi, -lo) with the sign bit cleared (signed zeros).
+__device__ __forceinline__ uint32_t amax_bits32(const float (&g)[32]) {
+  float hi[11], lo[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    hi[i] = max3_nan(g[3 * i], g[3 * i + 1], g[3 * i + 2]);
+    lo[i] = min3_nan(g[3 * i], g[3 * i + 1], g[3 * i + 2]);
+  }
+  hi[10] = max_nan(g[30], g[31]);
+  lo[10] = min_nan(g[30], g[31]);
+  const float h = max_nan(max3_nan(max3_nan(hi[0], hi[1], hi[2]), max3_nan(hi[3], hi[4], hi[5]),
+                                   max3_nan(hi[6], hi[7], hi[8])), max_nan(hi[9], hi[10]));
+  const float l = min_nan(min3_nan(min3_nan(lo[0], lo[1], lo[2]), min3_nan(lo[3], lo[4], lo[5]),
+                                   min3_nan(lo[6], lo[7], lo[8])), min_nan(lo[9], lo[10]));
+  return __float_as_uint(max_nan(h, -l)) & 0x7FFFFFFFu;
+}
 
-// Four codes from two paired converts -> their 24-bit group c0 | c1 << 6 | c2 << 12 | c3 << 18.
-__device__ __forceinline__ uint32_t pack4_pairs(uint32_t lo_pair, uint32_t hi_pair) {
-  return pack2(lo_pair) + 4096u * pack2(hi_pair);
+// Four values (already scaled by 2^-s) -> their E2M3 codes, one per byte (value i
+// in byte i): two paired converts joined into one 32-bit register.
+__device__ __forceinline__ uint32_t cvt_e2m3x4(float a0, float a1, float a2, float a3) {
+  uint32_t q;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e2m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(q)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return q;
+}
+
+// Four codes one per byte (c0 | c1 << 8 | c2 << 16 | c3 << 24) -> the 24-bit group
+// c0 | c1 << 6 | c2 << 12 | c3 << 18: per 16-bit half c + 256 c' - 192 c' = c + 64 c',
+// then lo + 65536 hi - 61440 hi = lo + 4096 hi.
+__device__ __forceinline__ uint32_t pack_codes4(uint32_t q) {
+  const uint32_t odd = __byte_perm(q, 0u, 0x4341u);   // c1 | c3 << 16
+  const uint32_t t = q - 192u * odd;
+  return t - 61440u * (t >> 16);
 }
 
 // Eight 24-bit groups (32 codes) -> the six little-endian words of their 24 bytes
@@ -62,9 +89,6 @@ __device__ __forceinline__ void pack_groups(const uint32_t (&grp)[8], uint32_t (
 
 // MXFP6 encoding of one 32-value block: returns the E8M0 code and the block's 24
 // code bytes as six little-endian words (the quantizer's rule, on fp32 values).
-// The code bits are assembled with multiply-adds of disjoint fields, which keeps
-// the integer ALU (also busy with the maxima and the converts) from being the
-// bottleneck.
 __device__ __forceinline__ uint32_t quant_block32(const float (&g)[32], uint32_t (&w)[6]) {
   const uint32_t amax = amax_bits32(g);
   if (amax >= 0x7F800000u) {  // Inf or NaN: E8M0 NaN, zero codes
@@ -75,11 +99,15 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&g)[32], uint32_t
   const int e = static_cast<int>(amax >> 23);
   const uint32_t sc = static_cast<uint32_t>(e > 2 ? e - 2 : 0);
   const float fac = __uint_as_float((254u - sc) << 23);  // 2^-s, exact
+  const uint64_t fac2 = f2_pack(fac, fac);
   uint32_t grp[8];   // 24-bit groups of four codes
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    grp[j] = pack4_pairs(cvt_e2m3x2(g[4 * j + 1] * fac, g[4 * j] * fac),
-                         cvt_e2m3x2(g[4 * j + 3] * fac, g[4 * j + 2] * fac));
+  for (int j = 0; j < 8; ++j) {
+    float t0, t1, t2, t3;   // the values times 2^-s (exact), two per packed multiply
+    f2_unpack(f2_mul(f2_pack(g[4 * j], g[4 * j + 1]), fac2), t0, t1);
+    f2_unpack(f2_mul(f2_pack(g[4 * j + 2], g[4 * j + 3]), fac2), t2, t3);
+    grp[j] = pack_codes4(cvt_e2m3x4(t0, t1, t2, t3));
+  }
   pack_groups(grp, w);
   return sc;
 }

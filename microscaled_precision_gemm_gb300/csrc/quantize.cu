@@ -108,12 +108,12 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_bf16_kernel(
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t v[4] = {raw[u][j].x, raw[u][j].y, raw[u][j].z, raw[u][j].w};
-          uint32_t p[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            p[i] = cvt_e2m3x2(__uint_as_float(v[i] & 0xFFFF0000u) * fac, __uint_as_float(v[i] << 16) * fac);
-          g[2 * j] = pack4_pairs(p[0], p[1]);
-          g[2 * j + 1] = pack4_pairs(p[2], p[3]);
+          g[2 * j] = pack_codes4(cvt_e2m3x4(__uint_as_float(v[0] << 16) * fac, __uint_as_float(v[0] & 0xFFFF0000u) * fac,
+                                            __uint_as_float(v[1] << 16) * fac, __uint_as_float(v[1] & 0xFFFF0000u) * fac));
+          g[2 * j + 1] = pack_codes4(cvt_e2m3x4(__uint_as_float(v[2] << 16) * fac,
+                                                __uint_as_float(v[2] & 0xFFFF0000u) * fac,
+                                                __uint_as_float(v[3] << 16) * fac,
+                                                __uint_as_float(v[3] & 0xFFFF0000u) * fac));
         }
         pack_groups(g, w);
       }
