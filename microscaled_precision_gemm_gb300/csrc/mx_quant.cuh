@@ -12,15 +12,10 @@
 
 namespace mxk {
 
-// Three- and two-input maxima / minima, NaN if any input is NaN (PTX max.NaN / min.NaN).
+// Three- and two-input maxima, NaN if any input is NaN (PTX max.NaN).
 __device__ __forceinline__ float max3_nan(float a, float b, float c) {
   float d;
   asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float min3_nan(float a, float b, float c) {
-  float d;
-  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 __device__ __forceinline__ float max_nan(float a, float b) {
@@ -28,30 +23,20 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
   return d;
 }
-__device__ __forceinline__ float min_nan(float a, float b) {
-  float d;
-  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-  return d;
-}
 
 // Block amax of 32 fp32 values as magnitude bits: +0 .. 0x7F7FFFFF finite, 0x7F800000
-// Inf, above that NaN (max.NaN returns the canonical NaN 0x7FFFFFFF). The largest
-// and the smallest value by three-input trees (32 -> 11 -> 4 -> 2 -> 1, no per-value
-// absolute value), then max(hi, -lo) with the sign bit cleared (signed zeros).
+// Inf, above that NaN (max.NaN returns the canonical NaN 0x7FFFFFFF). A tree of
+// three-input maxima of |v| (the absolute value folds into the max): 32 -> 11 -> 4 -> 1.
 __device__ __forceinline__ uint32_t amax_bits32(const float (&g)[32]) {
-  float hi[11], lo[11];
+  float m[11];
 #pragma unroll
-  for (int i = 0; i < 10; ++i) {
-    hi[i] = max3_nan(g[3 * i], g[3 * i + 1], g[3 * i + 2]);
-    lo[i] = min3_nan(g[3 * i], g[3 * i + 1], g[3 * i + 2]);
-  }
-  hi[10] = max_nan(g[30], g[31]);
-  lo[10] = min_nan(g[30], g[31]);
-  const float h = max_nan(max3_nan(max3_nan(hi[0], hi[1], hi[2]), max3_nan(hi[3], hi[4], hi[5]),
-                                   max3_nan(hi[6], hi[7], hi[8])), max_nan(hi[9], hi[10]));
-  const float l = min_nan(min3_nan(min3_nan(lo[0], lo[1], lo[2]), min3_nan(lo[3], lo[4], lo[5]),
-                                   min3_nan(lo[6], lo[7], lo[8])), min_nan(lo[9], lo[10]));
-  return __float_as_uint(max_nan(h, -l)) & 0x7FFFFFFFu;
+  for (int i = 0; i < 10; ++i) m[i] = max3_nan(fabsf(g[3 * i]), fabsf(g[3 * i + 1]), fabsf(g[3 * i + 2]));
+  m[10] = max_nan(fabsf(g[30]), fabsf(g[31]));
+  const float n0 = max3_nan(m[0], m[1], m[2]);
+  const float n1 = max3_nan(m[3], m[4], m[5]);
+  const float n2 = max3_nan(m[6], m[7], m[8]);
+  const float n3 = max_nan(m[9], m[10]);
+  return __float_as_uint(max_nan(max3_nan(n0, n1, n2), n3));
 }
 
 // Four values (already scaled by 2^-s) -> their E2M3 codes, one per byte (value i

@@ -106,14 +106,16 @@ __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_
     }
     const uint32_t xw[16] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y, cur[1].z, cur[1].w,
                              cur[2].x, cur[2].y, cur[2].z, cur[2].w, cur[3].x, cur[3].y, cur[3].z, cur[3].w};
-    // four interleaved partial sums keep the dependent chain 8 deep
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    // four interleaved partial sums (two packed pairs) keep the dependent chain 8 deep
+    uint64_t s2[2] = {0ull, 0ull};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float a = bf16_lo(xw[i]), b = bf16_hi(xw[i]);
-      s4[i & 3] = fmaf(a, a, s4[i & 3]);
-      s4[i & 3] = fmaf(b, b, s4[i & 3]);
+      const uint64_t xp = f2_pack(bf16_lo(xw[i]), bf16_hi(xw[i]));
+      s2[i & 1] = f2_fma(xp, xp, s2[i & 1]);
     }
+    float s4[4];
+    f2_unpack(s2[0], s4[0], s4[1]);
+    f2_unpack(s2[1], s4[2], s4[3]);
     float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -126,10 +128,12 @@ __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_
     uint32_t sc = 0;
     if (active) {
       float y[32];
+      const uint64_t rstd2 = f2_pack(rstd, rstd);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        y[2 * i] = fmaf(bf16_lo(xw[i]) * rstd, opp[2 * i], bf16_lo(sh[i]));
-        y[2 * i + 1] = fmaf(bf16_hi(xw[i]) * rstd, opp[2 * i + 1], bf16_hi(sh[i]));
+        const uint64_t xr = f2_mul(f2_pack(bf16_lo(xw[i]), bf16_hi(xw[i])), rstd2);
+        f2_unpack(f2_fma(xr, f2_pack(opp[2 * i], opp[2 * i + 1]), f2_pack(bf16_lo(sh[i]), bf16_hi(sh[i]))),
+                  y[2 * i], y[2 * i + 1]);
       }
       if constexpr (DBG) {
         float4* d = reinterpret_cast<float4*>(dbg + static_cast<int64_t>(row) * k + kb * kBlock);

@@ -7,8 +7,8 @@
 // v * 2^-s to the nearest E2M3 value, ties to even, saturating at +-7.5.
 //
 // HBM-bound: 2 bytes in, 0.75 + 1/32 bytes out per element. One lane owns one
-// 32-element block, so the amax is thread-local and the per-element work is the
-// scale multiply, the paired convert and 32-bit packing.
+// 32-element block, so the amax is thread-local; the lane widens its BF16 values to
+// fp32 (exact) and runs the block encoder the GEMM epilogues use.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -54,12 +54,11 @@ static FastDiv make_fast_div(uint32_t d) {
 }
 
 // One lane quantizes one 32-element block: 64 contiguous input bytes (four
-// 16-byte loads), a thread-local amax, sixteen paired E2M3 conversions, 24
-// packed code bytes. A warp owns 32 consecutive blocks of the flattened
+// 16-byte loads), a thread-local amax, the E2M3 conversions, 24 packed code bytes. A warp owns 32 consecutive blocks of the flattened
 // [rows][K/32] block grid, so its 768 code bytes are contiguous in the packed
 // output; they are staged in shared memory and written as 16-byte stores. Four
 // consecutive lanes (4 K-blocks of one row) form one 32-bit tiled scale word.
-__global__ void __launch_bounds__(kQuantThreads) quantize_bf16_kernel(
+__global__ void __launch_bounds__(kQuantThreads, 5) quantize_bf16_kernel(
     const uint16_t* __restrict__ x, int rows, int k, int64_t ld_x, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, FastDiv blocks_per_row, uint32_t total_blocks) {
   const int lane = threadIdx.x & 31;
@@ -85,38 +84,20 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_bf16_kernel(
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      // |v| ordering of BF16 equals unsigned ordering of (bits & 0x7FFF); NaN/Inf sort last.
-      uint32_t m2 = 0;
+      // BF16 -> fp32 is exact, so the fp32 block encoder gives the BF16 rule's result
+      // (amax, scale, codes; NaN/Inf blocks included)
+      float f[32];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        m2 = __vmaxu2(m2, raw[u][j].x & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, raw[u][j].y & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, raw[u][j].z & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, raw[u][j].w & 0x7FFF7FFFu);
-      }
-      const uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
-      uint32_t sc, w[6];
-      if (amax >= 0x7F80u) {  // Inf or NaN in the block: E8M0 NaN, zero codes
-        sc = 0xFFu;
+        const uint32_t v[4] = {raw[u][j].x, raw[u][j].y, raw[u][j].z, raw[u][j].w};
 #pragma unroll
-        for (int i = 0; i < 6; ++i) w[i] = 0;
-      } else {
-        const uint32_t e = amax >> 7;              // biased exponent of amax (0 if subnormal)
-        sc = e > 2 ? e - 2 : 0;                    // E8M0 code = max(floor(log2 amax) - 2, -127) + 127
-        const float fac = __uint_as_float((254u - sc) << 23);  // 2^-s, exact
-        uint32_t g[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t v[4] = {raw[u][j].x, raw[u][j].y, raw[u][j].z, raw[u][j].w};
-          g[2 * j] = pack_codes4(cvt_e2m3x4(__uint_as_float(v[0] << 16) * fac, __uint_as_float(v[0] & 0xFFFF0000u) * fac,
-                                            __uint_as_float(v[1] << 16) * fac, __uint_as_float(v[1] & 0xFFFF0000u) * fac));
-          g[2 * j + 1] = pack_codes4(cvt_e2m3x4(__uint_as_float(v[2] << 16) * fac,
-                                                __uint_as_float(v[2] & 0xFFFF0000u) * fac,
-                                                __uint_as_float(v[3] << 16) * fac,
-                                                __uint_as_float(v[3] & 0xFFFF0000u) * fac));
+        for (int i = 0; i < 4; ++i) {
+          f[8 * j + 2 * i] = __uint_as_float(v[i] << 16);
+          f[8 * j + 2 * i + 1] = __uint_as_float(v[i] & 0xFFFF0000u);
         }
-        pack_groups(g, w);
       }
+      uint32_t w[6];
+      const uint32_t sc = quant_block32(f, w);
       uint2* s2 = reinterpret_cast<uint2*>(&st[u][6 * lane]);
       s2[0] = make_uint2(w[0], w[1]);
       s2[1] = make_uint2(w[2], w[3]);
