@@ -83,11 +83,14 @@ S_QKV = "QKV+gate GEMM+bias+BF16"
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the current kernels, keyed by (config, kernel); None where no
 # capture of the current kernel exists. Source summaries live in profiles/.
-# Written by hand from profiles/*_full_mlp.md (ncu on the full DiT MLP block).
+# Written by hand from profiles/*_full_mlp.md and profiles/*_dit_block_swiglu.md.
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", "K1 quantize"): 125852416 + 22633728,
-    ("full_mlp", "K3 up GEMM+GELU+requant"): 80900096 + 148366080,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 237485312 + 105883392,
+    ("full_mlp", "K1 quantize"): 125857536 + 20701696,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 80957184 + 148376832,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 236790528 + 109019648,
+    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125873408 + 21330176,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89982976 + 102271488,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 277337344 + 104732928,
 }
 
 

@@ -21,7 +21,6 @@
 namespace mxk {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 1;   // blocks per lane per iteration (4 x 16-byte loads in flight)
 
 __device__ __forceinline__ uint4 ld_nc(const void* p) {
   uint4 v;
@@ -54,74 +53,70 @@ static FastDiv make_fast_div(uint32_t d) {
 }
 
 // One lane quantizes one 32-element block: 64 contiguous input bytes (four
-// 16-byte loads), a thread-local amax, the E2M3 conversions, 24 packed code bytes. A warp owns 32 consecutive blocks of the flattened
-// [rows][K/32] block grid, so its 768 code bytes are contiguous in the packed
-// output; they are staged in shared memory and written as 16-byte stores. Four
-// consecutive lanes (4 K-blocks of one row) form one 32-bit tiled scale word.
-__global__ void __launch_bounds__(kQuantThreads, 5) quantize_bf16_kernel(
+// 16-byte loads), a thread-local amax, the E2M3 conversions, 24 packed code bytes.
+// A warp owns 32 consecutive blocks of the flattened [rows][K/32] block grid, so
+// its 768 code bytes are contiguous in the packed output; they are staged in
+// shared memory and written as 16-byte stores. Four consecutive lanes (4 K-blocks
+// of one row) form one 32-bit tiled scale word. The loads of the lane's next block
+// are issued before the current one is encoded.
+__global__ void __launch_bounds__(kQuantThreads, 4) quantize_bf16_kernel(
     const uint16_t* __restrict__ x, int rows, int k, int64_t ld_x, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, FastDiv blocks_per_row, uint32_t total_blocks) {
   const int lane = threadIdx.x & 31;
   const uint32_t warp_global = (blockIdx.x * kQuantThreads + threadIdx.x) / 32;
-  const uint32_t warps_total = gridDim.x * kQuantThreads / 32;
-  __shared__ __align__(16) uint32_t stage[kQuantThreads / 32][kQuantUnroll][192];
-  uint32_t(*st)[192] = stage[threadIdx.x / 32];
+  const uint32_t stride = gridDim.x * kQuantThreads;   // blocks per grid-wide step
+  __shared__ __align__(16) uint32_t stage[kQuantThreads / 32][192];
+  uint32_t* st = stage[threadIdx.x / 32];
 
-  for (uint32_t base = warp_global * 32 * kQuantUnroll; base < total_blocks;
-       base += warps_total * 32 * kQuantUnroll) {
-    uint4 raw[kQuantUnroll][4];
-    uint32_t row[kQuantUnroll], kb[kQuantUnroll];
-    bool valid[kQuantUnroll];
+  auto load_block = [&](uint32_t b, uint4 (&v)[4]) {
+    const uint32_t r = fast_div(b, blocks_per_row);
+    const uint16_t* src = x + static_cast<int64_t>(r) * ld_x + (b - r * blocks_per_row.d) * 32;
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t b = base + 32 * u + lane;
-      valid[u] = b < total_blocks;
-      row[u] = fast_div(b, blocks_per_row);
-      kb[u] = b - row[u] * blocks_per_row.d;
-      const uint16_t* src = x + static_cast<int64_t>(row[u]) * ld_x + kb[u] * 32;
+    for (int j = 0; j < 4; ++j) v[j] = b < total_blocks ? ld_nc(src + 8 * j) : make_uint4(0, 0, 0, 0);
+  };
+  uint4 next[4];
+  load_block(warp_global * 32 + lane, next);
+  for (uint32_t base = warp_global * 32; base < total_blocks; base += stride) {
+    const uint32_t b = base + lane;
+    const bool valid = b < total_blocks;
+    const uint32_t row = fast_div(b, blocks_per_row);
+    const uint32_t kb = b - row * blocks_per_row.d;
+    uint4 raw[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) raw[u][j] = valid[u] ? ld_nc(src + 8 * j) : make_uint4(0, 0, 0, 0);
-    }
+    for (int j = 0; j < 4; ++j) raw[j] = next[j];
+    load_block(b + stride, next);
+    // BF16 -> fp32 is exact, so the fp32 block encoder gives the BF16 rule's result
+    // (amax, scale, codes; NaN/Inf blocks included)
+    float f[32];
 #pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      // BF16 -> fp32 is exact, so the fp32 block encoder gives the BF16 rule's result
-      // (amax, scale, codes; NaN/Inf blocks included)
-      float f[32];
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t v[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t v[4] = {raw[u][j].x, raw[u][j].y, raw[u][j].z, raw[u][j].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          f[8 * j + 2 * i] = __uint_as_float(v[i] << 16);
-          f[8 * j + 2 * i + 1] = __uint_as_float(v[i] & 0xFFFF0000u);
-        }
+      for (int i = 0; i < 4; ++i) {
+        f[8 * j + 2 * i] = __uint_as_float(v[i] << 16);
+        f[8 * j + 2 * i + 1] = __uint_as_float(v[i] & 0xFFFF0000u);
       }
-      uint32_t w[6];
-      const uint32_t sc = quant_block32(f, w);
-      uint2* s2 = reinterpret_cast<uint2*>(&st[u][6 * lane]);
-      s2[0] = make_uint2(w[0], w[1]);
-      s2[1] = make_uint2(w[2], w[3]);
-      s2[2] = make_uint2(w[4], w[5]);
-      // four consecutive blocks (K-blocks 4c..4c+3 of one row) -> one tiled scale word
-      const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
-      const uint32_t s2b = __shfl_down_sync(0xffffffffu, sc, 2);
-      const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
-      if (valid[u] && (lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(scales + scale_word_offset(row[u], kb[u] / 4, k)) =
-            sc | (s1 << 8) | (s2b << 16) | (s3 << 24);
     }
+    uint32_t w[6];
+    const uint32_t sc = quant_block32(f, w);
+    uint2* s2 = reinterpret_cast<uint2*>(&st[6 * lane]);
+    s2[0] = make_uint2(w[0], w[1]);
+    s2[1] = make_uint2(w[2], w[3]);
+    s2[2] = make_uint2(w[4], w[5]);
+    // four consecutive blocks (K-blocks 4c..4c+3 of one row) -> one tiled scale word
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
+    const uint32_t s2b = __shfl_down_sync(0xffffffffu, sc, 2);
+    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
+    if (valid && (lane & 3) == 0)
+      *reinterpret_cast<uint32_t*>(scales + scale_word_offset(row, kb / 4, k)) =
+          sc | (s1 << 8) | (s2b << 16) | (s3 << 24);
     __syncwarp();
     // the warp's blocks are consecutive: their codes are 24 * 32 contiguous bytes
-#pragma unroll
-    for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t b0 = base + 32 * u;
-      if (b0 >= total_blocks) break;
-      const uint32_t nblk = min(32u, total_blocks - b0);  // a multiple of 4
-      const uint32_t chunks = nblk * 24 / 16;
-      uint8_t* dst = codes + static_cast<int64_t>(b0) * 24;
-      const uint4* src = reinterpret_cast<const uint4*>(st[u]);
-      for (uint32_t c = lane; c < chunks; c += 32) reinterpret_cast<uint4*>(dst)[c] = src[c];
-    }
+    const uint32_t nblk = min(32u, total_blocks - base);  // a multiple of 4
+    const uint32_t chunks = nblk * 24 / 16;
+    uint4* dst = reinterpret_cast<uint4*>(codes + static_cast<int64_t>(base) * 24);
+    const uint4* src = reinterpret_cast<const uint4*>(st);
+    for (uint32_t c = lane; c < chunks; c += 32) dst[c] = src[c];
     __syncwarp();
   }
 
@@ -140,7 +135,7 @@ cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t
                                  int num_sms, cudaStream_t stream) {
   const int64_t total_blocks = rows * (k / kBlock);
   if (total_blocks > (int64_t{1} << 32) - (int64_t{1} << 28)) return cudaErrorInvalidValue;  // host checks first
-  const int64_t warps_needed = (total_blocks + 32 * kQuantUnroll - 1) / (32 * kQuantUnroll);
+  const int64_t warps_needed = (total_blocks + 31) / 32;
   int64_t blocks = (warps_needed * 32 + kQuantThreads - 1) / kQuantThreads;
   const int64_t pad_blocks = ((pad_rows(rows) - rows) * (k / kAtomK) + kQuantThreads - 1) / kQuantThreads;
   if (blocks < pad_blocks) blocks = pad_blocks;
