@@ -591,6 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // both CTAs' barriers and tensor memory exist before either touches the other's
   cluster_sync();
   tc_fence_after();
+  // the prologue above overlapped the previous kernel's tail; operands, bias and
+  // outputs are touched only once it has completed
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
   const uint32_t tmem = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
 
@@ -694,11 +698,15 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the kernel may start while the previous one in
+  // the stream finishes; it waits (griddepcontrol.wait) before touching memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -716,6 +724,7 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   }
   if (clusters > pairs) clusters = static_cast<int>(pairs);
   cfg.gridDim = dim3(kPair * clusters, 1, 1);
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, static_cast<const uint16_t*>(a.bias),
                          static_cast<const uint16_t*>(a.gate), static_cast<const uint16_t*>(a.residual), a.out,
                          static_cast<uint8_t*>(a.out_scales), a.debug_prequant, static_cast<int>(a.m),

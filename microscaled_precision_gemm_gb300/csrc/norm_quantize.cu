@@ -55,6 +55,11 @@ __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_
   __shared__ float partial[2][kNormMaxWarps];
   __shared__ __align__(16) uint32_t stage[kNormMaxWarps][192];
 
+  // programmatic dependent launch: let the next kernel be scheduled, and read the
+  // inputs / write the outputs only once the previous kernel has completed
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
+
   // this lane's 32 columns of the modulation: (1 + scale) in fp32, shift as BF16 pairs
   float opp[32];
   uint32_t sh[16];
@@ -205,10 +210,20 @@ cudaError_t launch_norm_modulate_quantize(const void* x, int64_t rows, int64_t k
   if (blocks > rows) blocks = rows;
   if (blocks < pad_blocks) blocks = pad_blocks;
   if (blocks < 1) blocks = 1;
-  kern<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint16_t*>(x), static_cast<int>(rows), static_cast<int>(k), ld_x,
-      static_cast<const uint16_t*>(shift), static_cast<const uint16_t*>(scale), eps, static_cast<uint8_t*>(codes),
-      static_cast<uint8_t*>(scales), dbg);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint16_t*>(x), static_cast<int>(rows),
+                                     static_cast<int>(k), ld_x, static_cast<const uint16_t*>(shift),
+                                     static_cast<const uint16_t*>(scale), eps, static_cast<uint8_t*>(codes),
+                                     static_cast<uint8_t*>(scales), dbg);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -78,6 +78,15 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their memory is visible (a no-op without such a dependency) ...
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// ... and let the grids that depend on this one be scheduled (they still wait for
+// this grid's completion before touching memory).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

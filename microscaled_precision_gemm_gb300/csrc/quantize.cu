@@ -68,6 +68,11 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_bf16_kernel(
   __shared__ __align__(16) uint32_t stage[kQuantThreads / 32][192];
   uint32_t* st = stage[threadIdx.x / 32];
 
+  // programmatic dependent launch: let the next kernel be scheduled, and read x /
+  // write the outputs only once the previous kernel has completed
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();
+
   auto load_block = [&](uint32_t b, uint4 (&v)[4]) {
     const uint32_t r = fast_div(b, blocks_per_row);
     const uint16_t* src = x + static_cast<int64_t>(r) * ld_x + (b - r * blocks_per_row.d) * 32;
@@ -152,10 +157,20 @@ cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t
   const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  quantize_bf16_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(x), static_cast<int>(rows), static_cast<int>(k), ld_x,
-      static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales),
-      make_fast_div(static_cast<uint32_t>(k / kBlock)), static_cast<uint32_t>(total_blocks));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kQuantThreads, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_bf16_kernel, static_cast<const uint16_t*>(x), static_cast<int>(rows),
+                                     static_cast<int>(k), ld_x, static_cast<uint8_t*>(codes),
+                                     static_cast<uint8_t*>(scales), make_fast_div(static_cast<uint32_t>(k / kBlock)),
+                                     static_cast<uint32_t>(total_blocks));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

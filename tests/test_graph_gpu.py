@@ -1,0 +1,116 @@
+"""The MLP entry points under CUDA graph capture.
+
+A step of the hot path is a fixed sequence of launches on one stream, so it can
+be captured once and replayed: every replay must equal an eager call on the
+same inputs bit for bit (the kernels are deterministic: no atomics, fixed
+reduction orders). Inputs are refreshed between replays by copying into the
+captured buffers, as a serving loop would. The first eager call on a device
+fills the library's per-device caches (kernel attributes, occupancy); capture
+comes after it.
+"""
+
+import pytest
+
+import synth
+from mxutil import bf16_to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _capture(fn):
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()   # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _replays_match(lib, fn_into, make_input, x_buf, y_buf, n=3):
+    """fn_into(x, y) runs the path from x into y; compares graph replays with eager calls."""
+    import torch
+
+    g = _capture(lambda: fn_into(x_buf, y_buf))
+    for i in range(n):
+        x_new = make_input(100 + i)
+        x_buf.copy_(x_new)
+        g.replay()
+        torch.cuda.synchronize()
+        y_eager = torch.empty_like(y_buf)
+        fn_into(x_new, y_eager)
+        torch.cuda.synchronize()
+        assert torch.equal(y_buf, y_eager), f"replay {i} differs from the eager call"
+    assert lib.mx_device_error() == 0
+
+
+def test_mlp_graph_replay(lib):
+    import torch
+
+    w = synth.full_mlp(M=384, d=512, ff=1024)
+    w1 = lib.mx_quantize(bf16_to_device(w["w1"]))
+    w2 = lib.mx_quantize(bf16_to_device(w["w2"]))
+    b1, b2 = bf16_to_device(w["b1"]), bf16_to_device(w["b2"])
+    ws = torch.empty(lib.mx_mlp_workspace_bytes(384, 512, 1024), dtype=torch.uint8, device="cuda")
+    x = bf16_to_device(w["x"])
+    y = torch.empty_like(x)
+
+    def run(xi, yi):
+        lib.mx_mlp(xi, w1, b1, w2, b2, y=yi, workspace=ws)
+
+    run(x, y)   # fills the per-device caches outside capture
+    _replays_match(lib, run, lambda s: bf16_to_device(synth.full_mlp(seed=s, M=384, d=512, ff=1024)["x"]), x, y)
+
+
+def test_dit_block_graph_replay_in_place(lib):
+    """The SwiGLU DiT sub-block updating its input in place, captured and replayed."""
+    import torch
+
+    w = synth.dit_block(M=300, d=256, ff=384, activation="swiglu")
+    wup = lib.mx_quantize(bf16_to_device(w["w_up"]))
+    w2 = lib.mx_quantize(bf16_to_device(w["w2"]))
+    vec = {k: bf16_to_device(w[k]) for k in ("shift", "scale", "gate", "b_up", "b2")}
+    ws = torch.empty(lib.mx_mlp_workspace_bytes(300, 256, 384), dtype=torch.uint8, device="cuda")
+
+    def run(xi, yi):
+        lib.mx_dit_mlp_block(xi, vec["shift"], vec["scale"], vec["gate"], wup, vec["b_up"], w2, vec["b2"],
+                             eps=w["eps"], activation=lib.MX_ACT_SWIGLU, y=yi, workspace=ws)
+
+    x = bf16_to_device(w["x"])
+    run(x.clone(), torch.empty_like(x))
+    # in place: the captured graph reads x and overwrites it with x + gate * MLP(x)
+    g = _capture(lambda: run(x, x))
+    for i in range(3):
+        x_new = bf16_to_device(synth.dit_block(seed=50 + i, M=300, d=256, ff=384, activation="swiglu")["x"])
+        x.copy_(x_new)
+        g.replay()
+        torch.cuda.synchronize()
+        y_eager = torch.empty_like(x)
+        run(x_new, y_eager)
+        torch.cuda.synchronize()
+        assert torch.equal(x, y_eager), f"in-place replay {i} differs from the eager call"
+        assert not torch.equal(x, x_new)
+    assert lib.mx_device_error() == 0
+
+
+def test_quantize_then_gemm_graph_many_replays(lib):
+    """K1 + a BF16-epilogue GEMM captured once, replayed 20 times on fresh inputs."""
+    import torch
+
+    w = synth.pr1(M=256, K=512, N=512)
+    wq = lib.mx_quantize(bf16_to_device(w["w"]))
+    b = bf16_to_device(w["b"])
+    x = bf16_to_device(w["x"])
+    xq = lib.mx_quantize(x)
+    y = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
+
+    def run(xi, yi):
+        q = lib.mx_quantize(xi, out=xq) if xi is x else lib.mx_quantize(xi)
+        lib.mx_gemm(q, wq, b, lib.MX_EPI_BIAS_BF16, out=yi)
+
+    _replays_match(lib, run, lambda s: bf16_to_device(synth.pr1(seed=s, M=256, K=512, N=512)["x"]), x, y, n=20)
