@@ -417,6 +417,28 @@ def run_gpu(args) -> dict | None:
                 "unit": "GB/s", "frac": stage_report[dom]["gbs"] / peaks["hbm_gbs"],
                 "traffic": NCU_TRAFFIC_BYTES.get((args.config, dom))}
 
+    # the quantizer alone, back to back over the copies with no event between launches
+    # (inside a step its event window also holds the launch gap after the previous kernel)
+    k1_isolated = None
+    k1_name = S_K1 if S_K1 in stage_names else (S_K1N if S_K1N in stage_names else None)
+    if k1_name is not None:
+        k1_fns = [dict(c.stages(mx))[k1_name] for c in copies]
+        for i in range(4):
+            k1_fns[i % len(k1_fns)]()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        n_iso = 50
+        a.record(stream)
+        for i in range(n_iso):
+            k1_fns[i % len(k1_fns)]()
+        b.record(stream)
+        torch.cuda.synchronize()
+        iso_ms = a.elapsed_time(b) / n_iso
+        k1_isolated = {"kernel": k1_name, "us": iso_ms * 1e3,
+                       "gbs": work[k1_name]["bytes"] / (iso_ms * 1e-3) / 1e9,
+                       "launches": n_iso, "note": "back-to-back launches over the input copies, outside the timed region"}
+
     # end to end through the public API with host buffers (rank 0's view; all ranks run it)
     e2e = run_e2e(mx, copies, cfg, args, world)
 
@@ -452,6 +474,9 @@ def run_gpu(args) -> dict | None:
     if k1 is not None:
         line["quantize_gbs"] = stage_report[k1]["gbs"]
         line["quantize_frac_hbm"] = stage_report[k1]["gbs"] / peaks["hbm_gbs"]
+        if k1_isolated is not None:
+            k1_isolated["frac_hbm"] = k1_isolated["gbs"] / peaks["hbm_gbs"]
+            line["quantize_isolated"] = k1_isolated
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_budget)
     return line
@@ -626,21 +651,30 @@ class OracleWorkload:
         return 2.0 * len(rows) * d * ff
 
 
+def _grow_sample(ow, rng, M: int, target_s: float):
+    """Doubles the row sample (from 16) until one oracle step on it takes at least
+    target_s / 2 (or covers all M rows); returns (rows, seconds, flops) of that step.
+    A step has a fixed cost (the oracle dequantizes its weights every time), so a
+    small calibration sample would over-estimate the cost of a row."""
+    n = 16
+    while True:
+        rows = np.sort(rng.choice(M, size=min(n, M), replace=False))
+        t0 = time.perf_counter()
+        flops = ow.step(rows)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 2 or n >= M:
+            return rows, dt, flops
+        n *= 2
+
+
 def cpu_baseline(cfg: dict, budget_s: float) -> dict:
     """The oracle, as it stands, on a bounded row sample of the same workload."""
     ow = OracleWorkload(cfg, sample_rows=64)
     rng = np.random.default_rng(0)
     M = cfg["M"]
-    # warm the thread pools, calibrate on 32 rows, then size the sample to about budget_s of CPU work
-    ow.step(rng.integers(0, M, 8))
-    t0 = time.perf_counter()
-    ow.step(rng.integers(0, M, 32))
-    per_row = (time.perf_counter() - t0) / 32
-    n = int(max(8, min(M, budget_s / max(per_row, 1e-6))))
-    rows = np.sort(rng.choice(M, size=n, replace=False))
-    t0 = time.perf_counter()
-    flops = ow.step(rows)
-    dt = time.perf_counter() - t0
+    ow.step(rng.integers(0, M, 8))   # warm the thread pools
+    rows, dt, flops = _grow_sample(ow, rng, M, budget_s)
+    n = len(rows)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
             "seconds": dt, "sample": f"{n} of {M} token rows of the same workload (weights quantized by the "
                                      f"oracle beforehand, untimed); fp64 numpy + brute-force E2M3 search"}
@@ -654,11 +688,9 @@ def run_reference(args) -> dict | None:
     ow = OracleWorkload(cfg, sample_rows=64)
     rng = np.random.default_rng(1)
     M = cfg["M"]
-    t0 = time.perf_counter()
-    ow.step(rng.integers(0, M, 4))
-    per_row = (time.perf_counter() - t0) / 4
+    ow.step(rng.integers(0, M, 4))   # warm the thread pools
     total_budget = args.cpu_budget * 4
-    rows_per_step = int(max(1, min(M, total_budget / max(per_row, 1e-6) / max(1, args.steps + args.warmup))))
+    rows_per_step = len(_grow_sample(ow, rng, M, total_budget / max(1, args.steps + args.warmup))[0])
     for _ in range(args.warmup):
         ow.step(rng.integers(0, M, rows_per_step))
     flops = 0.0

@@ -82,3 +82,12 @@ def test_outlier_heavy_wide_mlp(lib):
     """M=20480, d=4096, ff=16384, Student-t activations, hot channels, zero blocks."""
     w = synth.outlier_mlp()
     _run(lib, w, sample_rows(20480, n_random=128))
+
+
+@pytest.mark.slow
+def test_ragged_token_count_at_dit_width(lib):
+    """M=4133 tokens (not a multiple of the 128-row tile or the 256-row pair tile) at
+    d=3072, ff=12288: the last pair tile is partly past M, its second CTA entirely."""
+    w = synth.full_mlp(M=4133, d=3072, ff=12288)
+    rows = np.unique(np.concatenate([sample_rows(4133, n_random=64), np.arange(4096, 4133)]))
+    _run(lib, w, rows)
