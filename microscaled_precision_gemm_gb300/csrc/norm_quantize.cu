@@ -15,7 +15,8 @@
 // 32 w + l for every row, so its 32 modulation pairs (1 + scale, shift) stay in
 // registers for the whole kernel. Per row: each lane's sum of squares, a warp
 // tree, one barrier to combine the warps' partials (double-buffered slots), then
-// y, its amax and the paired E2M3 conversions; the next row is already in flight.
+// y, its amax and the paired E2M3 conversions; the next row is already in flight,
+// loaded into the other of two register buffers that alternate from row to row.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -92,23 +93,8 @@ __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_
     }
   }
 
-  uint4 cur[4] = {};
-  int row = blockIdx.x;
-  if (row < rows && active) {
-    const uint16_t* src = x + static_cast<int64_t>(row) * ld_x + kb * kBlock;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) cur[j] = ld_nc_v4(src + 8 * j);
-  }
   int parity = 0;
-  for (; row < rows; row += gridDim.x) {
-    // the next row's block is in flight while this one is reduced and quantized
-    const int nrow = row + gridDim.x;
-    uint4 nxt[4] = {};
-    if (nrow < rows && active) {
-      const uint16_t* src = x + static_cast<int64_t>(nrow) * ld_x + kb * kBlock;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) nxt[j] = ld_nc_v4(src + 8 * j);
-    }
+  auto process_row = [&](int row, const uint4 (&cur)[4]) {
     const uint32_t xw[16] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y, cur[1].z, cur[1].w,
                              cur[2].x, cur[2].y, cur[2].z, cur[2].w, cur[3].x, cur[3].y, cur[3].z, cur[3].w};
     // four interleaved partial sums (two packed pairs) keep the dependent chain 8 deep
@@ -169,9 +155,29 @@ __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_
       for (int c = lane; c < chunks; c += 32) dst[c] = src[c];
     }
     __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
     parity ^= 1;
+  };
+  auto load_row = [&](int r, uint4 (&v)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = make_uint4(0, 0, 0, 0);
+    if (r < rows && active) {
+      const uint16_t* src = x + static_cast<int64_t>(r) * ld_x + kb * kBlock;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = ld_nc_v4(src + 8 * j);
+    }
+  };
+  // two row buffers in turn: the next row's block is in flight while one row is
+  // reduced and quantized, without copying registers between iterations
+  const int step = gridDim.x;
+  uint4 buf0[4], buf1[4];
+  int row = blockIdx.x;
+  load_row(row, buf0);
+  for (; row < rows; row += 2 * step) {
+    load_row(row + step, buf1);
+    process_row(row, buf0);
+    if (row + step >= rows) break;
+    load_row(row + 2 * step, buf0);
+    process_row(row + step, buf1);
   }
 
   // Zero the scale words of the padding rows (rows .. rows rounded up to 128).
