@@ -86,12 +86,12 @@ S_QKV = "QKV+gate GEMM+bias+BF16"
 # capture of the current kernel exists. Source summaries live in profiles/.
 # Written by hand from profiles/*_full_mlp.md and profiles/*_dit_block_swiglu.md.
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", "K1 quantize"): 125857536 + 20701696,
-    ("full_mlp", "K3 up GEMM+GELU+requant"): 80957184 + 148376832,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 236790528 + 109019648,
-    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125873408 + 21330176,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89982976 + 102271488,
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 277337344 + 104732928,
+    ("full_mlp", "K1 quantize"): 125857280 + 19578880,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 80854528 + 148284928,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 237154048 + 108443136,
+    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125881856 + 21643776,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89757184 + 102222080,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 277535488 + 104813568,
 }
 
 
