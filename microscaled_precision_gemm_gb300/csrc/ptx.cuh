@@ -1,7 +1,9 @@
-// Inline-PTX wrappers for sm_103a: mbarriers, TMA / bulk copies, tcgen05
-// (tensor memory, block-scaled MMA, scale-factor copies) and the E2M3 convert.
-// Every instruction here is documented in the public PTX ISA (tcgen05, cp.async.bulk,
-// mbarrier and cvt chapters).
+// Inline-PTX wrappers for sm_103a: mbarriers, TMA tensor loads, tcgen05 (tensor
+// memory, block-scaled pair MMA, scale-factor copies), clusters, programmatic
+// dependent launch, conversions and packed fp32 pairs. Every instruction here is
+// documented in the public PTX ISA (tcgen05, cp.async.bulk.tensor, mbarrier,
+// griddepcontrol, cvt and f32x2 arithmetic chapters). The E2M3 convert and the
+// NaN-propagating maxima live with the block encoder (mx_quant.cuh).
 #pragma once
 
 #include <cstdint>
@@ -28,10 +30,6 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -66,11 +64,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
 // Relaxed arrive on a (possibly remote) mbarrier: a pure signal that orders no
 // memory operations, so it does not wait for this thread's earlier global stores
 // to become visible the way a release would.
@@ -93,32 +86,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// ------------------------------------------------------------------ TMA / bulk copies
+// ------------------------------------------------------------------ TMA tensor loads
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// 2-D tiled load of box {x .. x+box0, y .. y+box1} into shared memory; completes
-// its bytes on `bar`. x is the innermost (element) coordinate.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
-                                            int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-
-// As tma_load_2d, but the box lands at the same shared offset in every CTA of
-// `cta_mask` in this cluster, completing its bytes on each one's `bar` (same offset).
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
-                                                      int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
 }
 
 // Tiled loads into this CTA's shared memory whose bytes complete on an mbarrier
@@ -142,30 +113,7 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// Contiguous global -> shared copy (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // ------------------------------------------------------------------ tcgen05
-
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -173,40 +121,6 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-
-// As tc_commit, arriving on `bar` (same shared offset) in every CTA of `cta_mask`.
-__device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// Shared -> tensor memory copy of 32 rows x 128 bits, replicated into all four
-// 32-lane groups (the layout the block-scaled MMA reads scale factors from).
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// D[tmem] (+)= A[smem] x B[smem]^T with per-32-element E8M0 scales read from tensor memory.
-__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
-      "}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
 }
 
 // Each thread of the warp reads 32 consecutive 32-bit columns of its own lane.
@@ -295,16 +209,28 @@ __device__ __forceinline__ void cluster_sync() {
 
 // ------------------------------------------------------------------ conversions
 
-// Two fp32 -> two E2M3 codes, round-to-nearest-even, saturating to +-7.5.
-// Result: low byte holds lo's code, high byte hi's code (6-bit codes in bits 5..0).
-__device__ __forceinline__ uint32_t cvt_e2m3x2(float hi, float lo) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+// 2^x and 1/x on the special-function unit (PTX ex2.approx / rcp.approx, ftz):
+// relative errors of a couple of ulp; 2^x of a large x is +inf and 1/inf is 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
-// 2^x and 1/x on the special-function unit (PTX ex2.approx / rcp.approx, ftz):
-// relative errors of a couple of ulp; 2^x of a large x is +inf and 1/inf is 0.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Two fp32 -> packed bf16x2 (round-to-nearest-even); lo in the low half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float hi, float lo) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+
 // ------------------------------------------------------------------ packed fp32 pairs
 // Blackwell's two-wide fp32 arithmetic: one instruction rounds both lanes exactly
 // as the scalar add/mul/fma (.rn, no flush) would. A pair lives in a 64-bit register.
@@ -331,25 +257,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
-}
-
-__device__ __forceinline__ float ex2_approx(float x) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-__device__ __forceinline__ float rcp_approx(float x) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-// Two fp32 -> packed bf16x2 (round-to-nearest-even); lo in the low half.
-__device__ __forceinline__ uint32_t cvt_bf16x2(float hi, float lo) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
 }
 
 }  // namespace mxk
