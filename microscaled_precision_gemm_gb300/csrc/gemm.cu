@@ -43,6 +43,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cstring>
@@ -688,14 +689,15 @@ template <int EPI, bool DBG>
 static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                                    const CUtensorMap& tsb, const GemmArgs& a, int64_t pairs, cudaStream_t stream) {
   auto kern = mx_gemm_kernel<EPI, DBG>;
-  static bool configured[64] = {};
+  // per-device caches, filled on a device's first call (any thread may fill them)
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
@@ -713,14 +715,14 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // as many CTA pairs as are co-resident (one CTA per SM), at most one per tile pair
-  static int max_clusters[64] = {};
-  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : 0;
+  static std::atomic<int> max_clusters[64];
+  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev].load(std::memory_order_relaxed) : 0;
   if (clusters == 0) {
     cfg.gridDim = dim3(kPair * 64, 1, 1);
     e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
     if (e != cudaSuccess) return e;
     if (clusters < 1) return cudaErrorLaunchOutOfResources;
-    if (dev >= 0 && dev < 64) max_clusters[dev] = clusters;
+    if (dev >= 0 && dev < 64) max_clusters[dev].store(clusters, std::memory_order_relaxed);
   }
   if (clusters > pairs) clusters = static_cast<int>(pairs);
   cfg.gridDim = dim3(kPair * clusters, 1, 1);

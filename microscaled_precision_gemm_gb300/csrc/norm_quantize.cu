@@ -19,6 +19,7 @@
 // loaded into the other of two register buffers that alternate from row to row.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -201,15 +202,15 @@ cudaError_t launch_norm_modulate_quantize(const void* x, int64_t rows, int64_t k
   const int threads = 32 * warps;
   auto kern = dbg != nullptr ? norm_modulate_quantize_kernel<true> : norm_modulate_quantize_kernel<false>;
   // as many CTAs as are resident at once (each walks rows with a grid stride)
-  static int resident[64][2][kNormMaxWarps + 1] = {};
+  static std::atomic<int> resident[64][2][kNormMaxWarps + 1];   // any thread may fill it
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   const int di = dbg != nullptr ? 1 : 0;
-  int per_sm = (dev >= 0 && dev < 64) ? resident[dev][di][warps] : 0;
+  int per_sm = (dev >= 0 && dev < 64) ? resident[dev][di][warps].load(std::memory_order_relaxed) : 0;
   if (per_sm == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
     if (e != cudaSuccess || per_sm < 1) per_sm = 1;
-    if (dev >= 0 && dev < 64) resident[dev][di][warps] = per_sm;
+    if (dev >= 0 && dev < 64) resident[dev][di][warps].store(per_sm, std::memory_order_relaxed);
   }
   int64_t blocks = static_cast<int64_t>(num_sms) * per_sm;
   const int64_t pad_blocks = ((pad_rows(rows) - rows) * (k / kAtomK) + threads - 1) / threads;

@@ -11,6 +11,7 @@
 // fp32 (exact) and runs the block encoder the GEMM epilogues use.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -145,14 +146,14 @@ cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t
   const int64_t pad_blocks = ((pad_rows(rows) - rows) * (k / kAtomK) + kQuantThreads - 1) / kQuantThreads;
   if (blocks < pad_blocks) blocks = pad_blocks;
   // every block resident at once (grid-stride), so no second partial wave
-  static int resident_per_sm[64] = {};
+  static std::atomic<int> resident_per_sm[64];   // per-device occupancy, any thread may fill it
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  int per_sm = (dev >= 0 && dev < 64) ? resident_per_sm[dev] : 0;
+  int per_sm = (dev >= 0 && dev < 64) ? resident_per_sm[dev].load(std::memory_order_relaxed) : 0;
   if (per_sm == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_bf16_kernel, kQuantThreads, 0);
     if (e != cudaSuccess || per_sm < 1) per_sm = 1;
-    if (dev >= 0 && dev < 64) resident_per_sm[dev] = per_sm;
+    if (dev >= 0 && dev < 64) resident_per_sm[dev].store(per_sm, std::memory_order_relaxed);
   }
   const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
   if (blocks > cap) blocks = cap;

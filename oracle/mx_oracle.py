@@ -125,7 +125,8 @@ def e8m0_value(code):
 def bf16_bits_to_f64(bits) -> np.ndarray:
     """BF16 bit patterns (uint16) -> exact fp64 values (BF16 is the top half of fp32)."""
     bits = np.asarray(bits, dtype=np.uint16)
-    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):   # NaN patterns widen to NaN; numpy warns about them
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def f32_to_f64(x) -> np.ndarray:
