@@ -220,3 +220,29 @@ def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pkg._build, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         pkg.load()
+
+
+def test_c_caller_compiles_links_and_runs(mx, tmp_path):
+    """include/mx.h is valid C11; a C program links the library and gets the same answers."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if cc is None or not os.path.isdir(cuda_inc):
+        pytest.skip("gcc or the CUDA headers are not available")
+    src = os.path.join(ROOT, "tests", "helpers", "c_abi_probe.c")
+    exe = str(tmp_path / "c_abi_probe")
+    lib_dir = os.path.dirname(mx.library_path())
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, src,
+                    "-o", exe, "-L", lib_dir, "-lmxfp6", "-Wl,-rpath," + lib_dir], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    got = dict(line.split(" ", 1) for line in out.strip().splitlines())
+    assert got["version"] == "100"
+    assert int(got["codes_bytes"]) == 128 * 192
+    assert int(got["scales_bytes"]) == 384 * 8
+    assert int(got["workspace_bytes"]) == mx.mx_mlp_workspace_bytes(256, 512, 1024)
+    assert int(got["bad_shape"]) == SHAPE
+    assert int(got["null_ptr"]) == INVALID
+    assert got["status_ok"] == "MX_OK"
+    assert got["layout_round_trip"] == "1"
