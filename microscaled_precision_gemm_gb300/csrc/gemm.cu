@@ -37,9 +37,12 @@
 //                 kEpiGateRes   bias, times a per-column gate, plus a BF16 residual,
 //                               BF16 store (an output projection with its gate and
 //                               residual add)
-// Every wait is bounded (2 s on the global timer); on expiry the kernel records an
-// error bit, drains its in-flight copies and MMAs (again bounded), frees tensor
-// memory and returns.
+// Every mbarrier wait is bounded (2 s on the global timer); on expiry the kernel
+// records an error bit, drains its in-flight copies and MMAs (again bounded), frees
+// tensor memory and returns. Launched with programmatic dependent launch: the
+// prologue (barriers, tensor memory, tensor-map prefetch) may overlap the previous
+// kernel in the stream, and griddepcontrol.wait holds every access to global
+// memory until that kernel has completed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
