@@ -176,3 +176,23 @@ def test_dit_down_projection_full_size(lib):
 
 def test_no_device_errors(lib):
     assert lib.mx_device_error() == 0
+
+
+def test_extreme_scale_exponents(lib):
+    """E8M0 scales over the whole range (codes 1..254) on both operands, paired so
+    that every product 2^(sa + sb - 254) stays inside fp32's normal range: K-block j
+    gives B a scale near a code drawn across 1..254 and A the complementary one, so
+    the tensor cores must apply the full scale range exactly (bias-free, BF16 store)."""
+    M, N, K = 256, 256, 512
+    rng = np.random.default_rng(11)
+    a = rng.integers(0, 64, size=(M, K)).astype(np.uint8)
+    b = rng.integers(0, 64, size=(N, K)).astype(np.uint8)
+    kb = K // 32
+    base_b = rng.permutation(np.linspace(4, 250, kb).round().astype(np.int64))
+    d = rng.integers(-6, 7, size=kb)                       # per-block size of the products
+    sb = base_b[None, :] + rng.integers(-3, 4, size=(N, kb))
+    sa = (254 + d - base_b)[None, :] + rng.integers(-3, 4, size=(M, kb))
+    assert sa.min() >= 1 and sa.max() <= 254 and sb.min() >= 1 and sb.max() <= 254
+    sa, sb = sa.astype(np.uint8), sb.astype(np.uint8)
+    y = _gemm_bf16(lib, mx_upload(a, sa), mx_upload(b, sb))
+    assert_gemm_close(y, O.gemm(a, sa, b, sb), "extreme scales")
