@@ -196,3 +196,33 @@ def test_extreme_scale_exponents(lib):
     sa, sb = sa.astype(np.uint8), sb.astype(np.uint8)
     y = _gemm_bf16(lib, mx_upload(a, sa), mx_upload(b, sb))
     assert_gemm_close(y, O.gemm(a, sa, b, sb), "extreme scales")
+
+
+def test_nan_scale_block_propagates(lib):
+    """A block whose E8M0 scale is 0xFF (NaN: what the quantizer writes for a block
+    holding Inf/NaN) makes every output that sums it NaN, as in the oracle; other
+    rows are unaffected; a requantizing epilogue turns the NaN row into NaN blocks."""
+    M, N, K = 128, 256, 256
+    rng = np.random.default_rng(12)
+    a, sa = _random_mx(rng, M, K)
+    b, sb = _random_mx(rng, N, K)
+    sa = sa.copy()
+    a = a.copy()
+    sa[5, 2] = 0xFF
+    a[5, 64:96] = 0
+    y = _gemm_bf16(lib, mx_upload(a, sa), mx_upload(b, sb))
+    ref = O.gemm(a, sa, b, sb)
+    assert np.isnan(ref[5]).all()
+    assert np.isnan(y[5]).all(), f"row 5: {np.isnan(y[5]).sum()} NaN of {N}, sample {y[5, :4]}"
+    keep = np.arange(M) != 5
+    assert_gemm_close(y[keep], ref[keep], "rows without the NaN block")
+    # through the GELU + requantization epilogue: the NaN row's blocks get scale 0xFF
+    # and zero codes, the quantizer's rule for a block holding NaN
+    bias = np.zeros(N, np.uint16)
+    out, dbg = _gelu_mx(lib, mx_upload(a, sa), mx_upload(b, sb), bias, M, N)
+    g = dbg.cpu().numpy()
+    assert np.isnan(g[5]).all()
+    codes, scales = mx_to_host(out)
+    rc, rs = O.quantize_f32(g)
+    assert_codes_equal(codes, rc, scales, rs, "requant with a NaN row")
+    assert (scales[5] == 0xFF).all() and (codes[5] == 0).all()
