@@ -101,6 +101,27 @@ def test_norm_quantize_without_modulation_and_zero_rows(lib):
     assert_codes_equal(codes, rc, scales, rs, "plain RMSNorm codes")
 
 
+def test_norm_quantize_zero_row_without_eps(lib):
+    """eps = 0 and an all-zero row: 0 / sqrt(0) is NaN on both sides, so every block of
+    that row gets the E8M0 NaN scale and zero codes; the other rows are unaffected."""
+    rng = np.random.default_rng(78)
+    rows, k = 64, 512
+    x, shift, scale = _inputs(rng, rows, k)
+    x[3] = 0
+    out, dbg = _norm_quant(lib, x, shift, scale, 0.0)
+    y = dbg.cpu().numpy()
+    assert np.isnan(y[3]).all() and np.isfinite(np.delete(y, 3, axis=0)).all()
+    codes, scales = mx_to_host(out)
+    rc, rs = O.quantize_f32(y)
+    assert_codes_equal(codes, rc, scales, rs, "eps = 0")
+    assert (scales[3] == 0xFF).all() and (codes[3] == 0).all()
+    with np.errstate(invalid="ignore", divide="ignore"):
+        ref = O.rms_norm_modulate(x, shift, scale, 0.0)
+    assert np.isnan(ref[3]).all()
+    keep = np.arange(rows) != 3
+    assert_norm_close(y[keep], x[keep], shift, scale, 0.0, "rows with eps = 0")
+
+
 @pytest.mark.slow
 def test_norm_quantize_full_size(lib):
     """M=20480, d=3072 with the DiT block's conditioning vectors, sampled rows."""
