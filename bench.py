@@ -10,9 +10,11 @@ step (2*M*d*ff*2 flops per step, quantizer time included).
 
 Other --config values measure the smaller single-GEMM workloads (pr1, dit_up,
 dit_down), the outlier-heavy wide MLP, and the neighbouring fusions: the SwiGLU
-MLP (gated_mlp), the stacked query/key/value/gate projection (qkv_proj) and the
+MLP (gated_mlp), the stacked query/key/value/gate projection (qkv_proj), the
 MLP half of a DiT block with the fused RMSNorm quantizer and the gate/residual
-epilogue (dit_block, dit_block_swiglu).
+epilogue (dit_block, dit_block_swiglu), and the attention's input (fused RMSNorm
+quantizer -> stacked Q/K/V/gate projection: attn_in) and output projection with
+its gate and residual (attn_out).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 
@@ -69,6 +71,12 @@ CONFIGS = {
     "dit_block_swiglu": dict(kind="block", M=20480, d=3072, ff=8192, activation="swiglu",
                              workload="DiT MLP sub-block, SwiGLU (M=20480, d=3072, ff=8192: RMSNorm+modulation+"
                                       "MXFP6 quantize -> stacked gate/up+SwiGLU+requant -> down + gate + residual)"),
+    "attn_in": dict(kind="attn_in", M=20480, d=3072, ff=4 * 3072,
+                    workload="DiT attention input (M=20480, d=3072: RMSNorm+modulation+MXFP6 quantize -> stacked "
+                             "query/key/value/gate projection N=4*3072, bias+BF16)"),
+    "attn_out": dict(kind="attn_out", M=20480, d=3072, ff=3072,
+                     workload="DiT attention output projection (M=20480, K=N=3072: MXFP6 quantize of the attention "
+                              "output -> projection + bias + gate + residual, BF16)"),
 }
 
 # names of the launches of one step
@@ -80,6 +88,7 @@ S_DOWN = "K2 down GEMM+bias+BF16"
 S_DOWNR = "K2 down GEMM+bias+gate+residual"
 S_GEMM = "K2 GEMM+bias+BF16"
 S_QKV = "QKV+gate GEMM+bias+BF16"
+S_OUT = "out-proj GEMM+bias+gate+residual"
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the current kernels, keyed by (config, kernel); None where no
@@ -257,6 +266,26 @@ class Workload:
             else:
                 self.y = torch.empty((M, ff), dtype=torch.bfloat16, device=dev)
             self.host = w
+        elif kind == "attn_in":
+            w = synth.attn_in(seed=seed, M=M, d=d)
+            self.x = _bf16_dev(w["x"], dev)
+            self.shift, self.scale = _bf16_dev(w["shift"], dev), _bf16_dev(w["scale"], dev)
+            self.eps = w["eps"]
+            self.w1 = mx.mx_quantize(_bf16_dev(w["w"], dev))
+            self.b1 = _bf16_dev(w["b"], dev)
+            self.xq = mx_empty(M, d)
+            self.y = torch.empty((M, ff), dtype=torch.bfloat16, device=dev)
+            self.host = w
+        elif kind == "attn_out":
+            w = synth.attn_out(seed=seed, M=M, d=d)
+            self.a = _bf16_dev(w["a"], dev)
+            self.x = _bf16_dev(w["x"], dev)
+            self.w2 = mx.mx_quantize(_bf16_dev(w["w"], dev))
+            self.b2 = _bf16_dev(w["b"], dev)
+            self.gate = _bf16_dev(w["gate"], dev)
+            self.xq = mx_empty(M, d)
+            self.y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+            self.host = w
         elif kind == "down":
             w = synth.dit_down(seed=seed, M=M, ff=ff, d=d)
             z = torch.from_numpy(w["z"]).to(dev)
@@ -277,9 +306,15 @@ class Workload:
         out = []
         if kind in ("mlp", "gated_mlp", "up", "gemm", "qkv"):
             out.append((S_K1, lambda: mx.mx_quantize(self.x, out=self.xq)))
-        if kind == "block":
+        if kind in ("block", "attn_in"):
             out.append((S_K1N, lambda: mx.mx_quantize_rmsnorm_modulate(self.x, self.shift, self.scale, self.eps,
                                                                        out=self.xq)))
+        if kind == "attn_in":
+            out.append((S_QKV, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y)))
+        if kind == "attn_out":
+            out.append((S_K1, lambda: mx.mx_quantize(self.a, out=self.xq)))
+            out.append((S_OUT, lambda: mx.mx_gemm_gate_residual(self.xq, self.w2, self.b2, self.gate, self.x,
+                                                                out=self.y)))
         if kind in ("mlp", "gated_mlp", "up", "block"):
             epi = mx.MX_EPI_BIAS_SWIGLU_MXFP6 if swiglu else mx.MX_EPI_BIAS_GELU_MXFP6
             out.append((S_GU if swiglu else S_UP, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, epi, out=self.hq)))
@@ -304,8 +339,13 @@ def stage_work(cfg: dict, M: int) -> dict:
     out = {}
     if kind in ("mlp", "gated_mlp", "up", "gemm", "qkv"):
         out[S_K1] = {"bytes": M * d * (2 + q), "flops": 0.0}
-    if kind == "block":
+    if kind in ("block", "attn_in"):
         out[S_K1N] = {"bytes": M * d * (2 + q), "flops": 0.0}
+    if kind == "attn_in":
+        out[S_QKV] = {"flops": 2.0 * M * d * ff, "bytes": (M + ff) * d * q + M * ff * 2}
+    if kind == "attn_out":
+        out[S_K1] = {"bytes": M * d * (2 + q), "flops": 0.0}
+        out[S_OUT] = {"flops": 2.0 * M * d * ff, "bytes": M * d * q + ff * d * q + M * ff * 4}
     if kind in ("mlp", "up", "block") and not swiglu:
         out[S_UP] = {"flops": 2.0 * M * d * ff, "bytes": M * d * q + ff * d * q + M * ff * q}
     if swiglu:
@@ -498,6 +538,8 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
         src, dst = c.hq.codes, c.y
     elif kind == "up":
         src, dst = c.x, c.hq.codes
+    elif kind == "attn_out":
+        src, dst = c.a, c.y
     else:
         src, dst = c.x, c.y
     h_in = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
@@ -527,6 +569,12 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
             act = mx.MX_ACT_SWIGLU if cfg["activation"] == "swiglu" else mx.MX_ACT_GELU_TANH
             mx.mx_dit_mlp_block(x_buf[slot], c.shift, c.scale, c.gate, c.w1, c.b1, c.w2, c.b2, eps=c.eps,
                                 activation=act, y=y_buf[slot], workspace=ws, stream=s_comp)
+        elif kind == "attn_in":
+            mx.mx_quantize_rmsnorm_modulate(x_buf[slot], c.shift, c.scale, c.eps, out=c.xq, stream=s_comp)
+            mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp)
+        elif kind == "attn_out":
+            mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
+            mx.mx_gemm_gate_residual(c.xq, c.w2, c.b2, c.gate, c.x, out=y_buf[slot], stream=s_comp)
         elif kind == "down":
             mx.mx_gemm(mx.MxTensor(x_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), c.w2, c.b2,
                        mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp)
@@ -608,6 +656,9 @@ class OracleWorkload:
                 w_up = w["w_up"]
             self.w1q, self.w1s = O.quantize_bf16(w_up)
             self.w2q, self.w2s = O.quantize_bf16(w["w2"])
+        elif kind in ("attn_in", "attn_out"):
+            w = synth.attn_in(M=M, d=d) if kind == "attn_in" else synth.attn_out(M=M, d=d)
+            self.w1q, self.w1s = O.quantize_bf16(w["w"])
         elif kind in ("up", "gemm", "qkv"):
             if kind == "up":
                 w = synth.dit_up(M=M)
@@ -640,6 +691,15 @@ class OracleWorkload:
             xq, xs = O.quantize_bf16(w["x"][rows])
             g = O.up_projection(xq, xs, self.w1q, self.w1s, w["b"])
             O.quantize_f32(g.astype(np.float32))
+            return 2.0 * len(rows) * d * ff
+        if kind == "attn_in":
+            a = O.rms_norm_modulate(w["x"][rows], w["shift"], w["scale"], w["eps"])
+            xq, xs = O.quantize_f32(a.astype(np.float32))
+            O.gemm(xq, xs, self.w1q, self.w1s, w["b"])
+            return 2.0 * len(rows) * d * ff
+        if kind == "attn_out":
+            xq, xs = O.quantize_bf16(w["a"][rows])
+            O.gate_residual(O.gemm(xq, xs, self.w1q, self.w1s, w["b"]), w["gate"], w["x"][rows])
             return 2.0 * len(rows) * d * ff
         if kind in ("gemm", "qkv"):
             xq, xs = O.quantize_bf16(w["x"][rows])

@@ -22,6 +22,10 @@ qkv_proj       x[20480][3072] ~ N(0,1); stacked [W_q; W_k; W_v; W_gate][12288][3
                ~ N(0,0.02); b[12288] ~ N(0,0.01)
 dit_block      as full_mlp (or gated_mlp's weights), plus the conditioning vectors
                shift, scale, gate [3072] ~ N(0,0.5) and eps = 1e-6
+attn_in        x[20480][3072] ~ N(0,1), shift/scale [3072] ~ N(0,0.5), eps = 1e-6,
+               stacked [W_q; W_k; W_v; W_gate][12288][3072] ~ N(0,0.02), b ~ N(0,0.01)
+attn_out       attention output a[20480][3072] ~ N(0,1), residual x ~ N(0,1) (W2 child),
+               W_o[3072][3072] ~ N(0,0.02), b_o ~ N(0,0.01), gate [3072] ~ N(0,0.5)
 =============  ======================================================================
 
 Every workload uses seed 0 by default. Each tensor draws from its own child of
@@ -48,6 +52,8 @@ __all__ = [
     "gated_mlp",
     "qkv_proj",
     "dit_block",
+    "attn_in",
+    "attn_out",
     "WORKLOADS",
 ]
 
@@ -211,6 +217,33 @@ def dit_block(seed: int = 0, M: int = 20480, d: int = 3072, ff: int | None = Non
     }
 
 
+def attn_in(seed: int = 0, M: int = 20480, d: int = 3072) -> dict:
+    """Attention input of a DiT block: x, shift, scale, eps (RMSNorm + modulation),
+    then the stacked query/key/value/attention-gate weight w [4d][d] and bias b."""
+    r = _rngs(seed)
+    return {
+        "x": _normal_bf16(r["x"], (M, d), 1.0),
+        "shift": _normal_bf16(r["shift"], (d,), 0.5),
+        "scale": _normal_bf16(r["scale"], (d,), 0.5),
+        "eps": 1e-6,
+        "w": _normal_bf16(r["w1"], (4 * d, d), 0.02),
+        "b": _normal_bf16(r["b1"], (4 * d,), 0.01),
+    }
+
+
+def attn_out(seed: int = 0, M: int = 20480, d: int = 3072) -> dict:
+    """Attention output projection with gate and residual: the attention output a,
+    the block input x (the residual), W_o [d][d], b_o, gate [d]."""
+    r = _rngs(seed)
+    return {
+        "a": _normal_bf16(r["x"], (M, d), 1.0),
+        "x": _normal_bf16(r["w2"], (M, d), 1.0),
+        "w": _normal_bf16(r["w1"], (d, d), 0.02),
+        "b": _normal_bf16(r["b1"], (d,), 0.01),
+        "gate": _normal_bf16(r["gate"], (d,), 0.5),
+    }
+
+
 WORKLOADS = {
     "pr1": pr1,
     "dit_up": dit_up,
@@ -220,6 +253,8 @@ WORKLOADS = {
     "gated_mlp": gated_mlp,
     "qkv_proj": qkv_proj,
     "dit_block": dit_block,
+    "attn_in": attn_in,
+    "attn_out": attn_out,
 }
 
 
