@@ -216,7 +216,7 @@ def _bf16_dev(bits, dev):
 class Workload:
     """Device-resident inputs and outputs of one copy of the configuration."""
 
-    def __init__(self, mx, cfg: dict, seed: int, dev, m_rows: int):
+    def __init__(self, mx, cfg: dict, seed: int, dev, m_rows: int, split: bool = True):
         import torch
 
         self.cfg = cfg
@@ -297,6 +297,15 @@ class Workload:
             self.b2 = _bf16_dev(w["b"], dev)
             self.y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
             self.host = {"w": w["w"], "b": w["b"]}
+        # one split-tail workspace (arrival counters zeroed once; every GEMM leaves
+        # them zero) shared by the step's GEMMs, which run one after the other
+        shapes = {"mlp": [(M, ff, d), (M, d, ff)], "gated_mlp": [(M, 2 * ff, d), (M, d, ff)],
+                  "block": [(M, 2 * ff, d), (M, d, ff)], "up": [(M, ff, d)], "gemm": [(M, ff, d)],
+                  "qkv": [(M, ff, d)], "attn_in": [(M, ff, d)], "attn_out": [(M, d, d)], "down": [(M, d, ff)]}
+        need = max(mx.mx_gemm_workspace_bytes(*s) for s in shapes[kind]) if split else 0
+        # (a workspace smaller than mx_gemm_workspace_bytes runs the GEMMs unsplit)
+        self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        self.split = split
         torch.cuda.synchronize()
 
     def stages(self, mx):
@@ -310,23 +319,33 @@ class Workload:
             out.append((S_K1N, lambda: mx.mx_quantize_rmsnorm_modulate(self.x, self.shift, self.scale, self.eps,
                                                                        out=self.xq)))
         if kind == "attn_in":
-            out.append((S_QKV, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y)))
+            out.append((S_QKV, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y,
+                                                     workspace=self.ws)))
         if kind == "attn_out":
             out.append((S_K1, lambda: mx.mx_quantize(self.a, out=self.xq)))
             out.append((S_OUT, lambda: mx.mx_gemm_gate_residual(self.xq, self.w2, self.b2, self.gate, self.x,
-                                                                out=self.y)))
+                                                                out=self.y, workspace=self.ws)))
         if kind in ("mlp", "gated_mlp", "up", "block"):
             epi = mx.MX_EPI_BIAS_SWIGLU_MXFP6 if swiglu else mx.MX_EPI_BIAS_GELU_MXFP6
-            out.append((S_GU if swiglu else S_UP, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, epi, out=self.hq)))
+            out.append((S_GU if swiglu else S_UP, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, epi, out=self.hq,
+                                                                         workspace=self.ws)))
         if kind in ("gemm", "qkv"):
             out.append((S_QKV if kind == "qkv" else S_GEMM,
-                        lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y)))
+                        lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y,
+                                                     workspace=self.ws)))
         if kind in ("mlp", "gated_mlp", "down"):
-            out.append((S_DOWN, lambda: mx.mx_gemm(self.hq, self.w2, self.b2, mx.MX_EPI_BIAS_BF16, out=self.y)))
+            out.append((S_DOWN, lambda: mx.mx_gemm(self.hq, self.w2, self.b2, mx.MX_EPI_BIAS_BF16, out=self.y,
+                                                     workspace=self.ws)))
         if kind == "block":
             out.append((S_DOWNR, lambda: mx.mx_gemm_gate_residual(self.hq, self.w2, self.b2, self.gate, self.x,
-                                                                  out=self.y)))
+                                                                  out=self.y, workspace=self.ws)))
         return out
+
+
+def mlp_min_workspace_bytes(mx, M: int, d: int, ff: int) -> int:
+    """MLP workspace without the split-tail region: MXFP6 x and h, 256-byte aligned parts."""
+    parts = (mx.mx_codes_bytes(M, d), mx.mx_scales_bytes(M, d), mx.mx_codes_bytes(M, ff), mx.mx_scales_bytes(M, ff))
+    return sum(-(-n // 256) * 256 for n in parts)
 
 
 def stage_work(cfg: dict, M: int) -> dict:
@@ -379,7 +398,8 @@ def run_gpu(args) -> dict | None:
     M = cfg["M"]
     lo, hi = shard_rows(M, world, rank)
     # two independent copies; copy i uses seed (2*rank + i) so every rank's batch is its own
-    copies = [Workload(mx, cfg, seed=2 * rank + i, dev=dev, m_rows=hi - lo) for i in range(args.copies)]
+    copies = [Workload(mx, cfg, seed=2 * rank + i, dev=dev, m_rows=hi - lo, split=not args.no_split)
+              for i in range(args.copies)]
     stream = torch.cuda.current_stream()
     stage_names = [n for n, _ in copies[0].stages(mx)]
     launches = [c.stages(mx) for c in copies]
@@ -501,7 +521,8 @@ def run_gpu(args) -> dict | None:
                    "l2": f"inputs, weights and outputs rotate over {args.copies} independent copies per step; "
                          "each step's working set exceeds the 129 MB L2, so no step reads operands the "
                          "previous step left in L2" if args.copies > 1 else "single copy (profiling run)",
-                   "parallelism": f"token-sharded x{world}, weights replicated, no collective"},
+                   "parallelism": f"token-sharded x{world}, weights replicated, no collective",
+                   "split_tail": not args.no_split},
         "ms_per_mlp": ms_step if cfg["kind"] in ("mlp", "gated_mlp", "block") else None,
         "stages": stage_report,
         "roofline": roof,
@@ -551,7 +572,9 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
     y_buf = [dst, torch.empty_like(dst)]
     ws = None
     if kind in ("mlp", "gated_mlp", "block"):
-        ws = torch.empty(max(256, mx.mx_mlp_workspace_bytes(c.M, c.d, c.ff)), dtype=torch.uint8, device=dev)
+        ws_bytes = mx.mx_mlp_workspace_bytes(c.M, c.d, c.ff) if c.split else mlp_min_workspace_bytes(mx, c.M, c.d,
+                                                                                                      c.ff)
+        ws = torch.empty(max(256, ws_bytes), dtype=torch.uint8, device=dev)
     s_up, s_comp, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
     ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
     up_done = [ev(), ev()]
@@ -571,20 +594,21 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
                                 activation=act, y=y_buf[slot], workspace=ws, stream=s_comp)
         elif kind == "attn_in":
             mx.mx_quantize_rmsnorm_modulate(x_buf[slot], c.shift, c.scale, c.eps, out=c.xq, stream=s_comp)
-            mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp)
+            mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp, workspace=c.ws)
         elif kind == "attn_out":
             mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
-            mx.mx_gemm_gate_residual(c.xq, c.w2, c.b2, c.gate, c.x, out=y_buf[slot], stream=s_comp)
+            mx.mx_gemm_gate_residual(c.xq, c.w2, c.b2, c.gate, c.x, out=y_buf[slot], stream=s_comp,
+                                     workspace=c.ws)
         elif kind == "down":
             mx.mx_gemm(mx.MxTensor(x_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), c.w2, c.b2,
-                       mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp)
+                       mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp, workspace=c.ws)
         elif kind == "up":
             mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
             mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_GELU_MXFP6,
-                       out=mx.MxTensor(y_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), stream=s_comp)
+                       out=mx.MxTensor(y_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), stream=s_comp, workspace=c.ws)
         else:
             mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
-            mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp)
+            mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp, workspace=c.ws)
 
     def step(i):
         slot = i % 2
@@ -790,6 +814,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU work for the baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-split", action="store_true",
+                    help="run the GEMMs without the split tail (the same work, tiles whole; for comparison)")
     ap.add_argument("--copies", type=int, default=2,
                     help="independent input copies rotated between steps (2 keeps L2 cold; 1 for profiling)")
     args = ap.parse_args(argv)

@@ -145,10 +145,28 @@ mx_status mx_quantize_rmsnorm_modulate(const void* x, int64_t rows, int64_t K, i
  *   out_scales       : MXFP6 epilogues only: mx_scales_bytes(M, W) bytes; else ignored
  *   debug_prequant   : MXFP6 epilogues only, may be NULL: fp32 [M][W] receives g
  *                      (or h), the exact value the requantization rounded (test hook).
+ *   workspace        : NULL, or device scratch of workspace_bytes bytes (256-byte
+ *                      aligned, overlapping no other argument) for the split tail:
+ *                      when the 256 x 256 output tiles leave a last round at most a
+ *                      quarter full for the GPU's CTA pairs (76 on GB300) and K >= 4096,
+ *                      the first pairs + (tiles mod pairs) tiles are divided along K so
+ *                      every pair does the same work, and a tile two pairs share is
+ *                      summed through the workspace (the two fp32 partial sums are
+ *                      added once, so the result is deterministic but may differ from
+ *                      the unsplit one by fp32 rounding). Used when workspace_bytes >=
+ *                      mx_gemm_workspace_bytes(M, N, K) (> 0); otherwise, and for other
+ *                      shapes, the GEMM runs unsplit (mx_gemm_launch_plan tells which). Its first
+ *                      MX_GEMM_WORKSPACE_COUNTER_BYTES bytes are arrival counters that
+ *                      must be zero when the GEMM starts: zero them once when the
+ *                      workspace is new (e.g. cudaMemsetAsync); every launch that
+ *                      completes leaves them zero again (after mx_device_error
+ *                      reports a timeout, zero them anew). Calls sharing one
+ *                      workspace must not overlap on the GPU.
  */
 mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
                   const void* bias, int64_t M, int64_t N, int64_t K, mx_epilogue epi, void* out,
-                  void* out_scales, float* debug_prequant, cudaStream_t stream);
+                  void* out_scales, float* debug_prequant, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
 
 /*
  * mx_gemm_gate_residual -- an output projection fused with its gate and the
@@ -164,12 +182,41 @@ mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes
  *              residual itself (in-place update: each element is read before it
  *              is written, by the same thread); any other overlap returns
  *              MX_ERR_INVALID_ARG.
+ *   workspace, workspace_bytes : the optional split-tail scratch, as mx_gemm.
  */
 mx_status mx_gemm_gate_residual(const void* a_codes, const void* a_scales, const void* b_codes,
                                 const void* b_scales, const void* bias, const void* gate, const void* residual,
-                                int64_t M, int64_t N, int64_t K, void* out, cudaStream_t stream);
+                                int64_t M, int64_t N, int64_t K, void* out, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes mx_mlp and mx_gated_mlp need for M tokens: MXFP6 x (M x d) and MXFP6 h (M x ff). */
+/*
+ * Workspace bytes that let mx_gemm / mx_gemm_gate_residual of this shape split
+ * their tail: MX_GEMM_WORKSPACE_COUNTER_BYTES of arrival counters plus two 256 KB
+ * partial-sum slots per CTA pair, for at most 80 pairs (about 42 MB; GB300 runs
+ * 76); 0 when the shape never splits (K < 4096, a single tile, or an unsupported
+ * shape). Host only; depends on nothing but the shape (whether a launch splits
+ * also depends on the device's pair count: mx_gemm_launch_plan).
+ */
+#define MX_GEMM_WORKSPACE_COUNTER_BYTES ((size_t)10240)
+
+size_t mx_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * mx_gemm_launch_plan -- what a GEMM of this shape does on the current device:
+ *   pairs       (host, written): CTA pairs launched (co-resident pairs, at most one per tile)
+ *   split_tiles (host, written): leading tiles divided along K when called with a
+ *                                workspace of workspace_bytes bytes (0: no split)
+ * Shape rules as mx_gemm; M == 0 or N == 0 gives 0 and 0.
+ */
+mx_status mx_gemm_launch_plan(int64_t M, int64_t N, int64_t K, size_t workspace_bytes, int* pairs,
+                              int* split_tiles);
+
+/*
+ * Workspace bytes of mx_mlp, mx_gated_mlp and mx_dit_mlp_block for M tokens:
+ * MXFP6 x (M x d), MXFP6 h (M x ff) and the split-tail region both GEMMs use in
+ * turn (as mx_gemm_workspace_bytes, for the wider of the two). A smaller workspace
+ * that still holds x and h (the first four parts) runs without the split tail.
+ */
 size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff);
 
 /*
@@ -180,8 +227,12 @@ size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff);
  *   w2_*     : W2 as MXFP6, d x ff
  *   b1, b2   : BF16 [ff], [d], or NULL
  *   d % 256 == 0, ff % 256 == 0 (both are K of one GEMM and N of the other)
- *   workspace: device, >= mx_mlp_workspace_bytes(M, d, ff) bytes, 256-byte aligned;
- *              holds xq and hq; must not overlap any other argument.
+ *   workspace: device, mx_mlp_workspace_bytes(M, d, ff) bytes, 256-byte aligned;
+ *              holds xq, hq and the split-tail scratch (the first kernel zeroes its
+ *              arrival counters, so no initialisation is needed); must not overlap
+ *              any other argument. Without
+ *              room for the split-tail region the GEMMs run unsplit; without room
+ *              for xq and hq the call returns MX_ERR_WORKSPACE_TOO_SMALL.
  */
 mx_status mx_mlp(const void* x, int64_t M, int64_t d, int64_t ff, const void* w1_codes, const void* w1_scales,
                  const void* b1, const void* w2_codes, const void* w2_scales, const void* b2, void* y,
@@ -231,17 +282,18 @@ mx_status mx_dit_mlp_block(const void* x, int64_t M, int64_t d, int64_t ff, cons
  * with a device-memory budget fixed at start-up, and paths that cannot afford
  * cudaMalloc's implicit synchronization.
  *   Same arguments and results as mx_mlp, without workspace/workspace_bytes: the
- *   scratch (MXFP6 x and MXFP6 h) lives in a static device array of
- *   MX_MLP_NOALLOC_WORKSPACE_BYTES inside the library, which every GPU that loads
- *   the library holds until the process exits. The call allocates nothing.
- *   Sizes whose mx_mlp_workspace_bytes(M, d, ff) exceeds that capacity return
- *   MX_ERR_WORKSPACE_TOO_SMALL before anything is launched (for d = 3072,
+ *   scratch (MXFP6 x and MXFP6 h, and the split-tail region when it also fits)
+ *   lives in a static device array of MX_MLP_NOALLOC_WORKSPACE_BYTES inside the
+ *   library, which every GPU that loads the library holds until the process exits.
+ *   The call allocates nothing. Sizes whose MXFP6 x and h exceed that capacity
+ *   return MX_ERR_WORKSPACE_TOO_SMALL before anything is launched (for d = 3072,
  *   ff = 12288 that is M > 5590 tokens).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.
- *   Every call on a device shares the one array, and the kernels overwrite all of
- *   it that they read, so nothing needs clearing between calls; but calls whose
+ *   Every call on a device shares the one array, and the kernels write all of it
+ *   that they read before reading it (the first kernel zeroes the split-tail
+ *   counters), so nothing needs clearing between calls; but calls whose
  *   executions overlap on the GPU (different streams, no ordering between them)
  *   race on the array and must be serialized by the caller.
  */

@@ -38,6 +38,10 @@ __all__ = [
     "mx_codes_bytes",
     "mx_scales_bytes",
     "mx_mlp_workspace_bytes",
+    "mx_gemm_workspace_bytes",
+    "mx_gemm_launch_plan",
+    "mx_gemm_workspace",
+    "MX_GEMM_WORKSPACE_COUNTER_BYTES",
     "mx_quantize",
     "mx_quantize_rmsnorm_modulate",
     "mx_quantize_stacked",
@@ -62,6 +66,7 @@ MX_EPI_BIAS_GELU_MXFP6 = 1
 MX_EPI_BIAS_SWIGLU_MXFP6 = 2
 MX_ACT_GELU_TANH = 0
 MX_ACT_SWIGLU = 1
+MX_GEMM_WORKSPACE_COUNTER_BYTES = 10240
 
 EXPORTED_SYMBOLS = (
     "mx_codes_bytes",
@@ -81,6 +86,8 @@ EXPORTED_SYMBOLS = (
     "mx_gated_mlp",
     "mx_quantize_rmsnorm_modulate",
     "mx_dit_mlp_block",
+    "mx_gemm_workspace_bytes",
+    "mx_gemm_launch_plan",
 )
 
 _lib = None
@@ -118,11 +125,14 @@ def load():
             "mx_codes_bytes": (sz, [i64, i64]),
             "mx_scales_bytes": (sz, [i64, i64]),
             "mx_quantize": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp]),
-            "mx_gemm": (ctypes.c_int, [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]),
+            "mx_gemm": (ctypes.c_int, [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, sz, vp]),
+            "mx_gemm_workspace_bytes": (sz, [i64, i64, i64]),
+            "mx_gemm_launch_plan": (ctypes.c_int, [i64, i64, i64, sz, ctypes.POINTER(ctypes.c_int),
+                                                   ctypes.POINTER(ctypes.c_int)]),
             "mx_mlp_workspace_bytes": (sz, [i64, i64, i64]),
             "mx_mlp": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "mx_gated_mlp": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
-            "mx_gemm_gate_residual": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]),
+            "mx_gemm_gate_residual": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, sz, vp]),
             "mx_quantize_rmsnorm_modulate": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, ctypes.c_float, vp, vp, vp,
                                                             vp]),
             "mx_dit_mlp_block": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, ctypes.c_float, ctypes.c_int, vp, vp,
@@ -165,6 +175,50 @@ def mx_scales_bytes(rows: int, k: int) -> int:
 
 def mx_mlp_workspace_bytes(m: int, d: int, ff: int) -> int:
     return load().mx_mlp_workspace_bytes(m, d, ff)
+
+
+def mx_gemm_workspace_bytes(m: int, n: int, k: int) -> int:
+    """Bytes of the split-tail workspace of an [m][k] x [n][k]^T GEMM (0: it never splits)."""
+    return load().mx_gemm_workspace_bytes(m, n, k)
+
+
+def mx_gemm_launch_plan(m: int, n: int, k: int, workspace_bytes: int | None = None) -> tuple[int, int]:
+    """(CTA pairs launched, leading tiles divided along K) for this GEMM shape on the
+    current device, given a workspace of ``workspace_bytes`` (default: the full size)."""
+    lib = load()
+    if workspace_bytes is None:
+        workspace_bytes = lib.mx_gemm_workspace_bytes(m, n, k)
+    pairs, split = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib.mx_gemm_launch_plan(m, n, k, int(workspace_bytes), ctypes.byref(pairs), ctypes.byref(split)),
+           "mx_gemm_launch_plan")
+    return pairs.value, split.value
+
+
+def mx_gemm_workspace(m: int, n: int, k: int, device=None, stream=None):
+    """A split-tail workspace for [m][k] x [n][k]^T GEMMs, its arrival counters zeroed
+    on ``stream`` (reusable: every GEMM leaves them zero again), or None when the
+    shape never splits."""
+    torch = _torch()
+    need = load().mx_gemm_workspace_bytes(m, n, k)
+    if need == 0:
+        return None
+    dev = device if device is not None else "cuda"
+    if stream is None:
+        return torch.zeros(int(need), dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):   # allocated and zeroed in the order of the GEMM's stream
+        return torch.zeros(int(need), dtype=torch.uint8, device=dev)
+
+
+def _split_workspace(workspace, split: bool, m: int, n: int, k: int, device, stream):
+    """(workspace tensor or None, pointer, bytes): the caller's, a new one, or none."""
+    if workspace is not None:
+        return workspace, _ptr(workspace), workspace.numel()
+    if not split:
+        return None, None, 0
+    ws = mx_gemm_workspace(m, n, k, device, stream if hasattr(stream, "cuda_stream") else None)
+    if ws is None:
+        return None, None, 0
+    return ws, _ptr(ws), ws.numel()
 
 
 def _torch():
@@ -261,13 +315,16 @@ def mx_quantize_stacked(parts, stream=None) -> MxTensor:
 
 
 def mx_gemm(a: MxTensor, b: MxTensor, bias=None, epilogue: int = MX_EPI_BIAS_BF16, out=None,
-            debug_prequant=None, stream=None):
+            debug_prequant=None, stream=None, workspace=None, split: bool = True):
     """K2/K3: a [M][K] x b [N][K]^T on MXFP6 with the fused epilogue.
 
     Returns a BF16 [M][N] tensor (MX_EPI_BIAS_BF16) or an MxTensor of [M][W]
     (W = N for MX_EPI_BIAS_GELU_MXFP6, N/2 for MX_EPI_BIAS_SWIGLU_MXFP6, where b
     is the stacked [W_g; W_u]). ``debug_prequant`` (fp32 [M][W]) receives the
-    activation output the requantization rounds.
+    activation output the requantization rounds. ``workspace`` (from
+    mx_gemm_workspace, or uint8 with its first MX_GEMM_WORKSPACE_COUNTER_BYTES zero)
+    is the split-tail scratch; without one, a new one is taken unless ``split`` is
+    False (no split tail).
     """
     torch = _torch()
     lib = load()
@@ -288,8 +345,9 @@ def mx_gemm(a: MxTensor, b: MxTensor, bias=None, epilogue: int = MX_EPI_BIAS_BF1
         out_ptr, out_sc = _ptr(out.codes), _ptr(out.scales)
     if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != n):
         raise ValueError("bias must be bfloat16 [N]")
+    ws, ws_ptr, ws_bytes = _split_workspace(workspace, split, m, n, k, dev, stream)
     st = lib.mx_gemm(_ptr(a.codes), _ptr(a.scales), _ptr(b.codes), _ptr(b.scales), _ptr(bias), m, n, k,
-                     int(epilogue), out_ptr, out_sc, _ptr(debug_prequant), _stream_handle(stream))
+                     int(epilogue), out_ptr, out_sc, _ptr(debug_prequant), ws_ptr, ws_bytes, _stream_handle(stream))
     _check(st, "mx_gemm")
     return out
 
@@ -314,8 +372,10 @@ def mx_mlp(x, w1: MxTensor, b1, w2: MxTensor, b2, y=None, workspace=None, stream
     return y
 
 
-def mx_gemm_gate_residual(a: MxTensor, b: MxTensor, bias, gate, residual, out=None, stream=None):
-    """out = bf16(residual + gate * (a b^T + bias)); out may be residual (in place)."""
+def mx_gemm_gate_residual(a: MxTensor, b: MxTensor, bias, gate, residual, out=None, stream=None, workspace=None,
+                          split: bool = True):
+    """out = bf16(residual + gate * (a b^T + bias)); out may be residual (in place).
+    ``workspace`` / ``split``: the split-tail scratch, as mx_gemm."""
     torch = _torch()
     lib = load()
     if a.k != b.k:
@@ -328,8 +388,10 @@ def mx_gemm_gate_residual(a: MxTensor, b: MxTensor, bias, gate, residual, out=No
             raise ValueError(f"{name} must be bfloat16 [N]")
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=residual.device)
+    ws, ws_ptr, ws_bytes = _split_workspace(workspace, split, m, n, k, residual.device, stream)
     st = lib.mx_gemm_gate_residual(_ptr(a.codes), _ptr(a.scales), _ptr(b.codes), _ptr(b.scales), _ptr(bias),
-                                   _ptr(gate), _ptr(residual), m, n, k, _ptr(out), _stream_handle(stream))
+                                   _ptr(gate), _ptr(residual), m, n, k, _ptr(out), ws_ptr, ws_bytes,
+                                   _stream_handle(stream))
     _check(st, "mx_gemm_gate_residual")
     return out
 

@@ -97,8 +97,12 @@ mx_status check_gemm(const void* a_codes, const void* a_scales, const void* b_co
   return MX_OK;
 }
 
+// MLP workspace: xq | xs | hq | hs, then the split-tail region both GEMMs use in
+// turn (the first kernel zeroes its arrival counters). `base` is the smallest
+// workspace the MLP runs with (no split tail), `total` the one mx_mlp_workspace_bytes
+// reports.
 struct MlpLayout {
-  size_t xq, xs, hq, hs, total;
+  size_t xq, xs, hq, hs, split, base, total;
 };
 
 MlpLayout mlp_layout(int64_t M, int64_t d, int64_t ff) {
@@ -107,14 +111,19 @@ MlpLayout mlp_layout(int64_t M, int64_t d, int64_t ff) {
   l.xs = align256(l.xq + static_cast<size_t>(mxk::codes_bytes(M, d)));
   l.hq = align256(l.xs + static_cast<size_t>(mxk::scales_bytes(M, d)));
   l.hs = align256(l.hq + static_cast<size_t>(mxk::codes_bytes(M, ff)));
-  l.total = align256(l.hs + static_cast<size_t>(mxk::scales_bytes(M, ff)));
+  l.split = align256(l.hs + static_cast<size_t>(mxk::scales_bytes(M, ff)));
+  l.base = l.split;
+  // the up-projection is at most 2 ff wide (the stacked gate/up weight)
+  const size_t up = mxk::split_workspace_bytes(M, 2 * ff, d), down = mxk::split_workspace_bytes(M, d, ff);
+  l.total = align256(l.split + (up > down ? up : down));
   return l;
 }
 
+// split_ws: split-tail workspace (arrival counters zero) or null.
 mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
                       const void* bias, int64_t M, int64_t N, int64_t K, int epi, void* out, void* out_scales,
-                      float* dbg, int num_sms, cudaStream_t stream, const void* gate = nullptr,
-                      const void* residual = nullptr) {
+                      float* dbg, int num_sms, cudaStream_t stream, void* split_ws, size_t split_bytes,
+                      const void* gate = nullptr, const void* residual = nullptr) {
   if (M == 0 || N == 0) return MX_OK;
   mxk::GemmArgs a;
   a.a_codes = a_codes;
@@ -131,6 +140,8 @@ mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_c
   a.n = N;
   a.k = K;
   a.epilogue = epi;
+  a.workspace = split_ws;
+  a.workspace_bytes = split_ws != nullptr ? split_bytes : 0;
   bool encode_failed = false;
   cudaError_t e = mxk::launch_gemm(a, num_sms, stream, &encode_failed);
   if (encode_failed) return MX_ERR_CUDA;
@@ -152,12 +163,17 @@ mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, 
     return MX_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
   const MlpLayout l = mlp_layout(M, d, ff);
-  if (workspace_bytes < l.total) return MX_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < l.base) return MX_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* xq = ws + l.xq;
   void* xs = ws + l.xs;
   void* hq = ws + l.hq;
   void* hs = ws + l.hs;
+  // the split tail runs when the workspace holds its region (mx_mlp_workspace_bytes)
+  void* sw = workspace_bytes >= l.total && l.total > l.base ? ws + l.split : nullptr;
+  const size_t sbytes = sw != nullptr ? workspace_bytes - l.split : 0;
+  unsigned* zero = static_cast<unsigned*>(sw);
+  const int nzero = static_cast<int>(mxk::kArrivalsBytes / sizeof(unsigned));
   mx_status st = check_quantize(x, M, d, d, xq, xs);
   if (st != MX_OK) return st;
   st = check_gemm(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr);
@@ -166,11 +182,13 @@ mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, 
   if (st != MX_OK) return st;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
-  if (mxk::launch_quantize_bf16(x, M, d, d, xq, xs, sms, stream) != cudaSuccess) return MX_ERR_CUDA;
-  st = gemm_launch(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr, sms, stream);
+  if (mxk::launch_quantize_bf16(x, M, d, d, xq, xs, sms, stream, zero, nzero) != cudaSuccess) return MX_ERR_CUDA;
+  st = gemm_launch(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr, sms, stream, sw,
+                   sbytes);
   if (st != MX_OK) return st;
+  // the up-projection leaves the arrival counters at zero again
   return gemm_launch(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr, sms,
-                     stream);
+                     stream, sw, sbytes);
 }
 
 // The MLP half of a DiT block: fused norm quantizer -> up-projection -> down-projection
@@ -192,12 +210,16 @@ mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const 
     return MX_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
   const MlpLayout l = mlp_layout(M, d, ff);
-  if (workspace_bytes < l.total) return MX_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < l.base) return MX_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* xq = ws + l.xq;
   void* xs = ws + l.xs;
   void* hq = ws + l.hq;
   void* hs = ws + l.hs;
+  void* sw = workspace_bytes >= l.total && l.total > l.base ? ws + l.split : nullptr;
+  const size_t sbytes = sw != nullptr ? workspace_bytes - l.split : 0;
+  unsigned* zero = static_cast<unsigned*>(sw);
+  const int nzero = static_cast<int>(mxk::kArrivalsBytes / sizeof(unsigned));
   mx_status st = check_norm_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr);
   if (st != MX_OK) return st;
   st = check_gemm(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr);
@@ -210,16 +232,24 @@ mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const 
   if (x0 != y0 && x0 < y0 + bytes && y0 < x0 + bytes) return MX_ERR_INVALID_ARG;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
-  if (mxk::launch_norm_modulate_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr, sms, stream) !=
+  if (mxk::launch_norm_modulate_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr, sms, stream, zero, nzero) !=
       cudaSuccess)
     return MX_ERR_CUDA;
-  st = gemm_launch(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr, sms, stream);
+  st = gemm_launch(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr, sms, stream, sw,
+                   sbytes);
   if (st != MX_OK) return st;
   return gemm_launch(hq, hs, w2_codes, w2_scales, b2, M, d, ff, kEpiGateResidual, y, nullptr, nullptr, sms, stream,
-                     gate, x);
+                     sw, sbytes, gate, x);
 }
 
 }  // namespace
+
+namespace mxk {
+size_t mlp_min_workspace_bytes(int64_t M, int64_t d, int64_t ff) {
+  if (M < 0 || d < 0 || ff < 0) return 0;
+  return mlp_layout(M, d, ff).base;
+}
+}  // namespace mxk
 
 extern "C" {
 
@@ -258,20 +288,23 @@ mx_status mx_quantize_rmsnorm_modulate(const void* x, int64_t rows, int64_t K, i
 
 mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
                   const void* bias, int64_t M, int64_t N, int64_t K, mx_epilogue epi, void* out,
-                  void* out_scales, float* debug_prequant, cudaStream_t stream) {
+                  void* out_scales, float* debug_prequant, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
   if (static_cast<int>(epi) == kEpiGateResidual) return MX_ERR_INVALID_ARG;  // needs mx_gemm_gate_residual
   mx_status st = check_gemm(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, static_cast<int>(epi), out,
                             out_scales, debug_prequant);
   if (st != MX_OK || M == 0 || N == 0) return st;
+  if (workspace != nullptr && !aligned(workspace, 256)) return MX_ERR_MISALIGNED;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
   return gemm_launch(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, static_cast<int>(epi), out, out_scales,
-                     debug_prequant, sms, stream);
+                     debug_prequant, sms, stream, workspace, workspace_bytes);
 }
 
 mx_status mx_gemm_gate_residual(const void* a_codes, const void* a_scales, const void* b_codes,
                                 const void* b_scales, const void* bias, const void* gate, const void* residual,
-                                int64_t M, int64_t N, int64_t K, void* out, cudaStream_t stream) {
+                                int64_t M, int64_t N, int64_t K, void* out, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
   mx_status st = check_gemm(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, kEpiGateResidual, out, nullptr,
                             nullptr);
   if (st != MX_OK || M == 0 || N == 0) return st;
@@ -281,10 +314,37 @@ mx_status mx_gemm_gate_residual(const void* a_codes, const void* a_scales, const
   const uintptr_t r0 = reinterpret_cast<uintptr_t>(residual), o0 = reinterpret_cast<uintptr_t>(out);
   const uintptr_t bytes = static_cast<uintptr_t>(M) * static_cast<uintptr_t>(N) * 2u;
   if (r0 != o0 && r0 < o0 + bytes && o0 < r0 + bytes) return MX_ERR_INVALID_ARG;
+  if (workspace != nullptr && !aligned(workspace, 256)) return MX_ERR_MISALIGNED;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
   return gemm_launch(a_codes, a_scales, b_codes, b_scales, bias, M, N, K, kEpiGateResidual, out, nullptr, nullptr,
-                     sms, stream, gate, residual);
+                     sms, stream, workspace, workspace_bytes, gate, residual);
+}
+
+size_t mx_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || N % 256 != 0 || K % 128 != 0) return 0;
+  return mxk::split_workspace_bytes(M, N, K);
+}
+
+mx_status mx_gemm_launch_plan(int64_t M, int64_t N, int64_t K, size_t workspace_bytes, int* pairs,
+                              int* split_tiles) {
+  if (pairs == nullptr || split_tiles == nullptr || M < 0 || N < 0 || K < 0) return MX_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N % 256 != 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  *pairs = 0;
+  *split_tiles = 0;
+  if (M == 0 || N == 0) return MX_OK;
+  int sms = 0;
+  mx_status st = device_check(&sms);
+  if (st != MX_OK) return st;
+  int clusters = 0;
+  if (mxk::gemm_max_clusters(&clusters) != cudaSuccess) return MX_ERR_CUDA;
+  // any non-null pointer: only the size decides
+  const mxk::GemmPlan p = mxk::plan_gemm(M, N, K, clusters, workspace_bytes > 0 ? &clusters : nullptr,
+                                         workspace_bytes);
+  *pairs = p.clusters;
+  *split_tiles = p.sk_tiles;
+  return MX_OK;
 }
 
 size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff) {

@@ -107,6 +107,10 @@ static_assert(offsetof(SharedStorage, bias_s) % 16 == 0 && offsetof(SharedStorag
 static_assert(offsetof(SharedStorage, sfa) % 128 == 0 && offsetof(SharedStorage, sfb) % 128 == 0,
               "scale atoms are TMA destinations");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kPair * BM == kPairTileRows && BN == kPairTileCols && BK == kStepK, "tile geometry of the launch plan");
+static_assert(kPair * kEpiWarps == kArrivalWordsPerTile, "one arrival counter per CTA and epilogue warp");
+static_assert(kSplitSlotBytes == size_t{kPair} * kEpiWarps * kEpiChunks * 8 * 32 * sizeof(float4),
+              "a partial slot holds both CTAs' accumulators");
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
@@ -179,43 +183,97 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Tile walk shared by every role: cluster c takes tile pairs c, c + #clusters, ...
-// A pair tile is 256 rows (CTA r: row tile 2 p_m + r) x 256 columns.
-struct TileWalk {
-  int pairs, num_n, first, step, rank;
+// Work plan shared by every role. Tiles are pair tiles (256 rows x 256 columns,
+// CTA r of the pair: row tile 2 p_m + r) in row-major order. Without a split
+// tail, cluster c takes tiles c, c + #clusters, ... When the last round would
+// leave most pairs idle (the host's rule: at most a quarter of a round left over,
+// and long tiles), the first sk_tiles = #clusters + (tiles mod #clusters) tiles
+// are shared out along K instead: their sk_tiles * kblocks K-steps are cut into one contiguous
+// range per cluster (every cluster gets at least one tile's worth), and the
+// remaining tiles, a whole number of rounds, are taken whole as above. A range
+// boundary inside a tile makes it a split tile with exactly two contributors;
+// each stores its fp32 partial accumulator, and whichever arrives second adds
+// the other's partial and runs the epilogue. fp32 addition of two terms is
+// commutative, so the result does not depend on which one that is.
+struct Plan {
+  int tiles, num_n, kblocks, clusters, sk_tiles;
+  float4* partial;     // split tiles: 2 slots per cluster, each 2 CTAs x 128 rows x 256 fp32
+  unsigned* arrivals;  // split tiles: arrivals per (tile, CTA rank); zero before the launch
 };
 
-__device__ __forceinline__ void pair_tile(const TileWalk& w, int p, int* mb, int* nb) {
-  const int pm = p / w.num_n;
-  *nb = p - pm * w.num_n;
-  *mb = pm * kPair + w.rank;
+// A stretch of one tile's K-steps [kb0, kb1) that one cluster computes.
+struct Unit {
+  int tile, kb0, kb1;
+};
+
+// A cluster's split range, in K-steps counted from the start of tile 0 (the host
+// keeps sk_tiles * kblocks below 2^31).
+struct Cursor {
+  int pos, end;
+};
+
+// First K-step of cluster c's split range.
+__device__ __forceinline__ int split_start(const Plan& pl, int c) {
+  return static_cast<int>(static_cast<int64_t>(pl.sk_tiles) * pl.kblocks * c / pl.clusters);
+}
+
+__device__ __forceinline__ Cursor cursor_begin(const Plan& pl, int c) {
+  Cursor k;
+  k.pos = split_start(pl, c);
+  k.end = split_start(pl, c + 1);
+  return k;
+}
+
+// The next unit of the split range. Every role walks the same sequence: the
+// split range first (so the exchange of partials overlaps the whole tiles that
+// follow), then whole tiles sk_tiles + c, sk_tiles + c + #clusters, ... in a loop
+// of their own, which carries none of the split state.
+__device__ __forceinline__ bool cursor_next(const Plan& pl, Cursor& k, Unit& u) {
+  if (k.pos < k.end) {
+    const int t = k.pos / pl.kblocks;
+    const int lo = t * pl.kblocks;
+    u.tile = t;
+    u.kb0 = k.pos - lo;
+    u.kb1 = min(k.end - lo, pl.kblocks);
+    k.pos = lo + u.kb1;
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void pair_tile(const Plan& pl, int tile, int rank, int* mb, int* nb) {
+  const int pm = tile / pl.num_n;
+  *nb = tile - pm * pl.num_n;
+  *mb = pm * kPair + rank;
 }
 
 // gated: B is the stacked [gate; up] weight of 2 * n_out rows; CTA 0 of the pair
 // stages gate rows [128 nb, 128 nb + 128) and CTA 1 the up rows n_out rows further,
 // and both SMs' tensor memory gets the scale atoms of both row groups.
+template <bool SPLIT>
 __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap* ta, const CUtensorMap* tb,
-                                             const CUtensorMap* tsa, const CUtensorMap* tsb, const TileWalk& w,
-                                             int num_m, int kblocks, bool gated, int n_out,
+                                             const CUtensorMap* tsa, const CUtensorMap* tsb, const Plan& pl,
+                                             int cluster, int rank, bool gated, int n_out,
                                              volatile int* abort_flag) {
+  const int kblocks = pl.kblocks;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t filled = 0, fill_parity = 0;
   bool ok = true;
-  for (int p = w.first; p < w.pairs && ok; p += w.step) {
+  auto load_unit = [&](int tile, int kb0, int kb1) {
     int mb, nb;
-    pair_tile(w, p, &mb, &nb);
-    for (int kb = 0; kb < kblocks; ++kb) {
+    pair_tile(pl, tile, rank, &mb, &nb);
+    for (int kb = kb0; kb < kb1; ++kb) {
       if (!wait_bounded(&s.empty[stage], phase ^ 1u, abort_flag, kErrWaitProducer)) {
         ok = false;
-        break;
+        return;
       }
       // both CTAs' stage bytes complete on the leader's full barrier, which
       // expects them all; a row tile past M reads zeros (A and its scales)
       const uint32_t full_leader = mapa_shared(smem_u32(&s.full[stage]), 0);
-      if (w.rank == 0) mbar_arrive_expect_tx(&s.full[stage], kPair * kStageTx);
+      if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], kPair * kStageTx);
       tma_load_2d_pair(s.a[stage], ta, full_leader, kb * BK, mb * BM);
-      const int b_row = gated ? w.rank * n_out + nb * kBHalfRows : nb * BN + w.rank * kBHalfRows;
+      const int b_row = gated ? rank * n_out + nb * kBHalfRows : nb * BN + rank * kBHalfRows;
       tma_load_2d_pair(s.b[stage], tb, full_leader, kb * BK, b_row);
       tma_load_2d_pair(s.sfa[stage], tsa, full_leader, 0, mb * kblocks + kb);
       if (gated) {
@@ -231,31 +289,38 @@ __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap
         phase ^= 1u;
       }
     }
+  };
+  if constexpr (SPLIT) {
+    Cursor cur = cursor_begin(pl, cluster);
+    Unit u;
+    while (ok && cursor_next(pl, cur, u)) load_unit(u.tile, u.kb0, u.kb1);
   }
+  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; ok && p < pl.tiles; p += pl.clusters) load_unit(p, 0, kblocks);
   if (ok) {
     // every stage this CTA filled has been consumed by the pair's MMAs, so no
     // completion arrival from the leader is still heading here
     for (int st = 0; st < kStages; ++st)
       if ((filled >> st) & 1u) wait_drain(&s.empty[st], (fill_parity >> st) & 1u);
-  } else if (w.rank == 0) {
+  } else if (rank == 0) {
     for (int st = 0; st < kStages; ++st)
       if ((filled >> st) & 1u) wait_drain(&s.full[st], (fill_parity >> st) & 1u);
   }
 }
 
-__device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const TileWalk& w, int kblocks,
+template <bool SPLIT>
+__device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const Plan& pl, int cluster,
                                         volatile int* abort_flag) {
   int stage = 0;
   uint32_t phase = 0, acc_phase = 0;
   bool ok = true, issued = false;
-  for (int p = w.first; p < w.pairs && ok; p += w.step) {
+  auto mma_unit = [&](int kb0, int kb1) {
     // both CTAs' epilogues have drained the previous tile's accumulators
     if (!wait_bounded_cluster(&s.tmem_empty, acc_phase ^ 1u, abort_flag, kErrWaitMma)) {
       ok = false;
-      break;
+      return;
     }
     tc_fence_after();
-    for (int kb = 0; kb < kblocks; ++kb) {
+    for (int kb = kb0; kb < kb1; ++kb) {
       // operands of both CTAs landed, scales copied into both SMs' tensor memory
       if (!wait_bounded(&s.full[stage], phase, abort_flag, kErrWaitMma) ||
           !wait_bounded(&s.sfready[stage], phase, abort_flag, kErrWaitMma)) {
@@ -271,8 +336,7 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const T
 #pragma unroll
         for (uint32_t j = 0; j < 4; ++j) {
           // K step j: 32 elements = 32 bytes further along the swizzled 128-byte row
-          tc_mma_mx_pair(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j), sf_a, sf_b,
-                         (kb | static_cast<int>(j)) != 0);
+          tc_mma_mx_pair(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j), sf_a, sf_b, (kb != kb0) || j != 0);
         }
         tc_commit_pair(&s.empty[stage], kPairMask);  // frees the stage in both CTAs
         issued = true;
@@ -282,10 +346,16 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const T
         }
       }
     }
-    if (!ok) break;
+    if (!ok) return;
     tc_commit_pair(&s.tmem_full, kPairMask);
     acc_phase ^= 1u;
+  };
+  if constexpr (SPLIT) {
+    Cursor cur = cursor_begin(pl, cluster);
+    Unit u;
+    while (ok && cursor_next(pl, cur, u)) mma_unit(u.kb0, u.kb1);
   }
+  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; ok && p < pl.tiles; p += pl.clusters) mma_unit(0, pl.kblocks);
   if (!ok && issued) {
     tc_commit_pair(&s.drain, 0x1);
     wait_drain(&s.drain, 0);
@@ -294,10 +364,14 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const T
 
 // Leader CTA, scale warp: copies each stage's scale atoms into both SMs' tensor
 // memory in its own tcgen05 stream and signals sfready[stage] when they landed.
-__device__ __forceinline__ void run_scales(SharedStorage& s, uint32_t tmem, const TileWalk& w, int kblocks,
+template <bool SPLIT>
+__device__ __forceinline__ void run_scales(SharedStorage& s, uint32_t tmem, const Plan& pl, int cluster,
                                            volatile int* abort_flag) {
-  const int my_pairs = w.pairs > w.first ? (w.pairs - w.first + w.step - 1) / w.step : 0;
-  const int64_t steps = static_cast<int64_t>(my_pairs) * kblocks;
+  // the split range's K-steps, then kblocks per whole tile
+  const int first_whole = (SPLIT ? pl.sk_tiles : 0) + cluster;
+  const int64_t whole = first_whole < pl.tiles ? (pl.tiles - first_whole + pl.clusters - 1) / pl.clusters : 0;
+  int64_t steps = whole * pl.kblocks;
+  if constexpr (SPLIT) steps += split_start(pl, cluster + 1) - split_start(pl, cluster);
   int stage = 0;
   uint32_t phase = 0;
   for (int64_t g = 0; g < steps; ++g) {
@@ -403,156 +477,261 @@ __device__ __forceinline__ uint32_t chunk_col(int h, int c) {
     return static_cast<uint32_t>(h * kEpiCols + 32 * c);
 }
 
-// n_total: the GEMM's N (rows of B; stacked 2 F for kEpiSwiglu). Output width:
-// F = n_total / 2 for kEpiSwiglu, else n_total.
-template <int EPI, bool DBG>
-__device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, const TileWalk& wk,
-                                             int num_m, int m_total, int n_total,
+// A split tile: this warp stores its 32 rows x 128 columns of the partial
+// accumulator, counts its arrival, and if the other contributor's part is
+// already stored, adds it. Returns true when r holds the tile's full sum (this
+// warp arrived second), false when the other contributor will finish the tile.
+// Each epilogue warp has its own arrival counter, so no warp ever waits for another.
+__device__ __forceinline__ bool split_exchange(const Plan& pl, int cluster, int rank, int ew, int lane,
+                                               const Unit& u, uint32_t (&r)[kEpiChunks][32]) {
+  const int lo = u.tile * pl.kblocks;
+  const int64_t w = static_cast<int64_t>(pl.sk_tiles) * pl.kblocks;
+  // the two contributors: the cluster whose range holds the tile's first K-step, and the next one
+  const int first = static_cast<int>((static_cast<int64_t>(lo + 1) * pl.clusters - 1) / w);
+  const int other = cluster == first ? first + 1 : first;
+  // two slots per cluster: the tile its range starts in (0) and the tile it ends in (1)
+  const int mine_slot = 2 * cluster + (split_start(pl, cluster) >= lo ? 0 : 1);
+  const int other_slot = 2 * other + (split_start(pl, other) >= lo ? 0 : 1);
+  constexpr int kVec = kEpiChunks * 8;  // float4 values per thread
+  constexpr int64_t kSlot = static_cast<int64_t>(kPair) * kEpiWarps * kVec * 32;
+  const int64_t base = (static_cast<int64_t>(rank) * kEpiWarps + ew) * kVec * 32 + lane;
+  float4* mine = pl.partial + mine_slot * kSlot + base;
+#pragma unroll
+  for (int c = 0; c < kEpiChunks; ++c)
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      __stcg(mine + (c * 8 + v) * 32, make_float4(__uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
+                                                  __uint_as_float(r[c][4 * v + 2]),
+                                                  __uint_as_float(r[c][4 * v + 3])));
+  __threadfence();
+  __syncwarp();
+  unsigned* counter = pl.arrivals + (static_cast<int64_t>(u.tile) * kPair + rank) * kEpiWarps + ew;
+  unsigned old = 0;
+  if (lane == 0) old = atomicAdd(counter, 1u);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old == 0) return false;
+  __threadfence();
+  const float4* theirs = pl.partial + other_slot * kSlot + base;
+#pragma unroll
+  for (int c = 0; c < kEpiChunks; ++c)
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const float4 o = __ldcg(theirs + (c * 8 + v) * 32);
+      r[c][4 * v] = __float_as_uint(__uint_as_float(r[c][4 * v]) + o.x);
+      r[c][4 * v + 1] = __float_as_uint(__uint_as_float(r[c][4 * v + 1]) + o.y);
+      r[c][4 * v + 2] = __float_as_uint(__uint_as_float(r[c][4 * v + 2]) + o.z);
+      r[c][4 * v + 3] = __float_as_uint(__uint_as_float(r[c][4 * v + 3]) + o.w);
+    }
+  if (lane == 0) *counter = 0u;  // both arrivals are in: zero again for the next launch
+  return true;
+}
+
+// Epilogue state of one warp that stays the same from tile to tile.
+struct EpiCtx {
+  int warp, lane, q, h, rank, cluster;
+  int num_m, m_total, n_total, n_out;
+  uint32_t tmem, tmem_empty_leader;
+  float* bw;
+  float* gw;
+};
+
+// The epilogue of one output tile (or, SPLIT, of one unit of the split region):
+// drain the accumulator, release it, then the fused epilogue. Returns false when
+// a wait gave up. n_total: the GEMM's N (rows of B; stacked 2 F for kEpiSwiglu);
+// output width F = n_total / 2 for kEpiSwiglu, else n_total.
+template <int EPI, bool DBG, bool SPLIT>
+__device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e, int mb, int nb, uint32_t& acc_phase,
+                                              const Plan& pl, const Unit& u, const uint16_t* __restrict__ bias,
+                                              const uint16_t* __restrict__ gate, const uint16_t* residual, void* out,
+                                              uint8_t* __restrict__ out_scales, float* __restrict__ dbg,
+                                              volatile int* abort_flag) {
+  const int lane = e.lane, q = e.q, h = e.h, warp = e.warp, rank = e.rank, cluster = e.cluster;
+  const int num_m = e.num_m, m_total = e.m_total, n_total = e.n_total, n_out = e.n_out;
+  const uint32_t tmem = e.tmem, tmem_empty_leader = e.tmem_empty_leader;
+  float* bw = e.bw;
+  float* gw = e.gw;
+  // first output column of this warp: 64 of them (kEpiSwiglu) or 128
+  const int col0 = (EPI == kEpiSwiglu) ? nb * kBHalfRows + 64 * h : nb * BN + h * kEpiCols;
+  if constexpr (EPI == kEpiSwiglu)
+    stage_vec(bw, bias, col0, n_out + col0, lane, 0.f);
+  else
+    stage_vec(bw, bias, col0, col0 + 64, lane, 0.f);
+  if constexpr (EPI == kEpiGateRes) stage_vec(gw, gate, col0, col0 + 64, lane, 1.f);
+  int ok = 0;
+  if (lane == 0) ok = wait_bounded(&s.tmem_full, acc_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return false;
+  tc_fence_after();
+  uint32_t r[kEpiChunks][32];
+  const uint32_t t0 = tmem + (static_cast<uint32_t>(32 * q) << 16);
+#pragma unroll
+  for (int c = 0; c < kEpiChunks; ++c) tc_ld_32x32b_x32(t0 + chunk_col<EPI>(h, c), r[c]);
+  tc_wait_ld();
+  tc_fence_before();
+  __syncwarp();
+  // tcgen05.wait::ld has completed this warp's reads and the fence above orders
+  // them before the signal; no memory is handed over, so the arrive is relaxed
+  // (a release would first wait for the previous tile's global stores).
+  if (lane == 0) mbar_arrive_remote_relaxed(tmem_empty_leader);
+  acc_phase ^= 1u;
+  if constexpr (SPLIT) {
+    // a split tile's first contributor only stores its partial sum
+    if ((u.kb0 != 0 || u.kb1 != pl.kblocks) && !split_exchange(pl, cluster, rank, warp - 2, lane, u, r)) return true;
+  }
+
+  const int64_t row = static_cast<int64_t>(mb) * BM + 32 * q + lane;
+  const bool live = row < m_total;
+  if constexpr (EPI == kEpiBf16 || EPI == kEpiGateRes) {
+    uint16_t* y = static_cast<uint16_t*>(out);
+#pragma unroll
+    for (int c = 0; c < kEpiChunks; ++c) {
+      const int n = col0 + 32 * c;
+      uint32_t rw[16];  // kEpiGateRes: the residual's 32 BF16 values, two per word
+      if constexpr (EPI == kEpiGateRes) {
+        uint4 res[4] = {};
+        if (live) {
+          const uint4* src = reinterpret_cast<const uint4*>(residual + row * n_total + n);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) res[j] = __ldg(src + j);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          rw[4 * j] = res[j].x;
+          rw[4 * j + 1] = res[j].y;
+          rw[4 * j + 2] = res[j].z;
+          rw[4 * j + 3] = res[j].w;
+        }
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 b4 = staged4(bw, c, v);
+        uint64_t x01 = f2_add(f2_pack(__uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1])),
+                              f2_pack(b4.x, b4.y));
+        uint64_t x23 = f2_add(f2_pack(__uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3])),
+                              f2_pack(b4.z, b4.w));
+        if constexpr (EPI == kEpiGateRes) {
+          const float4 g4 = staged4(gw, c, v);
+          x01 = f2_fma(f2_pack(g4.x, g4.y), x01,
+                       f2_pack(__uint_as_float(rw[2 * v] << 16), __uint_as_float(rw[2 * v] & 0xFFFF0000u)));
+          x23 = f2_fma(f2_pack(g4.z, g4.w), x23,
+                       f2_pack(__uint_as_float(rw[2 * v + 1] << 16), __uint_as_float(rw[2 * v + 1] & 0xFFFF0000u)));
+        }
+        float x0, x1, x2, x3;
+        f2_unpack(x01, x0, x1);
+        f2_unpack(x23, x2, x3);
+        pk[2 * v] = cvt_bf16x2(x1, x0);
+        pk[2 * v + 1] = cvt_bf16x2(x3, x2);
+      }
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(y + row * n_total + n);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      }
+    }
+  } else {
+    // MXFP6 requantization along the output columns, one 32-column block at a time
+    constexpr int kBlocks = (EPI == kEpiSwiglu) ? kEpiChunks / 2 : kEpiChunks;
+    uint8_t* codes = static_cast<uint8_t*>(out);
+    uint32_t scale_word = 0;
+#pragma unroll
+    for (int c = 0; c < kBlocks; ++c) {
+      const int n = col0 + 32 * c;
+      float g[32];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 b4 = staged4(bw, c, v);
+        const uint64_t bb[2] = {f2_pack(b4.x, b4.y), f2_pack(b4.z, b4.w)};
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = 4 * v + 2 * t;
+          const uint64_t x = f2_add(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), bb[t]);
+          if constexpr (EPI == kEpiGelu) {
+            gelu_tanh2(x, g[i], g[i + 1]);
+          } else {
+            const float4 u4 = staged4(bw, 2 + c, v);
+            const uint64_t bu = t == 0 ? f2_pack(u4.x, u4.y) : f2_pack(u4.z, u4.w);
+            const uint64_t u = f2_add(f2_pack(__uint_as_float(r[2 + c][i]), __uint_as_float(r[2 + c][i + 1])), bu);
+            silu_mul2(x, u, g[i], g[i + 1]);
+          }
+        }
+      }
+      if constexpr (DBG) {
+        if (live) store_dbg32(dbg + row * n_out + n, g);
+      }
+      uint32_t w[6];
+      const uint32_t sc = quant_block32(g, w);
+      if (live) store_block_codes(codes + row * (n_out / 4 * 3) + n / 4 * 3, w);
+      scale_word |= sc << (8 * c);
+    }
+    // padding rows of the last row tile get zero scales; a row tile past the
+    // last one (second half of the last pair) has no scale storage at all
+    if (!live) scale_word = 0;
+    if (mb < num_m) {
+      uint8_t* sw = out_scales + scale_word_offset(row, col0 / kAtomK, n_out) + (col0 % kAtomK) / 32;
+      if constexpr (kBlocks == 4)
+        *reinterpret_cast<uint32_t*>(sw) = scale_word;
+      else
+        *reinterpret_cast<uint16_t*>(sw) = static_cast<uint16_t>(scale_word);
+    }
+  }
+  return true;
+}
+
+template <int EPI, bool DBG, bool SPLIT>
+__device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, const Plan& pl,
+                                             int cluster, int rank, int num_m, int m_total, int n_total,
                                              const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate,
                                              const uint16_t* residual, void* out, uint8_t* __restrict__ out_scales,
                                              float* __restrict__ dbg, volatile int* abort_flag) {
-  const int q = warp & 3;           // tensor-memory lane quadrant this warp may access
-  const int h = (warp - 2) >> 2;    // column group of the 256-wide tile
-  const int n_out = (EPI == kEpiSwiglu) ? n_total / 2 : n_total;
-  uint32_t acc_phase = 0;
+  EpiCtx e;
+  e.warp = warp;
+  e.lane = lane;
+  e.q = warp & 3;           // tensor-memory lane quadrant this warp may access
+  e.h = (warp - 2) >> 2;    // column group of the 256-wide tile
+  e.rank = rank;
+  e.cluster = cluster;
+  e.num_m = num_m;
+  e.m_total = m_total;
+  e.n_total = n_total;
+  e.n_out = (EPI == kEpiSwiglu) ? n_total / 2 : n_total;
+  e.tmem = tmem;
   // the accumulator is released to the leader CTA's barrier (both CTAs' warps count)
-  const uint32_t tmem_empty_leader = mapa_shared(smem_u32(&s.tmem_empty), 0);
-  float* bw = s.bias_s[warp - 2];
-  float* gw = s.gate_s[warp - 2];
-  for (int p = wk.first; p < wk.pairs; p += wk.step) {
-    int mb, nb;
-    pair_tile(wk, p, &mb, &nb);
-    // first output column of this warp: 64 of them (kEpiSwiglu) or 128
-    const int col0 = (EPI == kEpiSwiglu) ? nb * kBHalfRows + 64 * h : nb * BN + h * kEpiCols;
-    if constexpr (EPI == kEpiSwiglu)
-      stage_vec(bw, bias, col0, n_out + col0, lane, 0.f);
-    else
-      stage_vec(bw, bias, col0, col0 + 64, lane, 0.f);
-    if constexpr (EPI == kEpiGateRes) stage_vec(gw, gate, col0, col0 + 64, lane, 1.f);
-    int ok = 0;
-    if (lane == 0) ok = wait_bounded(&s.tmem_full, acc_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) break;
-    tc_fence_after();
-    uint32_t r[kEpiChunks][32];
-    const uint32_t t0 = tmem + (static_cast<uint32_t>(32 * q) << 16);
-#pragma unroll
-    for (int c = 0; c < kEpiChunks; ++c) tc_ld_32x32b_x32(t0 + chunk_col<EPI>(h, c), r[c]);
-    tc_wait_ld();
-    tc_fence_before();
-    __syncwarp();
-    // tcgen05.wait::ld has completed this warp's reads and the fence above orders
-    // them before the signal; no memory is handed over, so the arrive is relaxed
-    // (a release would first wait for the previous tile's global stores).
-    if (lane == 0) mbar_arrive_remote_relaxed(tmem_empty_leader);
-    acc_phase ^= 1u;
-
-    const int64_t row = static_cast<int64_t>(mb) * BM + 32 * q + lane;
-    const bool live = row < m_total;
-    if constexpr (EPI == kEpiBf16 || EPI == kEpiGateRes) {
-      uint16_t* y = static_cast<uint16_t*>(out);
-#pragma unroll
-      for (int c = 0; c < kEpiChunks; ++c) {
-        const int n = col0 + 32 * c;
-        uint32_t rw[16];  // kEpiGateRes: the residual's 32 BF16 values, two per word
-        if constexpr (EPI == kEpiGateRes) {
-          uint4 res[4] = {};
-          if (live) {
-            const uint4* src = reinterpret_cast<const uint4*>(residual + row * n_total + n);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) res[j] = __ldg(src + j);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            rw[4 * j] = res[j].x;
-            rw[4 * j + 1] = res[j].y;
-            rw[4 * j + 2] = res[j].z;
-            rw[4 * j + 3] = res[j].w;
-          }
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float4 b4 = staged4(bw, c, v);
-          uint64_t x01 = f2_add(f2_pack(__uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1])),
-                                f2_pack(b4.x, b4.y));
-          uint64_t x23 = f2_add(f2_pack(__uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3])),
-                                f2_pack(b4.z, b4.w));
-          if constexpr (EPI == kEpiGateRes) {
-            const float4 g4 = staged4(gw, c, v);
-            x01 = f2_fma(f2_pack(g4.x, g4.y), x01,
-                         f2_pack(__uint_as_float(rw[2 * v] << 16), __uint_as_float(rw[2 * v] & 0xFFFF0000u)));
-            x23 = f2_fma(f2_pack(g4.z, g4.w), x23,
-                         f2_pack(__uint_as_float(rw[2 * v + 1] << 16), __uint_as_float(rw[2 * v + 1] & 0xFFFF0000u)));
-          }
-          float x0, x1, x2, x3;
-          f2_unpack(x01, x0, x1);
-          f2_unpack(x23, x2, x3);
-          pk[2 * v] = cvt_bf16x2(x1, x0);
-          pk[2 * v + 1] = cvt_bf16x2(x3, x2);
-        }
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(y + row * n_total + n);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        }
-      }
-    } else {
-      // MXFP6 requantization along the output columns, one 32-column block at a time
-      constexpr int kBlocks = (EPI == kEpiSwiglu) ? kEpiChunks / 2 : kEpiChunks;
-      uint8_t* codes = static_cast<uint8_t*>(out);
-      uint32_t scale_word = 0;
-#pragma unroll
-      for (int c = 0; c < kBlocks; ++c) {
-        const int n = col0 + 32 * c;
-        float g[32];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float4 b4 = staged4(bw, c, v);
-          const uint64_t bb[2] = {f2_pack(b4.x, b4.y), f2_pack(b4.z, b4.w)};
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int i = 4 * v + 2 * t;
-            const uint64_t x = f2_add(f2_pack(__uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1])), bb[t]);
-            if constexpr (EPI == kEpiGelu) {
-              gelu_tanh2(x, g[i], g[i + 1]);
-            } else {
-              const float4 u4 = staged4(bw, 2 + c, v);
-              const uint64_t bu = t == 0 ? f2_pack(u4.x, u4.y) : f2_pack(u4.z, u4.w);
-              const uint64_t u = f2_add(f2_pack(__uint_as_float(r[2 + c][i]), __uint_as_float(r[2 + c][i + 1])), bu);
-              silu_mul2(x, u, g[i], g[i + 1]);
-            }
-          }
-        }
-        if constexpr (DBG) {
-          if (live) store_dbg32(dbg + row * n_out + n, g);
-        }
-        uint32_t w[6];
-        const uint32_t sc = quant_block32(g, w);
-        if (live) store_block_codes(codes + row * (n_out / 4 * 3) + n / 4 * 3, w);
-        scale_word |= sc << (8 * c);
-      }
-      // padding rows of the last row tile get zero scales; a row tile past the
-      // last one (second half of the last pair) has no scale storage at all
-      if (!live) scale_word = 0;
-      if (mb < num_m) {
-        uint8_t* sw = out_scales + scale_word_offset(row, col0 / kAtomK, n_out) + (col0 % kAtomK) / 32;
-        if constexpr (kBlocks == 4)
-          *reinterpret_cast<uint32_t*>(sw) = scale_word;
-        else
-          *reinterpret_cast<uint16_t*>(sw) = static_cast<uint16_t>(scale_word);
-      }
+  e.tmem_empty_leader = mapa_shared(smem_u32(&s.tmem_empty), 0);
+  e.bw = s.bias_s[warp - 2];
+  e.gw = s.gate_s[warp - 2];
+  uint32_t acc_phase = 0;
+  // the split region first, in its own loop
+  if constexpr (SPLIT) {
+    Cursor cur = cursor_begin(pl, cluster);
+    Unit u;
+    while (cursor_next(pl, cur, u)) {
+      int mb, nb;
+      pair_tile(pl, u.tile, rank, &mb, &nb);
+      if (!epilogue_tile<EPI, DBG, true>(s, e, mb, nb, acc_phase, pl, u, bias, gate, residual, out, out_scales, dbg,
+                                         abort_flag))
+        return;
     }
+  }
+  const Unit whole = {0, 0, 0};
+  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; p < pl.tiles; p += pl.clusters) {
+    int mb, nb;
+    pair_tile(pl, p, rank, &mb, &nb);
+    if (!epilogue_tile<EPI, DBG, false>(s, e, mb, nb, acc_phase, pl, whole, bias, gate, residual, out, out_scales,
+                                        dbg, abort_flag))
+      return;
   }
 }
 
-template <int EPI, bool DBG>
+// SPLIT: the launch divides its first sk_tiles tiles along K (a separate instance,
+// so the whole-tile kernel carries none of that code).
+template <int EPI, bool DBG, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sb,
                    const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate, const uint16_t* residual,
                    void* out, uint8_t* __restrict__ out_scales, float* __restrict__ dbg, int m_total, int n_total,
-                   int k_total) {
+                   int k_total, SplitArgs split) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   SharedStorage& s =
@@ -561,13 +740,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
   const int num_n = n_total / BN;
   const int num_m = (m_total + BM - 1) / BM;
-  const int kblocks = k_total / BK;
-  TileWalk walk;
-  walk.num_n = num_n;
-  walk.pairs = ((num_m + kPair - 1) / kPair) * num_n;
-  walk.first = static_cast<int>(cluster_id_x());
-  walk.step = static_cast<int>(cluster_count_x());
-  walk.rank = static_cast<int>(cluster_ctarank());
+  Plan plan;
+  plan.num_n = num_n;
+  plan.tiles = ((num_m + kPair - 1) / kPair) * num_n;
+  plan.kblocks = k_total / BK;
+  plan.clusters = static_cast<int>(cluster_count_x());
+  plan.sk_tiles = split.sk_tiles;
+  plan.partial = split.partial;
+  plan.arrivals = split.arrivals;
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int rank = static_cast<int>(cluster_ctarank());
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -604,15 +786,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0)
-      run_producer(s, &tmap_a, &tmap_b, &tmap_sa, &tmap_sb, walk, num_m, kblocks, EPI == kEpiSwiglu, n_total / 2,
+      run_producer<SPLIT>(s, &tmap_a, &tmap_b, &tmap_sa, &tmap_sb, plan, cluster, rank, EPI == kEpiSwiglu, n_total / 2,
                    abort_flag);
   } else if (warp == 1) {
-    if (lane == 0 && walk.rank == 0) run_mma(s, tmem, walk, kblocks, abort_flag);
+    if (lane == 0 && rank == 0) run_mma<SPLIT>(s, tmem, plan, cluster, abort_flag);
   } else if (warp == 2 + kEpiWarps) {
-    if (lane == 0 && walk.rank == 0) run_scales(s, tmem, walk, kblocks, abort_flag);
+    if (lane == 0 && rank == 0) run_scales<SPLIT>(s, tmem, plan, cluster, abort_flag);
   } else {
-    run_epilogue<EPI, DBG>(s, tmem, warp, lane, walk, num_m, m_total, n_total, bias, gate, residual, out,
-                           out_scales, dbg, abort_flag);
+    run_epilogue<EPI, DBG, SPLIT>(s, tmem, warp, lane, plan, cluster, rank, num_m, m_total, n_total, bias, gate, residual,
+                           out, out_scales, dbg, abort_flag);
   }
   __syncwarp();
   tc_fence_before();
@@ -688,20 +870,39 @@ static bool make_scale_maps(CUtensorMap* sa, CUtensorMap* sb, const void* a_scal
   return r == CUDA_SUCCESS;
 }
 
+// Per-device caches of the kernel attribute and of the co-resident cluster count,
+// filled on a device's first call (any thread may fill them).
+template <int EPI, bool DBG, bool SPLIT>
+static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) {
+  auto kern = mx_gemm_kernel<EPI, DBG, SPLIT>;
+  static std::atomic<bool> configured[64];
+  static std::atomic<int> cached[64];
+  const bool cacheable = dev >= 0 && dev < 64;
+  if (!cacheable || !configured[dev].load(std::memory_order_acquire)) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    if (cacheable) configured[dev].store(true, std::memory_order_release);
+  }
+  int n = cacheable ? cached[dev].load(std::memory_order_relaxed) : 0;
+  if (n == 0) {
+    cfg.gridDim = dim3(kPair * 64, 1, 1);
+    cfg.numAttrs = 1;  // the cluster shape only
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorLaunchOutOfResources;
+    if (cacheable) cached[dev].store(n, std::memory_order_relaxed);
+  }
+  *clusters = n;
+  return cudaSuccess;
+}
+
 template <int EPI, bool DBG>
 static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                                   const CUtensorMap& tsb, const GemmArgs& a, int64_t pairs, cudaStream_t stream) {
-  auto kern = mx_gemm_kernel<EPI, DBG>;
-  // per-device caches, filled on a device's first call (any thread may fill them)
-  static std::atomic<bool> configured[64];
+                                   const CUtensorMap& tsb, const GemmArgs& a, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
-  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -716,24 +917,31 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // as many CTA pairs as are co-resident (one CTA per SM), at most one per tile pair
-  static std::atomic<int> max_clusters[64];
-  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev].load(std::memory_order_relaxed) : 0;
-  if (clusters == 0) {
-    cfg.gridDim = dim3(kPair * 64, 1, 1);
-    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorLaunchOutOfResources;
-    if (dev >= 0 && dev < 64) max_clusters[dev].store(clusters, std::memory_order_relaxed);
-  }
-  if (clusters > pairs) clusters = static_cast<int>(pairs);
-  cfg.gridDim = dim3(kPair * clusters, 1, 1);
   cfg.numAttrs = 2;
+  int clusters = 0;
+  e = max_clusters<EPI, DBG, false>(dev, cfg, &clusters);
+  if (e != cudaSuccess) return e;
+  // as many CTA pairs as are co-resident (one CTA per SM), at most one per tile
+  const GemmPlan plan = plan_gemm(a.m, a.n, a.k, clusters, a.workspace, a.workspace_bytes);
+  SplitArgs split = {};
+  if (plan.sk_tiles > 0) {
+    split.sk_tiles = plan.sk_tiles;
+    split.arrivals = static_cast<unsigned*>(a.workspace);
+    split.partial = reinterpret_cast<float4*>(static_cast<uint8_t*>(a.workspace) + kArrivalsBytes);
+  }
+  cfg.gridDim = dim3(kPair * plan.clusters, 1, 1);
+  if (plan.sk_tiles > 0) {
+    // the split instance has the same resources; its attribute is set on first use
+    int same = 0;
+    e = max_clusters<EPI, DBG, true>(dev, cfg, &same);
+    if (e != cudaSuccess) return e;
+    if (same != clusters) return cudaErrorLaunchOutOfResources;
+  }
+  auto kern = plan.sk_tiles > 0 ? mx_gemm_kernel<EPI, DBG, true> : mx_gemm_kernel<EPI, DBG, false>;
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, static_cast<const uint16_t*>(a.bias),
                          static_cast<const uint16_t*>(a.gate), static_cast<const uint16_t*>(a.residual), a.out,
                          static_cast<uint8_t*>(a.out_scales), a.debug_prequant, static_cast<int>(a.m),
-                         static_cast<int>(a.n), static_cast<int>(a.k));
+                         static_cast<int>(a.n), static_cast<int>(a.k), split);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -748,19 +956,35 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, boo
     return cudaSuccess;
   }
   (void)num_sms;
-  const int64_t pairs = ((a.m + kPair * BM - 1) / (kPair * BM)) * (a.n / BN);
   const bool dbg = a.debug_prequant != nullptr;
   switch (a.epilogue) {
-    case kEpiBf16: return launch_instance<kEpiBf16, false>(ta, tb, tsa, tsb, a, pairs, stream);
+    case kEpiBf16: return launch_instance<kEpiBf16, false>(ta, tb, tsa, tsb, a, stream);
     case kEpiGelu:
-      return dbg ? launch_instance<kEpiGelu, true>(ta, tb, tsa, tsb, a, pairs, stream)
-                 : launch_instance<kEpiGelu, false>(ta, tb, tsa, tsb, a, pairs, stream);
+      return dbg ? launch_instance<kEpiGelu, true>(ta, tb, tsa, tsb, a, stream)
+                 : launch_instance<kEpiGelu, false>(ta, tb, tsa, tsb, a, stream);
     case kEpiSwiglu:
-      return dbg ? launch_instance<kEpiSwiglu, true>(ta, tb, tsa, tsb, a, pairs, stream)
-                 : launch_instance<kEpiSwiglu, false>(ta, tb, tsa, tsb, a, pairs, stream);
-    case kEpiGateRes: return launch_instance<kEpiGateRes, false>(ta, tb, tsa, tsb, a, pairs, stream);
+      return dbg ? launch_instance<kEpiSwiglu, true>(ta, tb, tsa, tsb, a, stream)
+                 : launch_instance<kEpiSwiglu, false>(ta, tb, tsa, tsb, a, stream);
+    case kEpiGateRes: return launch_instance<kEpiGateRes, false>(ta, tb, tsa, tsb, a, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t gemm_max_clusters(int* clusters) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return max_clusters<kEpiBf16, false, false>(dev, cfg, clusters);
 }
 
 // A wait that nothing will ever satisfy: it must give up after the bound, set

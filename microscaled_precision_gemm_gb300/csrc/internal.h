@@ -5,6 +5,8 @@
 
 #include <cstdint>
 
+#include "mx.h"
+
 namespace mxk {
 
 // Bits of the device-side error word (read by mx_device_error).
@@ -16,14 +18,88 @@ enum : unsigned {
   kErrSelfTest = 1u << 4,       // the deliberate timeout of mx_selftest_wait_timeout
 };
 
+// zero_words / zero_count: a buffer the kernel also sets to zero (after the previous
+// kernel in the stream has completed), e.g. the split-tail arrival counters of the
+// GEMMs that follow; null / 0 for none.
 cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t ld_x, void* codes, void* scales,
-                                 int num_sms, cudaStream_t stream);
+                                 int num_sms, cudaStream_t stream, unsigned* zero_words = nullptr,
+                                 int zero_count = 0);
 
 // Fused RMSNorm + modulation + MXFP6 quantization (K <= norm_quantize_max_k()).
 int norm_quantize_max_k();
 cudaError_t launch_norm_modulate_quantize(const void* x, int64_t rows, int64_t k, int64_t ld_x, const void* shift,
                                           const void* scale, float eps, void* codes, void* scales, float* dbg,
-                                          int num_sms, cudaStream_t stream);
+                                          int num_sms, cudaStream_t stream, unsigned* zero_words = nullptr,
+                                          int zero_count = 0);
+
+// ---------------------------------------------------------------- split tail
+// The GEMM walks pair tiles of 256 x 256 outputs, 128 K-elements per step.
+// When the tile count leaves only a small last round for the co-resident CTA
+// pairs, most pairs would idle through it; with a workspace, the first
+// pairs + (tiles mod pairs) tiles are instead divided along K so that every
+// pair gets the same number of K-steps, and a tile two pairs share is summed
+// through the workspace (gemm.cu). The split costs about a third of a long tile
+// per pair (two more tile boundaries, the partial sums' stores and loads), so it
+// is taken only where it wins on GB300 (measured): the leftover round at most a
+// quarter full, and at least 32 K-steps (K >= 4096) per tile. Workspace layout
+// (256-byte aligned):
+//   [0, kArrivalsBytes)   arrival counters, one per (split tile, CTA, epilogue warp);
+//                         zero before the launch (the caller's duty, or the MLP's
+//                         first kernel), and zero again after it
+//   [kArrivalsBytes, ...) partial accumulators, two 256 KB slots per pair
+constexpr int kPairTileRows = 256;
+constexpr int kPairTileCols = 256;
+constexpr int kStepK = 128;
+constexpr int kMaxSplitClusters = 80;             // pairs the workspace bound covers (GB300 runs 76)
+constexpr int kMinSplitKSteps = 32;               // shorter tiles: the exchange costs more than it saves
+constexpr int kMaxSplitLeftoverDiv = 4;           // split when tiles mod pairs <= pairs / 4
+constexpr size_t kSplitSlotBytes = size_t{2} * 128 * 256 * 4;
+constexpr int kArrivalWordsPerTile = 2 * 8;       // CTAs x epilogue warps
+constexpr size_t kArrivalsBytes =
+    ((size_t{2} * kMaxSplitClusters * kArrivalWordsPerTile * 4) + 255) / 256 * 256;
+static_assert(kArrivalsBytes == MX_GEMM_WORKSPACE_COUNTER_BYTES, "counter bytes of the public header");
+
+struct SplitArgs {
+  int sk_tiles;          // tiles divided along K (0: none)
+  float4* partial;       // partial-accumulator slots
+  unsigned* arrivals;    // arrival counters
+};
+
+struct GemmPlan {
+  int64_t tiles;    // pair tiles
+  int clusters;     // CTA pairs launched
+  int sk_tiles;     // leading tiles divided along K
+};
+
+inline int64_t gemm_pair_tiles(int64_t m, int64_t n) {
+  return ((m + kPairTileRows - 1) / kPairTileRows) * (n / kPairTileCols);
+}
+
+inline size_t split_arrival_words(int sk_tiles) { return static_cast<size_t>(sk_tiles) * kArrivalWordsPerTile; }
+
+// Workspace bytes that let a GEMM of this shape divide its tail (0: it never does;
+// whether it does also depends on the device's pair count).
+inline size_t split_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+  const int64_t tiles = gemm_pair_tiles(m, n);
+  if (k / kStepK < kMinSplitKSteps || tiles < 2) return 0;
+  const int64_t pairs = tiles - 1 < kMaxSplitClusters ? tiles - 1 : kMaxSplitClusters;
+  return kArrivalsBytes + static_cast<size_t>(2 * pairs) * kSplitSlotBytes;
+}
+
+// Launch plan: CTA pairs (co-resident ones, at most one per tile) and the split tail.
+inline GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int max_clusters, const void* workspace,
+                          size_t workspace_bytes) {
+  GemmPlan p;
+  p.tiles = gemm_pair_tiles(m, n);
+  p.clusters = static_cast<int>(max_clusters < p.tiles ? max_clusters : p.tiles);
+  p.sk_tiles = 0;
+  const int64_t rem = p.clusters > 0 ? p.tiles % p.clusters : 0;
+  if (workspace != nullptr && p.tiles > p.clusters && rem != 0 && rem * kMaxSplitLeftoverDiv <= p.clusters &&
+      k / kStepK >= kMinSplitKSteps && p.clusters <= kMaxSplitClusters && (p.clusters + rem) * (k / kStepK) < (int64_t{1} << 31) &&
+      workspace_bytes >= kArrivalsBytes + static_cast<size_t>(2 * p.clusters) * kSplitSlotBytes)
+    p.sk_tiles = static_cast<int>(p.clusters + rem);
+  return p;
+}
 
 struct GemmArgs {
   const void* a_codes;
@@ -39,11 +115,20 @@ struct GemmArgs {
   int64_t m, n, k;         // n: rows of B (2F for the stacked gate/up weight)
   int epilogue;            // 0: bias + BF16, 1: bias + GELU + MXFP6, 2: bias + SwiGLU + MXFP6
                            // (F = N/2 outputs), 3: residual + gate * (C + bias), BF16
+  void* workspace;         // split-tail workspace (256-byte aligned, counters zero) or null
+  size_t workspace_bytes;
 };
 
 // Returns cudaSuccess or the first CUDA error; `encode_failed` is set when the
 // tensor-map encoder rejected the operands.
 cudaError_t launch_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream, bool* encode_failed);
+
+// Smallest workspace mx_mlp / mx_gated_mlp / mx_dit_mlp_block run with: the MXFP6
+// activations and intermediate, without the split-tail region.
+size_t mlp_min_workspace_bytes(int64_t M, int64_t d, int64_t ff);
+
+// Co-resident CTA pairs of the GEMM kernel on the current device (cached per device).
+cudaError_t gemm_max_clusters(int* clusters);
 
 cudaError_t launch_wait_selftest(cudaStream_t stream);
 

@@ -13,6 +13,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "internal.h"
 #include "mx.h"
 
 namespace {
@@ -49,8 +50,9 @@ extern "C" mx_status mx_mlp_noalloc(const void* x, int64_t M, int64_t d, int64_t
                                     const void* w2_scales, const void* b2, void* y, cudaStream_t stream) {
   if (M < 0 || d < 0 || ff < 0) return MX_ERR_INVALID_ARG;
   if (M == 0) return MX_OK;
-  // sizes beyond the static scratch are refused before anything is launched
-  if (mx_mlp_workspace_bytes(M, d, ff) > kScratchBytes) return MX_ERR_WORKSPACE_TOO_SMALL;
+  // sizes beyond the static scratch are refused before anything is launched; when
+  // the scratch also holds the split-tail region, mx_mlp uses it
+  if (mxk::mlp_min_workspace_bytes(M, d, ff) > kScratchBytes) return MX_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   const mx_status st = scratch_address(&scratch);
   if (st != MX_OK) return st;

@@ -46,7 +46,7 @@ template <bool DBG>
 __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_kernel(
     const uint16_t* __restrict__ x, int rows, int k, int64_t ld_x, const uint16_t* __restrict__ shift,
     const uint16_t* __restrict__ scale, float eps, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-    float* __restrict__ dbg) {
+    float* __restrict__ dbg, unsigned* __restrict__ zero_words, int zero_count) {
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int nwarps = blockDim.x / 32;
@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(kNormMaxWarps * 32, 2) norm_modulate_quantize_
   // inputs / write the outputs only once the previous kernel has completed
   if (threadIdx.x == 0) griddep_launch_dependents();
   griddep_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero_words[i] = 0u;
 
   // this lane's 32 columns of the modulation: (1 + scale) in fp32, shift as BF16 pairs
   float opp[32];
@@ -196,7 +198,7 @@ int norm_quantize_max_k() { return kNormMaxWarps * 1024; }
 
 cudaError_t launch_norm_modulate_quantize(const void* x, int64_t rows, int64_t k, int64_t ld_x, const void* shift,
                                           const void* scale, float eps, void* codes, void* scales, float* dbg,
-                                          int num_sms, cudaStream_t stream) {
+                                          int num_sms, cudaStream_t stream, unsigned* zero_words, int zero_count) {
   if (k % kAtomK != 0 || k > norm_quantize_max_k() || rows > (int64_t{1} << 31) - 1) return cudaErrorInvalidValue;
   const int warps = static_cast<int>((k / kBlock + 31) / 32);
   const int threads = 32 * warps;
@@ -229,7 +231,7 @@ cudaError_t launch_norm_modulate_quantize(const void* x, int64_t rows, int64_t k
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint16_t*>(x), static_cast<int>(rows),
                                      static_cast<int>(k), ld_x, static_cast<const uint16_t*>(shift),
                                      static_cast<const uint16_t*>(scale), eps, static_cast<uint8_t*>(codes),
-                                     static_cast<uint8_t*>(scales), dbg);
+                                     static_cast<uint8_t*>(scales), dbg, zero_words, zero_words ? zero_count : 0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

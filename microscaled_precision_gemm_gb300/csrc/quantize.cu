@@ -62,7 +62,8 @@ static FastDiv make_fast_div(uint32_t d) {
 // are issued before the current one is encoded.
 __global__ void __launch_bounds__(kQuantThreads, 4) quantize_bf16_kernel(
     const uint16_t* __restrict__ x, int rows, int k, int64_t ld_x, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, FastDiv blocks_per_row, uint32_t total_blocks) {
+    uint8_t* __restrict__ scales, FastDiv blocks_per_row, uint32_t total_blocks, unsigned* __restrict__ zero_words,
+    int zero_count) {
   const int lane = threadIdx.x & 31;
   const uint32_t warp_global = (blockIdx.x * kQuantThreads + threadIdx.x) / 32;
   const uint32_t stride = gridDim.x * kQuantThreads;   // blocks per grid-wide step
@@ -73,6 +74,8 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_bf16_kernel(
   // write the outputs only once the previous kernel has completed
   if (threadIdx.x == 0) griddep_launch_dependents();
   griddep_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < zero_count; i += kQuantThreads) zero_words[i] = 0u;
 
   auto load_block = [&](uint32_t b, uint4 (&v)[4]) {
     const uint32_t r = fast_div(b, blocks_per_row);
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_bf16_kernel(
 }
 
 cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t ld_x, void* codes, void* scales,
-                                 int num_sms, cudaStream_t stream) {
+                                 int num_sms, cudaStream_t stream, unsigned* zero_words, int zero_count) {
   const int64_t total_blocks = rows * (k / kBlock);
   if (total_blocks > (int64_t{1} << 32) - (int64_t{1} << 28)) return cudaErrorInvalidValue;  // host checks first
   const int64_t warps_needed = (total_blocks + 31) / 32;
@@ -170,7 +173,7 @@ cudaError_t launch_quantize_bf16(const void* x, int64_t rows, int64_t k, int64_t
   cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_bf16_kernel, static_cast<const uint16_t*>(x), static_cast<int>(rows),
                                      static_cast<int>(k), ld_x, static_cast<uint8_t*>(codes),
                                      static_cast<uint8_t*>(scales), make_fast_div(static_cast<uint32_t>(k / kBlock)),
-                                     static_cast<uint32_t>(total_blocks));
+                                     static_cast<uint32_t>(total_blocks), zero_words, zero_words ? zero_count : 0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

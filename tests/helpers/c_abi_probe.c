@@ -15,7 +15,8 @@ int main(void) {
   /* K % 128 != 0 is rejected before any device call */
   printf("bad_shape %d\n", (int)mx_quantize((const void*)0x10000, 128, 100, 100, (void*)0x20000, (void*)0x30000, 0));
   /* a null pointer is rejected before any device call */
-  printf("null_ptr %d\n", (int)mx_gemm(0, 0, 0, 0, 0, 128, 256, 128, MX_EPI_BIAS_BF16, 0, 0, 0, 0));
+  printf("null_ptr %d\n", (int)mx_gemm(0, 0, 0, 0, 0, 128, 256, 128, MX_EPI_BIAS_BF16, 0, 0, 0, 0, 0, 0));
+  printf("gemm_workspace_bytes %zu\n", mx_gemm_workspace_bytes(20480, 3072, 12288));
   printf("status_ok %s\n", mx_status_string(MX_OK));
   /* host layout round trip: plain -> tiled -> plain */
   uint8_t plain[130 * 4], tiled[256 * 4], back[130 * 4];

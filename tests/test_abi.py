@@ -61,7 +61,18 @@ def test_size_queries(lib):
     assert lib.mx_codes_bytes(-1, 256) == 0
     ws = lib.mx_mlp_workspace_bytes(20480, 3072, 12288)
     need = 20480 * 3072 * 3 // 4 + 20480 * 96 + 20480 * 12288 * 3 // 4 + 20480 * 384
-    assert need <= ws <= need + 4 * 256
+    assert _mlp_base(lib, 20480, 3072, 12288) == need
+    # plus the split-tail region the larger of the two GEMMs needs (here the
+    # down-projection; the up-projection's 24 K-steps never split)
+    up, down = lib.mx_gemm_workspace_bytes(20480, 2 * 12288, 3072), lib.mx_gemm_workspace_bytes(20480, 3072, 12288)
+    assert up == 0 and down > 0
+    assert ws == need + max(up, down)
+
+
+def _mlp_base(lib, M, d, ff):
+    """Smallest MLP workspace: MXFP6 x and h, each part 256-byte aligned."""
+    return sum(-(-n // 256) * 256 for n in (lib.mx_codes_bytes(M, d), lib.mx_scales_bytes(M, d),
+                                            lib.mx_codes_bytes(M, ff), lib.mx_scales_bytes(M, ff)))
 
 
 def _q(lib, x=A32, rows=128, k=256, ld=256, codes=A32b, scales=A32c):
@@ -83,8 +94,8 @@ def test_quantize_rejects_bad_arguments(lib):
 
 
 def _g(lib, a=A32, sa=A32b, b=A32c, sb=A32d, bias=None, M=128, N=512, K=256, epi=BF16, out=A32e,
-       out_sc=A32, dbg=None):
-    return lib.mx_gemm(a, sa, b, sb, bias, M, N, K, epi, out, out_sc, dbg, None)
+       out_sc=A32, dbg=None, ws=None, wsb=0):
+    return lib.mx_gemm(a, sa, b, sb, bias, M, N, K, epi, out, out_sc, dbg, ws, wsb, None)
 
 
 def test_gemm_rejects_bad_arguments(lib):
@@ -102,6 +113,7 @@ def test_gemm_rejects_bad_arguments(lib):
     assert _g(lib, bias=A32 + 2) == MISALIGNED
     assert _g(lib, epi=GELU, out=A32e + 16) == MISALIGNED
     assert _g(lib, epi=GELU, dbg=A32 + 4) == MISALIGNED
+    assert _g(lib, ws=0x100000 + 64, wsb=1 << 26) == MISALIGNED   # the split workspace wants 256 bytes
     assert _g(lib, M=0, a=None, sa=None, b=None, sb=None, out=None) == OK   # empty: no-op
     assert _g(lib, N=0, a=None, sa=None, b=None, sb=None, out=None) == OK
 
@@ -120,7 +132,12 @@ def test_mlp_rejects_bad_arguments(lib):
     assert call(ff=640) == SHAPE
     assert call(x=None) == INVALID
     assert call(ws=0x100000 + 128) == MISALIGNED
-    assert call(wsb=lib.mx_mlp_workspace_bytes(256, 512, 1024) - 1) == WS_SMALL
+    # the smallest workspace holds MXFP6 x and h; the split-tail region after them is optional
+    base = _mlp_base(lib, 256, 512, 1024)
+    assert lib.mx_mlp_workspace_bytes(256, 512, 1024) == base      # K <= 1024: no split region
+    assert lib.mx_mlp_workspace_bytes(256, 4096, 4096) > _mlp_base(lib, 256, 4096, 4096)
+    assert call(wsb=base - 1) == WS_SMALL
+    assert call(wsb=base) not in (OK, WS_SMALL, INVALID, SHAPE, MISALIGNED)   # valid: stops at the device
     assert call(M=0, x=None, y=None, ws=None) == OK
 
 
@@ -133,7 +150,7 @@ def test_swiglu_gemm_arguments(lib):
 
 
 def _gr(lib, bias=None, gate=None, res=0x200000, M=128, N=512, K=256, out=0x400000):
-    return lib.mx_gemm_gate_residual(A32, A32b, A32c, A32d, bias, gate, res, M, N, K, out, None)
+    return lib.mx_gemm_gate_residual(A32, A32b, A32c, A32d, bias, gate, res, M, N, K, out, None, 0, None)
 
 
 def test_gate_residual_rejects_bad_arguments(lib):
@@ -153,7 +170,7 @@ def test_gated_mlp_rejects_bad_arguments(lib):
     assert call(d=384) == SHAPE
     assert call(ff=192) == SHAPE                       # ff % 128
     assert call(x=None) == INVALID
-    assert call(wsb=lib.mx_mlp_workspace_bytes(256, 512, 1024) - 1) == WS_SMALL
+    assert call(wsb=_mlp_base(lib, 256, 512, 1024) - 1) == WS_SMALL
     assert call(M=0, x=None) == OK
 
 
@@ -187,7 +204,7 @@ def test_dit_block_rejects_bad_arguments(lib):
     assert call(eps=-1.0) == INVALID
     assert call(y=A32 + 512) == INVALID                # partial overlap of y and x
     assert call(gate=A32 + 2) == MISALIGNED
-    assert call(wsb=lib.mx_mlp_workspace_bytes(256, 512, 1024) - 1) == WS_SMALL
+    assert call(wsb=_mlp_base(lib, 256, 512, 1024) - 1) == WS_SMALL
     assert call(M=0, x=None, y=None) == OK
 
 
@@ -244,5 +261,21 @@ def test_c_caller_compiles_links_and_runs(mx, tmp_path):
     assert int(got["workspace_bytes"]) == mx.mx_mlp_workspace_bytes(256, 512, 1024)
     assert int(got["bad_shape"]) == SHAPE
     assert int(got["null_ptr"]) == INVALID
+    assert int(got["gemm_workspace_bytes"]) == mx.mx_gemm_workspace_bytes(20480, 3072, 12288)
     assert got["status_ok"] == "MX_OK"
     assert got["layout_round_trip"] == "1"
+
+
+def test_gemm_workspace_bytes(lib):
+    """Split-tail workspace: 10 KB of arrival counters plus two 256 KB slots per CTA
+    pair, for at most 80 pairs and at most one pair fewer than the tiles; none for
+    tiles shorter than 32 K-steps."""
+    slot, counters = 2 * 128 * 256 * 4, 10240
+    assert lib.mx_gemm_workspace_bytes(20480, 3072, 12288) == counters + 2 * 80 * slot
+    assert lib.mx_gemm_workspace_bytes(20480, 12288, 4096) == counters + 2 * 80 * slot
+    assert lib.mx_gemm_workspace_bytes(20480, 12288, 3072) == 0     # 24 K-steps
+    assert lib.mx_gemm_workspace_bytes(1024, 1280, 4096) == counters + 2 * 19 * slot   # 4 x 5 tiles
+    assert lib.mx_gemm_workspace_bytes(4096, 3072, 3968) == 0     # 31 K-steps: never splits
+    assert lib.mx_gemm_workspace_bytes(256, 256, 8192) == 0       # one tile
+    assert lib.mx_gemm_workspace_bytes(256, 384, 8192) == 0       # unsupported N
+    assert lib.mx_gemm_workspace_bytes(0, 256, 8192) == 0
