@@ -12,41 +12,9 @@ comes after it.
 import pytest
 
 import synth
-from mxutil import bf16_to_device
+from mxutil import bf16_to_device, graph_capture as _capture, graph_replays_match as _replays_match
 
 pytestmark = pytest.mark.gpu
-
-
-def _capture(fn):
-    import torch
-
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        fn()   # warm-up on the capture stream
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g):
-        fn()
-    return g
-
-
-def _replays_match(lib, fn_into, make_input, x_buf, y_buf, n=3):
-    """fn_into(x, y) runs the path from x into y; compares graph replays with eager calls."""
-    import torch
-
-    g = _capture(lambda: fn_into(x_buf, y_buf))
-    for i in range(n):
-        x_new = make_input(100 + i)
-        x_buf.copy_(x_new)
-        g.replay()
-        torch.cuda.synchronize()
-        y_eager = torch.empty_like(y_buf)
-        fn_into(x_new, y_eager)
-        torch.cuda.synchronize()
-        assert torch.equal(y_buf, y_eager), f"replay {i} differs from the eager call"
-    assert lib.mx_device_error() == 0
 
 
 def test_mlp_graph_replay(lib):

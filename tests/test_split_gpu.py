@@ -10,8 +10,8 @@ that split with GB300's 76 pairs:
   * the split result against the fp64 oracle (the library's GEMM tolerance);
   * tiles outside the split region bit-identical to the unsplit launch (same
     MMA sequence), split tiles within the tolerance of it;
-  * the same result on repeated calls (two partial sums are added in either
-    order, and fp32 addition of two terms is commutative);
+  * the same result on repeated calls and in CUDA-graph replays (two partial
+    sums are added in either order, and fp32 addition of two terms is commutative);
   * the fused GELU requantization bit-exact given the kernel's own fp32 values,
     SwiGLU and the gate/residual epilogue (in place) on split tiles;
   * the arrival counters zero again after every launch, partial slots holding
@@ -25,7 +25,8 @@ import pytest
 import oracle as O
 import synth
 from mxutil import (assert_codes_equal, assert_gemm_close, assert_swiglu_close, bf16_from_device, bf16_to_device,
-                    f32_from_bf16_bits, gemm_tolerance_report, mx_to_host, mx_upload, sample_rows)
+                    f32_from_bf16_bits, gemm_tolerance_report, graph_replays_match, mx_to_host, mx_upload,
+                    sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -219,3 +220,29 @@ def test_mlp_split_tail(lib):
     # rounding boundary, so a few outputs may move by more than the GEMM bound
     assert r["frac_ok"] >= 0.999, r
     assert lib.mx_device_error() == 0
+
+
+def test_split_mlp_graph_replay(lib):
+    """mx_mlp with both GEMMs split, captured once and replayed on fresh inputs:
+    each replay equals an eager call bit for bit (the first kernel zeroes the
+    counters inside the graph too)."""
+    import torch
+
+    M, d, ff = 5000, 4096, 4096
+    _plan(lib, M, ff, d)
+    _plan(lib, M, d, ff)
+    rng = np.random.default_rng(26)
+
+    def bf16(shape, sd):
+        return bf16_to_device(synth.bf16_round(rng.standard_normal(shape).astype(np.float32) * sd))
+
+    w1, w2 = lib.mx_quantize(bf16((ff, d), 0.02)), lib.mx_quantize(bf16((d, ff), 0.02))
+    b1, b2 = bf16(ff, 0.01), bf16(d, 0.01)
+    ws = torch.empty(lib.mx_mlp_workspace_bytes(M, d, ff), dtype=torch.uint8, device="cuda")
+    x = bf16((M, d), 1.0)
+    y = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+
+    def run(xi, yi):
+        lib.mx_mlp(xi, w1, b1, w2, b2, y=yi, workspace=ws)
+
+    graph_replays_match(lib, run, lambda s: bf16((M, d), 1.0), x, y, n=3)
