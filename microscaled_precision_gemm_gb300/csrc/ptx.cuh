@@ -32,14 +32,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// A waiting thread is suspended until the phase completes or this many nanoseconds
+// pass (the try_wait suspend-time hint). Without it, try_wait returns almost at
+// once and a wait loop spins: the polling warps took issue slots from the MMA and
+// TMA threads on their sub-partitions (measured: SM issue 14% vs 4% for a library
+// GEMM, and 3-6% longer GEMMs). The callers' loops still bound the total wait.
+constexpr uint32_t kWaitSuspendHintNs = 1000000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kWaitSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -49,10 +56,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kWaitSuspendHintNs)
       : "memory");
   return ok != 0;
 }

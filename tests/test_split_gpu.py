@@ -80,6 +80,7 @@ def test_launch_plan_policy(lib):
 
 
 @pytest.mark.parametrize("M,N,K", [(5000, 1024, 4096),    # 80 tiles: all in the split region
+                                   (4900, 1024, 4096),    # the last pair's second CTA wholly past M
                                    (8292, 1280, 4096)])   # 165 tiles: one whole round + the split region
 def test_split_bf16_matches_oracle_and_unsplit(lib, M, N, K):
     import torch
