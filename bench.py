@@ -95,12 +95,12 @@ S_OUT = "out-proj GEMM+bias+gate+residual"
 # capture of the current kernel exists. Source summaries live in profiles/.
 # Written by hand from profiles/*_full_mlp.md and profiles/*_dit_block_swiglu.md.
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", "K1 quantize"): 125857280 + 19578880,
-    ("full_mlp", "K3 up GEMM+GELU+requant"): 80854528 + 148284928,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 237154048 + 108443136,
-    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125881856 + 21643776,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89757184 + 102222080,
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 277535488 + 104813568,
+    ("full_mlp", "K1 quantize"): 125858560 + 19620096,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 80897792 + 148131072,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 236512768 + 108086784,
+    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125879040 + 21440000,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89898752 + 102358784,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 277331712 + 104389632,
 }
 
 
