@@ -21,7 +21,7 @@ its gate and residual (attn_out).
 Timing: CUDA events on the launching stream around exactly K steps, after W
 warm-up steps, with a synchronize (and, under torchrun, a barrier) on both sides;
 the maximum over ranks is reported. Per-kernel events (the roofline's kernel
-times) are recorded inside the same timed region on every other step. Between steps the inputs rotate over two
+times) are recorded inside the same timed region on every fourth step. Between steps the inputs rotate over two
 independent copies (weights, activations, outputs: 2 x 556 MB > 129 MB L2), so no
 step reads operands another step left in L2. nvidia-smi clocks are sampled during
 the timed region.
@@ -158,7 +158,7 @@ class ClockSampler:
 
     def __init__(self, device_index: int):
         self.proc = None
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "25"]
         bus = _pci_bus_id(device_index)
         if bus:
             cmd += ["-i", bus]
@@ -412,10 +412,10 @@ def run_gpu(args) -> dict | None:
         raise RuntimeError("a kernel reported a device-side wait timeout during warm-up")
 
     n_st = len(stage_names)
-    # per-kernel events on every other timed step: an event recorded between two
+    # per-kernel events on every fourth timed step: an event recorded between two
     # kernels ends the programmatic overlap of the second one's launch with the
     # first one's tail, so the uninstrumented steps keep it
-    probe = [i for i in range(args.steps) if i % 2 == 1] or [0]
+    probe = [i for i in range(args.steps) if i % 4 == 3] or [0]
     ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for i in probe}
     clocks = ClockSampler(dev.index or 0)
     time.sleep(0.3)
