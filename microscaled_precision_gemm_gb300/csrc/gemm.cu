@@ -321,9 +321,12 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const P
     }
     tc_fence_after();
     for (int kb = kb0; kb < kb1; ++kb) {
-      // operands of both CTAs landed, scales copied into both SMs' tensor memory
-      if (!wait_bounded(&s.full[stage], phase, abort_flag, kErrWaitMma) ||
-          !wait_bounded(&s.sfready[stage], phase, abort_flag, kErrWaitMma)) {
+      // scales copied into both SMs' tensor memory, and therefore operands landed:
+      // the scale warp copies a stage only after its own wait on full[stage] (which
+      // both CTAs' operand loads complete), and its commit arrives on sfready after
+      // those copies, so acquiring sfready orders this thread after the operand
+      // writes too. One wait per K-step instead of two (measured ~1% faster).
+      if (!wait_bounded(&s.sfready[stage], phase, abort_flag, kErrWaitMma)) {
         ok = false;
         break;
       }
