@@ -19,7 +19,9 @@
 //               atoms its SM's tensor memory needs (its own A rows, all 256 B rows).
 //               All four loads of both CTAs complete on the leader CTA's barrier,
 //               which expects both CTAs' bytes (cta_group::2 TMA completion).
-//   warp 1      leader CTA: issues four tcgen05.mma cta_group::2 kind::mxf8f6f4
+//   warp 1      leader CTA: once the stage's scales are in tensor memory (which
+//               the scale warp signals only after the stage's operands landed),
+//               issues four tcgen05.mma cta_group::2 kind::mxf8f6f4
 //               block_scale per stage (M=256, N=256, K=32, E2M3 x E2M3, E8M0) into
 //               each SM's fp32 accumulator (128 lanes x 256 columns).
 //   warp 10     leader CTA: copies each stage's scale atoms into both SMs' tensor
@@ -37,9 +39,13 @@
 //                 kEpiGateRes   bias, times a per-column gate, plus a BF16 residual,
 //                               BF16 store (an output projection with its gate and
 //                               residual add)
-// Every mbarrier wait is bounded (2 s on the global timer); on expiry the kernel
+// Every mbarrier wait suspends the waiting thread until its phase completes (a
+// try_wait suspend-time hint: spinning waits took issue slots from the MMA and
+// TMA threads) and is bounded (2 s on the global timer); on expiry the kernel
 // records an error bit, drains its in-flight copies and MMAs (again bounded), frees
-// tensor memory and returns. Launched with programmatic dependent launch: the
+// tensor memory and returns. A second instance of the kernel (SPLIT) divides a
+// nearly empty last round of tiles along K across all pairs (see Plan below).
+// Launched with programmatic dependent launch: the
 // prologue (barriers, tensor memory, tensor-map prefetch) may overlap the previous
 // kernel in the stream, and griddepcontrol.wait holds every access to global
 // memory until that kernel has completed.
@@ -188,8 +194,8 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
 // tail, cluster c takes tiles c, c + #clusters, ... When the last round would
 // leave most pairs idle (the host's rule: at most a quarter of a round left over,
 // and long tiles), the first sk_tiles = #clusters + (tiles mod #clusters) tiles
-// are shared out along K instead: their sk_tiles * kblocks K-steps are cut into one contiguous
-// range per cluster (every cluster gets at least one tile's worth), and the
+// are shared out along K instead: their sk_tiles * kblocks K-steps are cut into
+// one contiguous range per cluster (every cluster gets at least one tile's worth), and the
 // remaining tiles, a whole number of rounds, are taken whole as above. A range
 // boundary inside a tile makes it a split tile with exactly two contributors;
 // each stores its fp32 partial accumulator, and whichever arrives second adds
@@ -198,7 +204,7 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
 struct Plan {
   int tiles, num_n, kblocks, clusters, sk_tiles;
   float4* partial;     // split tiles: 2 slots per cluster, each 2 CTAs x 128 rows x 256 fp32
-  unsigned* arrivals;  // split tiles: arrivals per (tile, CTA rank); zero before the launch
+  unsigned* arrivals;  // split tiles: arrivals per (tile, CTA rank, epilogue warp); zero before the launch
 };
 
 // A stretch of one tile's K-steps [kb0, kb1) that one cluster computes.
