@@ -95,12 +95,12 @@ S_OUT = "out-proj GEMM+bias+gate+residual"
 # capture of the current kernel exists. Source summaries live in profiles/.
 # Written by hand from profiles/*_full_mlp.md and profiles/*_dit_block_swiglu.md.
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", "K1 quantize"): 125858560 + 19620096,
-    ("full_mlp", "K3 up GEMM+GELU+requant"): 80897792 + 148131072,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 236512768 + 108086784,
+    ("full_mlp", "K1 quantize"): 125851136 + 19622400,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 81476864 + 148084480,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 243476480 + 104085760,
     ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125879040 + 21440000,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89898752 + 102358784,
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 277331712 + 104389632,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): None,   # kernel changed since the capture
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): None,
 }
 
 
@@ -342,6 +342,51 @@ class Workload:
         return out
 
 
+def gemm_shapes(cfg: dict, M: int) -> list:
+    """(m, n, k) of the step's GEMMs, in BF16 terms (the SwiGLU gate/up GEMM is one 2 ff wide matmul)."""
+    d, ff, kind = cfg["d"], cfg["ff"], cfg["kind"]
+    swiglu = kind == "gated_mlp" or (kind == "block" and cfg.get("activation") == "swiglu")
+    if kind in ("mlp", "gated_mlp", "block"):
+        return [(M, 2 * ff if swiglu else ff, d), (M, d, ff)]
+    if kind in ("up", "gemm", "qkv", "attn_in"):
+        return [(M, ff, d)]
+    if kind == "down":
+        return [(M, d, ff)]
+    if kind == "attn_out":
+        return [(M, d, d)]
+    return []
+
+
+def bf16_context(shapes: list, dev, iters: int = 20) -> dict | None:
+    """torch.matmul in BF16 (cuBLAS) on each shape, back to back after warm-up, CUDA events."""
+    import torch
+
+    if not shapes:
+        return None
+    gen = torch.Generator(device=dev).manual_seed(0)
+    per, total = [], 0.0
+    for (m, n, k) in shapes:
+        a = torch.randn((m, k), device=dev, dtype=torch.bfloat16, generator=gen)
+        b = torch.randn((n, k), device=dev, dtype=torch.bfloat16, generator=gen)
+        out = torch.empty((m, n), device=dev, dtype=torch.bfloat16)
+        for _ in range(3):
+            torch.matmul(a, b.t(), out=out)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            torch.matmul(a, b.t(), out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        per.append({"m": m, "n": n, "k": k, "ms": ms, "tflops": 2 * m * n * k / (ms * 1e-3) / 1e12})
+        total += ms
+        del a, b, out
+    return {"kernel": "torch.matmul BF16 (cuBLAS), the step's GEMM shapes, back to back, outside the timed region",
+            "ms": total, "gemms": per}
+
+
 def mlp_min_workspace_bytes(mx, M: int, d: int, ff: int) -> int:
     """MLP workspace without the split-tail region: MXFP6 x and h, 256-byte aligned parts."""
     parts = (mx.mx_codes_bytes(M, d), mx.mx_scales_bytes(M, d), mx.mx_codes_bytes(M, ff), mx.mx_scales_bytes(M, ff))
@@ -502,6 +547,14 @@ def run_gpu(args) -> dict | None:
     # end to end through the public API with host buffers (rank 0's view; all ranks run it)
     e2e = run_e2e(mx, copies, cfg, args, world)
 
+    # context: the default BF16 GEMM (torch.matmul, cuBLAS) on the step's GEMM shapes,
+    # against this step's MXFP6 GEMM stages (the comparison the source pages make)
+    bf16_ctx = bf16_context(gemm_shapes(cfg, hi - lo), dev)
+    if bf16_ctx is not None:
+        ours = sum(stage_report[n]["ms"] for n in stage_names if work[n]["flops"])
+        bf16_ctx["mxfp6_gemm_ms"] = ours
+        bf16_ctx["mxfp6_speedup"] = bf16_ctx["ms"] / ours if ours > 0 else None
+
     if rank != 0:
         return None
     line = {
@@ -538,6 +591,8 @@ def run_gpu(args) -> dict | None:
         if k1_isolated is not None:
             k1_isolated["frac_hbm"] = k1_isolated["gbs"] / peaks["hbm_gbs"]
             line["quantize_isolated"] = k1_isolated
+    if bf16_ctx is not None:
+        line["bf16_context"] = bf16_ctx
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_budget)
     return line
