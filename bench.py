@@ -99,8 +99,8 @@ NCU_TRAFFIC_BYTES: dict = {
     ("full_mlp", "K3 up GEMM+GELU+requant"): 81476864 + 148084480,
     ("full_mlp", "K2 down GEMM+bias+BF16"): 243476480 + 104085760,
     ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125879040 + 21440000,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): None,   # kernel changed since the capture
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): None,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 90307840 + 102225152,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 277507072 + 101099008,
 }
 
 
