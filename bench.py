@@ -30,6 +30,7 @@ the timed region.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -152,7 +153,7 @@ def barrier(world: int):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -167,7 +168,9 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self) -> dict:
+    def stop(self, window: tuple[float, float] | None = None) -> dict:
+        """Summary of the samples taken inside `window` (wall-clock seconds, the timed
+        region), or of all samples when none fell inside it."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         self.proc.terminate()
@@ -176,23 +179,28 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-                power.append(float(parts[2]))
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                vals = (float(parts[1]), float(parts[2]), float(parts[3]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[3:7]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
+            active = {name for name, val in zip(names, parts[4:8]) if val.lower().startswith("active")}
+            rows.append((t, vals, active))
+        inside = [r for r in rows if window is not None and window[0] <= r[0] <= window[1]]
+        use = inside or rows
+        sm = [r[1][0] for r in use]
+        smax = [r[1][1] for r in use]
+        power = [r[1][2] for r in use]
+        reasons = set().union(*(r[2] for r in use)) if use else set()
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None,
+                "window": "timed region" if inside else "whole sampling run"}
 
 
 def _pci_bus_id(device_index: int) -> str | None:
@@ -468,6 +476,7 @@ def run_gpu(args) -> dict | None:
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    t_region0 = time.time()
     start.record(stream)
     for i in range(args.steps):
         e = ev.get(i)
@@ -479,8 +488,9 @@ def run_gpu(args) -> dict | None:
                 e[j + 1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
+    t_region1 = time.time()
     barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop(window=(t_region0, t_region1))
     total_ms = max_over_ranks(start.elapsed_time(stop), world)
     per_stage = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in probe) / len(probe) for j in range(n_st)]
     if mx.mx_device_error() != 0:
