@@ -1,0 +1,76 @@
+"""Host logic of bench.py that needs no GPU: the per-workload GEMM shapes of the
+BF16 context against the algorithmic work the roofline uses, and the clock
+record's restriction to the samples taken inside the timed region."""
+
+import datetime
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+@pytest.mark.parametrize("name", sorted(bench.CONFIGS))
+def test_bf16_context_shapes_carry_the_step_flops(name):
+    """The BF16 context times the same contractions the step's MXFP6 GEMM stages do."""
+    cfg = bench.CONFIGS[name]
+    M = cfg["M"]
+    shapes = bench.gemm_shapes(cfg, M)
+    work = bench.stage_work(cfg, M)
+    gemm_flops = sum(w["flops"] for w in work.values())
+    assert shapes, name
+    assert sum(2.0 * m * n * k for m, n, k in shapes) == pytest.approx(gemm_flops, rel=1e-12)
+    assert all(m == M for m, _, _ in shapes)
+
+
+class _FakeSmi:
+    """Stands in for the nvidia-smi process: ten samples 25 ms apart starting at t0."""
+
+    def __init__(self, t0: float, cap_at: int):
+        self.t0, self.cap_at = t0, cap_at
+
+    def terminate(self):
+        pass
+
+    def communicate(self, timeout=None):
+        lines = []
+        for i in range(10):
+            ts = datetime.datetime.fromtimestamp(self.t0 + 0.025 * i).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+            cap = "Active" if i == self.cap_at else "Not Active"
+            lines.append(f"{ts}, {1400 + 10 * i}, 2070, {500 + i}.0, Not Active, Not Active, Not Active, {cap}")
+        return "\n".join(lines) + "\n", ""
+
+
+def _sampler(fake):
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.proc = fake
+    return s
+
+
+def test_clock_record_keeps_only_the_timed_region():
+    t0 = 1_700_000_000.0
+    clk = _sampler(_FakeSmi(t0, cap_at=5)).stop(window=(t0 + 0.06, t0 + 0.16))
+    # samples 3, 4, 5, 6 (at +75, +100, +125, +150 ms) fall inside
+    assert clk["window"] == "timed region"
+    assert clk["samples"] == 4
+    assert clk["sm_mhz"] == pytest.approx((1440 + 1450) / 2)
+    assert clk["reasons"] == ["sw_power_cap"]
+    assert clk["power_w_max"] == pytest.approx(506.0)
+
+
+def test_clock_record_outside_the_window_ignores_its_reasons():
+    t0 = 1_700_000_000.0
+    clk = _sampler(_FakeSmi(t0, cap_at=9)).stop(window=(t0, t0 + 0.1))
+    assert clk["samples"] == 5 and clk["reasons"] == []
+
+
+def test_clock_record_without_samples_in_the_window_falls_back_to_all():
+    t0 = 1_700_000_000.0
+    clk = _sampler(_FakeSmi(t0, cap_at=2)).stop(window=(t0 + 10.0, t0 + 11.0))
+    assert clk["window"] == "whole sampling run"
+    assert clk["samples"] == 10 and clk["reasons"] == ["sw_power_cap"]
