@@ -28,6 +28,12 @@ attn_out       attention output a[20480][3072] ~ N(0,1), residual x ~ N(0,1) (W2
                W_o[3072][3072] ~ N(0,0.02), b_o ~ N(0,0.01), gate [3072] ~ N(0,0.5)
 =============  ======================================================================
 
+Tensors too large to draw on the host (the tests of byte offsets beyond 2^32)
+come from a counter-based generator instead, ``hash_bf16_rows`` (numpy, any set of
+rows) and ``hash_bf16_fill_`` (torch, a whole tensor on its device). Both compute
+the same integer function of (row, column, seed), so a test fills the device
+tensor and regenerates only the rows it checks on the host.
+
 Every workload uses seed 0 by default. Each tensor draws from its own child of
 SeedSequence(seed), spawned in the fixed order x, W1, b1, W2, b2, channel
 scales, masks, shift, scale, gate, so that shrinking one tensor never changes
@@ -43,6 +49,8 @@ import numpy as np
 __all__ = [
     "bf16_round",
     "bf16_to_f32",
+    "hash_bf16_rows",
+    "hash_bf16_fill_",
     "workload",
     "pr1",
     "dit_up",
@@ -71,6 +79,59 @@ def bf16_round(x) -> np.ndarray:
 def bf16_to_f32(bits) -> np.ndarray:
     """BF16 bit patterns -> fp32 (exact)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# Counter-based BF16 values. Element (r, c) takes the key
+#   (r * 0x9E3779B1 + c + seed * 0x632BE5AB) mod 2^32
+# through Wellons' "lowbias32" integer hash (x ^= x >> 16; x *= 0x7FEB352D;
+# x ^= x >> 15; x *= 0x846CA68B; x ^= x >> 16, all mod 2^32); hash bit 31 is the
+# sign, bits 24..27 pick the biased exponent 118..133 (magnitudes 2^-9 .. 2^7) and
+# bits 0..6 the mantissa, so every value is a finite normal BF16. All arithmetic
+# runs on int64 values below 2^63 (the 32-bit products are taken in 16-bit halves),
+# so numpy and torch, on any device, compute identical bits. The row multiplier is
+# odd, so two rows' keys differ at every column unless the rows are 2^32 apart.
+_HASH_ROW = 0x9E3779B1
+_HASH_SEED = 0x632BE5AB
+_M32 = 0xFFFFFFFF
+
+
+def _mul32(x, c: int):
+    """x * c mod 2^32 for 0 <= x < 2^32, without leaving int64."""
+    return (x * (c & 0xFFFF) + (((x * (c >> 16)) & 0xFFFF) << 16)) & _M32
+
+
+def _hash_bits(r, c, seed: int):
+    x = (r * _HASH_ROW + c + seed * _HASH_SEED) & _M32
+    x = x ^ (x >> 16)
+    x = _mul32(x, 0x7FEB352D)
+    x = x ^ (x >> 15)
+    x = _mul32(x, 0x846CA68B)
+    x = x ^ (x >> 16)
+    return ((x >> 31) << 15) | ((118 + ((x >> 24) & 15)) << 7) | (x & 0x7F)
+
+
+def hash_bf16_rows(rows, k: int, seed: int = 0) -> np.ndarray:
+    """BF16 bit patterns [len(rows)][k] of the counter-based generator, rows by index."""
+    r = np.asarray(rows, dtype=np.int64).reshape(-1, 1)
+    c = np.arange(k, dtype=np.int64).reshape(1, -1)
+    return _hash_bits(r, c, seed).astype(np.uint16)
+
+
+def hash_bf16_fill_(t, seed: int = 0, row0: int = 0, slab_rows: int = 32768):
+    """Fill a contiguous torch.bfloat16 [R][k] tensor in place with the same values
+    as hash_bf16_rows(range(row0, row0 + R), k, seed), computed on the tensor's
+    device in slabs."""
+    import torch
+
+    rows, k = t.shape
+    dst = t.view(torch.int16)
+    c = torch.arange(k, dtype=torch.int64, device=t.device).reshape(1, -1)
+    for lo in range(0, rows, slab_rows):
+        hi = min(rows, lo + slab_rows)
+        r = torch.arange(row0 + lo, row0 + hi, dtype=torch.int64, device=t.device).reshape(-1, 1)
+        bits = _hash_bits(r, c, seed)
+        dst[lo:hi].copy_(torch.where(bits >= 32768, bits - 65536, bits).to(torch.int16))
+    return t
 
 
 def _rngs(seed: int) -> dict:
