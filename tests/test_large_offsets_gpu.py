@@ -175,3 +175,52 @@ def test_gemm_gelu_requant_beyond_32bit_offsets(lib):
     _padding_scales_zero(out)
     del out
     _free()
+
+
+def test_mlp_beyond_32bit_offsets(lib):
+    """mx_mlp at M = 240,077 tokens, d = 3072, ff = 12288: the MXFP6 intermediate in
+    its workspace holds 2.2 GB (offsets past 2^31 bytes). Activations from the
+    counter-based generator, weights of the full DiT MLP workload. Stage-wise on the
+    boundary rows as in the full-size MLP tests, then end to end against an
+    independent oracle run (>= 99.9% of elements within the tolerance)."""
+    import torch
+
+    from mxutil import gemm_tolerance_report
+
+    M, d, ff = 240_077, 3072, 12288
+    w = synth.full_mlp(M=1, d=d, ff=ff)
+    x = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+    synth.hash_bf16_fill_(x, seed=15)
+    w1q = lib.mx_quantize(bf16_to_device(w["w1"]))
+    w2q = lib.mx_quantize(bf16_to_device(w["w2"]))
+    b1, b2 = bf16_to_device(w["b1"]), bf16_to_device(w["b2"])
+    y = lib.mx_mlp(x, w1q, b1, w2q, b2)
+    xq = lib.mx_quantize(x)
+    del x
+    dbg = torch.empty((M, ff), dtype=torch.float32, device="cuda")
+    hq = lib.mx_gemm(xq, w1q, b1, lib.MX_EPI_BIAS_GELU_MXFP6, debug_prequant=dbg)
+    assert torch.equal(y, lib.mx_gemm(hq, w2q, b2, lib.MX_EPI_BIAS_BF16)), "mx_mlp differs from its three stages"
+
+    rows = _rows(M, [_crossing_row(1 << 32, 4 * ff), _crossing_row(1 << 33, 4 * ff),
+                     _crossing_row(1 << 31, ff * 3 // 4), M - 77], seed=5)
+    idx = torch.as_tensor(rows, device="cuda")
+    x_rows = synth.hash_bf16_rows(rows, d, seed=15)
+    r_w1q, r_w1s = O.quantize_bf16(w["w1"])
+    r_w2q, r_w2s = O.quantize_bf16(w["w2"])
+    rxq, rxs = O.quantize_bf16(x_rows)
+    assert_codes_equal(_codes_rows(xq, rows), rxq, _scale_rows(xq, rows), rxs, "xq")
+    g = dbg.index_select(0, idx).cpu().numpy()
+    del dbg
+    assert_gemm_close(g, O.up_projection(rxq, rxs, r_w1q, r_w1s, w["b1"]), "gelu(x W1^T + b1)")
+    ghq, ghs = _codes_rows(hq, rows), _scale_rows(hq, rows)
+    rhq, rhs = O.quantize_f32(g)
+    assert_codes_equal(ghq, rhq, ghs, rhs, "hq")
+    _padding_scales_zero(hq)
+    got = f32_from_bf16_bits(bf16_from_device(y.index_select(0, idx))).astype(np.float64)
+    assert_gemm_close(got, O.down_projection(ghq, ghs, r_w2q, r_w2s, w["b2"]), "y")
+    y_ref, _ = O.mlp(x_rows, r_w1q, r_w1s, w["b1"], r_w2q, r_w2s, w["b2"])
+    rep = gemm_tolerance_report(got, y_ref)
+    assert rep["frac_ok"] >= 0.999, rep
+    assert lib.mx_device_error() == 0
+    del y, xq, hq
+    _free()
