@@ -212,6 +212,7 @@ def mx_gemm_workspace(m: int, n: int, k: int, device=None, stream=None):
 def _split_workspace(workspace, split: bool, m: int, n: int, k: int, device, stream):
     """(workspace tensor or None, pointer, bytes): the caller's, a new one, or none."""
     if workspace is not None:
+        _on(workspace, device, "workspace", _torch().uint8)
         return workspace, _ptr(workspace), workspace.numel()
     if not split:
         return None, None, 0
@@ -252,6 +253,54 @@ def _empty_u8(n: int, device):
     return _torch().empty(int(n), dtype=_torch().uint8, device=device)
 
 
+def _cuda_device(t, name: str):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.device
+
+
+def _on(t, dev, name: str, dtype, numel: int | None = None, exact: bool = False):
+    """Refuse a tensor that is not a contiguous CUDA tensor of ``dtype`` on ``dev``
+    holding at least (``exact``: exactly) ``numel`` elements. The library takes raw
+    pointers and sizes, so a short, misplaced or strided buffer would be read or
+    written out of bounds on the device; it is refused here instead."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.device != dev:
+        raise ValueError(f"{name} must be a CUDA tensor on {dev}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, not {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and (t.numel() != numel if exact else t.numel() < numel):
+        raise ValueError(f"{name} holds {t.numel()} elements; {'exactly ' if exact else ''}{numel} needed")
+    return t
+
+
+def _vec(t, dev, name: str, n: int):
+    """An optional BF16 vector of exactly n elements on dev."""
+    return None if t is None else _on(t, dev, name, _torch().bfloat16, n, exact=True)
+
+
+def _mx_on(t, dev, name: str, rows: int, k: int):
+    """An MxTensor of [rows][k] whose codes and scales are uint8 buffers on dev of
+    at least the library's sizes."""
+    lib = load()
+    if not isinstance(t, MxTensor) or t.rows != rows or t.k != k:
+        raise ValueError(f"{name} must be an MxTensor of [{rows}][{k}]")
+    _on(t.codes, dev, f"{name}.codes", _torch().uint8, lib.mx_codes_bytes(rows, k))
+    _on(t.scales, dev, f"{name}.scales", _torch().uint8, lib.mx_scales_bytes(rows, k))
+    return t
+
+
+def _bf16_matrix(x, name: str, dev=None):
+    """A contiguous CUDA bfloat16 [rows][K] tensor (on dev when given)."""
+    torch = _torch()
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError(f"{name} must be a bfloat16 [rows][K] CUDA tensor")
+    return _on(x, dev if dev is not None else _cuda_device(x, name), name, torch.bfloat16)
+
+
 def mx_quantize(x, out: MxTensor | None = None, stream=None) -> MxTensor:
     """K1: quantize a BF16 [rows][K] CUDA tensor (row stride may exceed K) to MXFP6."""
     torch = _torch()
@@ -263,6 +312,7 @@ def mx_quantize(x, out: MxTensor | None = None, stream=None) -> MxTensor:
         codes = _empty_u8(lib.mx_codes_bytes(rows, k), x.device).view(rows, -1) if rows else \
             _empty_u8(0, x.device).view(0, k // 4 * 3)
         out = MxTensor(codes, _empty_u8(lib.mx_scales_bytes(rows, k), x.device), rows, k)
+    _mx_on(out, x.device, "out", rows, k)
     st = lib.mx_quantize(_ptr(x), rows, k, x.stride(0), _ptr(out.codes), _ptr(out.scales), _stream_handle(stream))
     _check(st, "mx_quantize")
     return out
@@ -276,13 +326,15 @@ def mx_quantize_rmsnorm_modulate(x, shift=None, scale=None, eps: float = 1e-6, o
     if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
         raise ValueError("mx_quantize_rmsnorm_modulate wants a CUDA bfloat16 [rows][K] tensor")
     rows, k = x.shape
-    for name, v in (("shift", shift), ("scale", scale)):
-        if v is not None and (v.dtype != torch.bfloat16 or v.numel() != k):
-            raise ValueError(f"{name} must be bfloat16 [K]")
+    _vec(shift, x.device, "shift", k)
+    _vec(scale, x.device, "scale", k)
+    if debug_y is not None:
+        _on(debug_y, x.device, "debug_y", torch.float32, rows * k)
     if out is None:
         codes = _empty_u8(lib.mx_codes_bytes(rows, k), x.device).view(rows, -1) if rows else \
             _empty_u8(0, x.device).view(0, k // 4 * 3)
         out = MxTensor(codes, _empty_u8(lib.mx_scales_bytes(rows, k), x.device), rows, k)
+    _mx_on(out, x.device, "out", rows, k)
     st = lib.mx_quantize_rmsnorm_modulate(_ptr(x), rows, k, x.stride(0), _ptr(shift), _ptr(scale), float(eps),
                                           _ptr(out.codes), _ptr(out.scales), _ptr(debug_y), _stream_handle(stream))
     _check(st, "mx_quantize_rmsnorm_modulate")
@@ -331,10 +383,14 @@ def mx_gemm(a: MxTensor, b: MxTensor, bias=None, epilogue: int = MX_EPI_BIAS_BF1
     if a.k != b.k:
         raise ValueError("inner dimensions differ")
     m, n, k = a.rows, b.rows, a.k
-    dev = a.codes.device
+    dev = _cuda_device(a.codes, "a.codes")
+    _mx_on(a, dev, "a", m, k)
+    _mx_on(b, dev, "b", n, k)
+    _vec(bias, dev, "bias", n)
     if epilogue == MX_EPI_BIAS_BF16:
         if out is None:
             out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        _on(out, dev, "out", torch.bfloat16, m * n)
         out_ptr, out_sc = _ptr(out), None
     else:
         w = n // 2 if epilogue == MX_EPI_BIAS_SWIGLU_MXFP6 else n
@@ -342,9 +398,10 @@ def mx_gemm(a: MxTensor, b: MxTensor, bias=None, epilogue: int = MX_EPI_BIAS_BF1
             out = MxTensor(_empty_u8(lib.mx_codes_bytes(m, w), dev).view(m, -1) if m else
                            _empty_u8(0, dev).view(0, w // 4 * 3),
                            _empty_u8(lib.mx_scales_bytes(m, w), dev), m, w)
+        _mx_on(out, dev, "out", m, w)
+        if debug_prequant is not None:
+            _on(debug_prequant, dev, "debug_prequant", torch.float32, m * w)
         out_ptr, out_sc = _ptr(out.codes), _ptr(out.scales)
-    if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != n):
-        raise ValueError("bias must be bfloat16 [N]")
     ws, ws_ptr, ws_bytes = _split_workspace(workspace, split, m, n, k, dev, stream)
     st = lib.mx_gemm(_ptr(a.codes), _ptr(a.scales), _ptr(b.codes), _ptr(b.scales), _ptr(bias), m, n, k,
                      int(epilogue), out_ptr, out_sc, _ptr(debug_prequant), ws_ptr, ws_bytes, _stream_handle(stream))
@@ -356,15 +413,22 @@ def mx_mlp(x, w1: MxTensor, b1, w2: MxTensor, b2, y=None, workspace=None, stream
     """K1 + K3 + K2: y = bf16(MXFP6(gelu(MXFP6(x) W1^T + b1)) W2^T + b2)."""
     torch = _torch()
     lib = load()
+    dev = _bf16_matrix(x, "x").device
     m, d = x.shape
     ff = w1.rows
     if w1.k != d or w2.rows != d or w2.k != ff:
         raise ValueError("weight shapes do not match x")
+    _mx_on(w1, dev, "w1", ff, d)
+    _mx_on(w2, dev, "w2", d, ff)
+    _vec(b1, dev, "b1", ff)
+    _vec(b2, dev, "b2", d)
     if y is None:
         y = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
+    _on(y, dev, "y", torch.bfloat16, m * d)
     need = lib.mx_mlp_workspace_bytes(m, d, ff)
     if workspace is None:
         workspace = _empty_u8(max(need, 256), x.device)
+    _on(workspace, dev, "workspace", torch.uint8)
     st = lib.mx_mlp(_ptr(x), m, d, ff, _ptr(w1.codes), _ptr(w1.scales), _ptr(b1), _ptr(w2.codes),
                     _ptr(w2.scales), _ptr(b2), _ptr(y), _ptr(workspace), workspace.numel(),
                     _stream_handle(stream))
@@ -381,13 +445,17 @@ def mx_gemm_gate_residual(a: MxTensor, b: MxTensor, bias, gate, residual, out=No
     if a.k != b.k:
         raise ValueError("inner dimensions differ")
     m, n, k = a.rows, b.rows, a.k
-    if residual.dtype != torch.bfloat16 or tuple(residual.shape) != (m, n) or not residual.is_contiguous():
+    dev = _cuda_device(residual, "residual")
+    if tuple(residual.shape) != (m, n):
         raise ValueError("residual must be a contiguous bfloat16 [M][N] tensor")
-    for name, v in (("bias", bias), ("gate", gate)):
-        if v is not None and (v.dtype != torch.bfloat16 or v.numel() != n):
-            raise ValueError(f"{name} must be bfloat16 [N]")
+    _on(residual, dev, "residual", torch.bfloat16, m * n)
+    _mx_on(a, dev, "a", m, k)
+    _mx_on(b, dev, "b", n, k)
+    _vec(bias, dev, "bias", n)
+    _vec(gate, dev, "gate", n)
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=residual.device)
+    _on(out, dev, "out", torch.bfloat16, m * n)
     ws, ws_ptr, ws_bytes = _split_workspace(workspace, split, m, n, k, residual.device, stream)
     st = lib.mx_gemm_gate_residual(_ptr(a.codes), _ptr(a.scales), _ptr(b.codes), _ptr(b.scales), _ptr(bias),
                                    _ptr(gate), _ptr(residual), m, n, k, _ptr(out), ws_ptr, ws_bytes,
@@ -401,15 +469,22 @@ def mx_gated_mlp(x, wgu: MxTensor, bgu, w2: MxTensor, b2, y=None, workspace=None
     [g | u] = MXFP6(x) [W_g; W_u]^T + [b_g; b_u]."""
     torch = _torch()
     lib = load()
+    dev = _bf16_matrix(x, "x").device
     m, d = x.shape
     ff = wgu.rows // 2
     if wgu.k != d or wgu.rows != 2 * ff or w2.rows != d or w2.k != ff:
         raise ValueError("weight shapes do not match x")
+    _mx_on(wgu, dev, "wgu", 2 * ff, d)
+    _mx_on(w2, dev, "w2", d, ff)
+    _vec(bgu, dev, "bgu", 2 * ff)
+    _vec(b2, dev, "b2", d)
     if y is None:
         y = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
+    _on(y, dev, "y", torch.bfloat16, m * d)
     need = lib.mx_mlp_workspace_bytes(m, d, ff)
     if workspace is None:
         workspace = _empty_u8(max(need, 256), x.device)
+    _on(workspace, dev, "workspace", torch.uint8)
     st = lib.mx_gated_mlp(_ptr(x), m, d, ff, _ptr(wgu.codes), _ptr(wgu.scales), _ptr(bgu), _ptr(w2.codes),
                           _ptr(w2.scales), _ptr(b2), _ptr(y), _ptr(workspace), workspace.numel(),
                           _stream_handle(stream))
@@ -422,16 +497,24 @@ def mx_dit_mlp_block(x, shift, scale, gate, w_up: MxTensor, b_up, w2: MxTensor, 
     """y = x + gate * MLP(MXFP6(rmsnorm(x) * (1 + scale) + shift)); y may be x (in place)."""
     torch = _torch()
     lib = load()
+    dev = _bf16_matrix(x, "x").device
     m, d = x.shape
     ff = w2.k
     rows_up = 2 * ff if activation == MX_ACT_SWIGLU else ff
     if w_up.k != d or w_up.rows != rows_up or w2.rows != d:
         raise ValueError("weight shapes do not match x")
+    _mx_on(w_up, dev, "w_up", rows_up, d)
+    _mx_on(w2, dev, "w2", d, ff)
+    for name, v, n in (("shift", shift, d), ("scale", scale, d), ("gate", gate, d), ("b_up", b_up, rows_up),
+                       ("b2", b2, d)):
+        _vec(v, dev, name, n)
     if y is None:
         y = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
+    _on(y, dev, "y", torch.bfloat16, m * d)
     need = lib.mx_mlp_workspace_bytes(m, d, ff)
     if workspace is None:
         workspace = _empty_u8(max(need, 256), x.device)
+    _on(workspace, dev, "workspace", torch.uint8)
     st = lib.mx_dit_mlp_block(_ptr(x), m, d, ff, _ptr(shift), _ptr(scale), _ptr(gate), float(eps), int(activation),
                               _ptr(w_up.codes), _ptr(w_up.scales), _ptr(b_up), _ptr(w2.codes), _ptr(w2.scales),
                               _ptr(b2), _ptr(y), _ptr(workspace), workspace.numel(), _stream_handle(stream))
