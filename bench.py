@@ -592,6 +592,8 @@ def run_gpu(args) -> dict | None:
         "pct_fp6_peak_spec_5pf": value / FP6_SPEC_PEAK_TFLOPS,
         "gpu_launches": args.steps * n_st,
         "clocks": clk,
+        "gpu": {"name": torch.cuda.get_device_name(dev),
+                "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
         "e2e": e2e,
     }
     k1 = S_K1 if S_K1 in stage_report else (S_K1N if S_K1N in stage_report else None)
@@ -721,6 +723,20 @@ def _cores() -> int:
         return os.cpu_count() or 1
 
 
+def _cpu_model() -> str:
+    """The host CPU's model name and architecture ("Neoverse-V2 (aarch64)" on a Grace host)."""
+    import platform
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return f"{ln.split(':', 1)[1].strip()} ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine() or "unknown"
+
+
 class OracleWorkload:
     """The configuration's inputs with oracle-quantized weights (setup, untimed)."""
 
@@ -824,8 +840,8 @@ def cpu_baseline(cfg: dict, budget_s: float) -> dict:
     ow.step(rng.integers(0, M, 8))   # warm the thread pools
     rows, dt, flops = _grow_sample(ow, rng, M, budget_s)
     n = len(rows)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
-            "seconds": dt, "sample": f"{n} of {M} token rows of the same workload (weights quantized by the "
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "cpu_model": _cpu_model(),
+            "kind": "oracle", "seconds": dt, "sample": f"{n} of {M} token rows of the same workload (weights quantized by the "
                                      f"oracle beforehand, untimed); fp64 numpy + brute-force E2M3 search"}
 
 
@@ -865,7 +881,8 @@ def run_reference(args) -> dict | None:
         "dtype": "f64",
         "data": "synthetic (seeded numpy PCG64, BF16 RNE; random-init weights)",
         "config": {"workload": cfg["workload"], "M_per_gpu": M, "d": cfg["d"], "ff": cfg["ff"]},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "cpu_model": _cpu_model(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

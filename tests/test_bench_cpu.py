@@ -74,3 +74,11 @@ def test_clock_record_without_samples_in_the_window_falls_back_to_all():
     clk = _sampler(_FakeSmi(t0, cap_at=2)).stop(window=(t0 + 10.0, t0 + 11.0))
     assert clk["window"] == "whole sampling run"
     assert clk["samples"] == 10 and clk["reasons"] == ["sw_power_cap"]
+
+
+def test_cpu_model_names_the_host():
+    import platform
+
+    name = bench._cpu_model()
+    assert isinstance(name, str) and name
+    assert platform.machine() in name
