@@ -96,12 +96,12 @@ S_OUT = "out-proj GEMM+bias+gate+residual"
 # capture of the current kernel exists. Source summaries live in profiles/.
 # Written by hand from profiles/*_full_mlp.md and profiles/*_dit_block_swiglu.md.
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", "K1 quantize"): 125851136 + 19622400,
-    ("full_mlp", "K3 up GEMM+GELU+requant"): 81476864 + 148084480,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 243476480 + 104085760,
-    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125879040 + 21440000,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 90307840 + 102225152,
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 277507072 + 101099008,
+    ("full_mlp", "K1 quantize"): 125853952 + 19825152,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 81096704 + 147971840,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 248584704 + 108426752,
+    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125878528 + 21619200,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 90269184 + 102149376,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 278013440 + 105329408,
 }
 
 

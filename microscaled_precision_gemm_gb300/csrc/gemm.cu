@@ -39,6 +39,11 @@
 //                 kEpiGateRes   bias, times a per-column gate, plus a BF16 residual,
 //                               BF16 store (an output projection with its gate and
 //                               residual add)
+//               The two BF16 epilogues stage each 32-row x 32-column block in the
+//               warp's own 2 KB shared slot and write it with one TMA tensor store:
+//               whole 64-byte row segments instead of a 16-byte piece of 32 rows per
+//               store instruction, which kept the shared-memory pipe busy that the
+//               main loop's operand traffic needs.
 // Every mbarrier wait suspends the waiting thread until its phase completes (a
 // try_wait suspend-time hint: spinning waits took issue slots from the MMA and
 // TMA threads) and is bounded (2 s on the global timer); on expiry the kernel
@@ -90,6 +95,8 @@ constexpr uint32_t kStageTx = (kABytes + kBBytes) / 4 * 3 + kSfaBytes + kSfbByte
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = BN;  // scale slots after the accumulator: stage s at +16 s (A +0, B +8)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kOutBoxCols = 32;                                   // one epilogue chunk
+constexpr uint32_t kOutStageBytes = 32 * kOutBoxCols * 2;         // 32 rows of BF16
 
 struct __align__(1024) SharedStorage {
   uint8_t a[kStages][kABytes];
@@ -106,6 +113,9 @@ struct __align__(1024) SharedStorage {
   int abort_flag;
   alignas(16) float bias_s[kEpiWarps][kEpiCols];   // each epilogue warp's bias values (read as float4)
   alignas(16) float gate_s[kEpiWarps][kEpiCols];   // kEpiGateRes: each epilogue warp's gate values
+  // BF16 epilogues: each epilogue warp's 32 x 32 output block (64-byte swizzle),
+  // the source of its TMA stores
+  alignas(1024) uint8_t out_stage[kEpiWarps][kOutStageBytes];
 };
 constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;
 static_assert(offsetof(SharedStorage, bias_s) % 16 == 0 && offsetof(SharedStorage, gate_s) % 16 == 0,
@@ -113,6 +123,8 @@ static_assert(offsetof(SharedStorage, bias_s) % 16 == 0 && offsetof(SharedStorag
 static_assert(offsetof(SharedStorage, sfa) % 128 == 0 && offsetof(SharedStorage, sfb) % 128 == 0,
               "scale atoms are TMA destinations");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(offsetof(SharedStorage, out_stage) % 1024 == 0 && kOutStageBytes % 1024 == 0,
+              "TMA store sources sit on 1024-byte boundaries (the 64-byte swizzle repeats every 512 bytes)");
 static_assert(kPair * BM == kPairTileRows && BN == kPairTileCols && BK == kStepK, "tile geometry of the launch plan");
 static_assert(kPair * kEpiWarps == kArrivalWordsPerTile, "one arrival counter per CTA and epilogue warp");
 static_assert(kSplitSlotBytes == size_t{kPair} * kEpiWarps * kEpiChunks * 8 * 32 * sizeof(float4),
@@ -542,6 +554,8 @@ struct EpiCtx {
   uint32_t tmem, tmem_empty_leader;
   float* bw;
   float* gw;
+  const CUtensorMap* tmap_out;   // BF16 epilogues: the output, box 32 x 32, 64-byte swizzle
+  uint8_t* ostage;               // this warp's TMA store source
 };
 
 // The epilogue of one output tile (or, SPLIT, of one unit of the split region):
@@ -588,10 +602,10 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
     if ((u.kb0 != 0 || u.kb1 != pl.kblocks) && !split_exchange(pl, cluster, rank, warp - 2, lane, u, r)) return true;
   }
 
-  const int64_t row = static_cast<int64_t>(mb) * BM + 32 * q + lane;
+  const int64_t row0 = static_cast<int64_t>(mb) * BM + 32 * q;   // the warp's first row
+  const int64_t row = row0 + lane;
   const bool live = row < m_total;
   if constexpr (EPI == kEpiBf16 || EPI == kEpiGateRes) {
-    uint16_t* y = static_cast<uint16_t*>(out);
 #pragma unroll
     for (int c = 0; c < kEpiChunks; ++c) {
       const int n = col0 + 32 * c;
@@ -632,10 +646,21 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
         pk[2 * v] = cvt_bf16x2(x1, x0);
         pk[2 * v + 1] = cvt_bf16x2(x3, x2);
       }
-      if (live) {
-        uint4* dst = reinterpret_cast<uint4*>(y + row * n_total + n);
+      // the slot is free once the warp's previous store has read it
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      // 16-byte piece j of row `lane` at piece j ^ ((lane >> 1) & 3) of the row (the
+      // 64-byte swizzle), so the warp's 16-byte writes fall on distinct banks
+      uint4* srow = reinterpret_cast<uint4*>(e.ostage + lane * (kOutBoxCols * 2));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      for (int j = 0; j < 4; ++j)
+        srow[j ^ ((lane >> 1) & 3)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      fence_proxy_async_shared();
+      __syncwarp();
+      // rows past M in the box are not written; a box wholly past M is not issued
+      if (lane == 0 && row0 < m_total) {
+        tma_store_2d(e.tmap_out, e.ostage, n, static_cast<int32_t>(row0));
+        bulk_commit_group();
       }
     }
   } else {
@@ -689,7 +714,8 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
 
 template <int EPI, bool DBG, bool SPLIT>
 __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, const Plan& pl,
-                                             int cluster, int rank, int num_m, int m_total, int n_total,
+                                             const CUtensorMap* tmap_out, int cluster, int rank, int num_m,
+                                             int m_total, int n_total,
                                              const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate,
                                              const uint16_t* residual, void* out, uint8_t* __restrict__ out_scales,
                                              float* __restrict__ dbg, volatile int* abort_flag) {
@@ -709,6 +735,8 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
   e.tmem_empty_leader = mapa_shared(smem_u32(&s.tmem_empty), 0);
   e.bw = s.bias_s[warp - 2];
   e.gw = s.gate_s[warp - 2];
+  e.tmap_out = tmap_out;
+  e.ostage = s.out_stage[warp - 2];
   uint32_t acc_phase = 0;
   // the split region first, in its own loop
   if constexpr (SPLIT) {
@@ -738,7 +766,7 @@ template <int EPI, bool DBG, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sb,
-                   const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate, const uint16_t* residual,
+                   const __grid_constant__ CUtensorMap tmap_out, const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate, const uint16_t* residual,
                    void* out, uint8_t* __restrict__ out_scales, float* __restrict__ dbg, int m_total, int n_total,
                    int k_total, SplitArgs split) {
   extern __shared__ uint8_t smem_raw[];
@@ -782,6 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmap_b);
     prefetch_tensormap(&tmap_sa);
     prefetch_tensormap(&tmap_sb);
+    if constexpr (EPI == kEpiBf16 || EPI == kEpiGateRes) prefetch_tensormap(&tmap_out);
   }
   // both CTAs' barriers and tensor memory exist before either touches the other's
   cluster_sync();
@@ -802,8 +831,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 2 + kEpiWarps) {
     if (lane == 0 && rank == 0) run_scales<SPLIT>(s, tmem, plan, cluster, abort_flag);
   } else {
-    run_epilogue<EPI, DBG, SPLIT>(s, tmem, warp, lane, plan, cluster, rank, num_m, m_total, n_total, bias, gate, residual,
-                           out, out_scales, dbg, abort_flag);
+    run_epilogue<EPI, DBG, SPLIT>(s, tmem, warp, lane, plan, &tmap_out, cluster, rank, num_m, m_total, n_total, bias,
+                                  gate, residual, out, out_scales, dbg, abort_flag);
+    // the stores' writes are complete (and their shared sources read) before the
+    // CTA leaves, also after a wait gave up
+    if constexpr (EPI == kEpiBf16 || EPI == kEpiGateRes) {
+      if (lane == 0) bulk_wait_all();
+    }
   }
   __syncwarp();
   tc_fence_before();
@@ -879,6 +913,22 @@ static bool make_scale_maps(CUtensorMap* sa, CUtensorMap* sb, const void* a_scal
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over a BF16 output [m][n] for the epilogues' TMA stores: box 32
+// columns x 32 rows (one epilogue warp's block), 64-byte swizzle.
+static bool make_bf16_out_map(CUtensorMap* map, void* out, int64_t m, int64_t n) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  std::memset(map, 0, sizeof(*map));
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(n) * 2};
+  cuuint32_t box[2] = {kOutBoxCols, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Per-device caches of the kernel attribute and of the co-resident cluster count,
 // filled on a device's first call (any thread may fill them).
 template <int EPI, bool DBG, bool SPLIT>
@@ -908,7 +958,8 @@ static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) 
 
 template <int EPI, bool DBG>
 static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                                   const CUtensorMap& tsb, const GemmArgs& a, cudaStream_t stream) {
+                                   const CUtensorMap& tsb, const CUtensorMap& tout, const GemmArgs& a,
+                                   cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -947,7 +998,7 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
     if (same != clusters) return cudaErrorLaunchOutOfResources;
   }
   auto kern = plan.sk_tiles > 0 ? mx_gemm_kernel<EPI, DBG, true> : mx_gemm_kernel<EPI, DBG, false>;
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, static_cast<const uint16_t*>(a.bias),
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tout, static_cast<const uint16_t*>(a.bias),
                          static_cast<const uint16_t*>(a.gate), static_cast<const uint16_t*>(a.residual), a.out,
                          static_cast<uint8_t*>(a.out_scales), a.debug_prequant, static_cast<int>(a.m),
                          static_cast<int>(a.n), static_cast<int>(a.k), split);
@@ -957,24 +1008,27 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, bool* encode_failed) {
   *encode_failed = false;
-  CUtensorMap ta, tb, tsa, tsb;
+  CUtensorMap ta, tb, tsa, tsb, tout;
+  std::memset(&tout, 0, sizeof(tout));   // read only by the BF16 epilogues
+  const bool bf16_out = a.epilogue == kEpiBf16 || a.epilogue == kEpiGateRes;
   if (!make_codes_map(&ta, a.a_codes, a.m, a.k, BM) ||
       !make_codes_map(&tb, a.b_codes, a.n, a.k, kBHalfRows) ||
-      !make_scale_maps(&tsa, &tsb, a.a_scales, a.b_scales, a.m, a.n, a.k, a.epilogue == kEpiSwiglu ? 1u : 2u)) {
+      !make_scale_maps(&tsa, &tsb, a.a_scales, a.b_scales, a.m, a.n, a.k, a.epilogue == kEpiSwiglu ? 1u : 2u) ||
+      (bf16_out && !make_bf16_out_map(&tout, a.out, a.m, a.n))) {
     *encode_failed = true;
     return cudaSuccess;
   }
   (void)num_sms;
   const bool dbg = a.debug_prequant != nullptr;
   switch (a.epilogue) {
-    case kEpiBf16: return launch_instance<kEpiBf16, false>(ta, tb, tsa, tsb, a, stream);
+    case kEpiBf16: return launch_instance<kEpiBf16, false>(ta, tb, tsa, tsb, tout, a, stream);
     case kEpiGelu:
-      return dbg ? launch_instance<kEpiGelu, true>(ta, tb, tsa, tsb, a, stream)
-                 : launch_instance<kEpiGelu, false>(ta, tb, tsa, tsb, a, stream);
+      return dbg ? launch_instance<kEpiGelu, true>(ta, tb, tsa, tsb, tout, a, stream)
+                 : launch_instance<kEpiGelu, false>(ta, tb, tsa, tsb, tout, a, stream);
     case kEpiSwiglu:
-      return dbg ? launch_instance<kEpiSwiglu, true>(ta, tb, tsa, tsb, a, stream)
-                 : launch_instance<kEpiSwiglu, false>(ta, tb, tsa, tsb, a, stream);
-    case kEpiGateRes: return launch_instance<kEpiGateRes, false>(ta, tb, tsa, tsb, a, stream);
+      return dbg ? launch_instance<kEpiSwiglu, true>(ta, tb, tsa, tsb, tout, a, stream)
+                 : launch_instance<kEpiSwiglu, false>(ta, tb, tsa, tsb, tout, a, stream);
+    case kEpiGateRes: return launch_instance<kEpiGateRes, false>(ta, tb, tsa, tsb, tout, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
