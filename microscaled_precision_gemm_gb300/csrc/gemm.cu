@@ -39,11 +39,12 @@
 //                 kEpiGateRes   bias, times a per-column gate, plus a BF16 residual,
 //                               BF16 store (an output projection with its gate and
 //                               residual add)
-//               The two BF16 epilogues stage each 32-row x 32-column block in the
-//               warp's own 2 KB shared slot and write it with one TMA tensor store:
-//               whole 64-byte row segments instead of a 16-byte piece of 32 rows per
-//               store instruction, which kept the shared-memory pipe busy that the
-//               main loop's operand traffic needs.
+//               Every epilogue stages its output in the warp's own 2 KB shared slot
+//               and writes it with TMA tensor stores: a 32-row x 32-column BF16
+//               block, or the 6-bit codes of two 32-column MX blocks (48 bytes) of
+//               32 rows. Each thread storing its own row instead (a 16- or 8-byte
+//               piece of 32 rows per store instruction) kept busy the
+//               shared-memory pipe that the main loop's operand traffic needs.
 // Every mbarrier wait suspends the waiting thread until its phase completes (a
 // try_wait suspend-time hint: spinning waits took issue slots from the MMA and
 // TMA threads) and is bounded (2 s on the global timer); on expiry the kernel
@@ -97,6 +98,8 @@ constexpr uint32_t kSfCol0 = BN;  // scale slots after the accumulator: stage s 
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kOutBoxCols = 32;                                   // one epilogue chunk
 constexpr uint32_t kOutStageBytes = 32 * kOutBoxCols * 2;         // 32 rows of BF16
+constexpr uint32_t kCodesBoxBytes = 48;                           // two MX blocks of 6-bit codes
+static_assert(32 * kCodesBoxBytes <= kOutStageBytes, "a codes box fits the store slot");
 
 struct __align__(1024) SharedStorage {
   uint8_t a[kStages][kABytes];
@@ -113,8 +116,8 @@ struct __align__(1024) SharedStorage {
   int abort_flag;
   alignas(16) float bias_s[kEpiWarps][kEpiCols];   // each epilogue warp's bias values (read as float4)
   alignas(16) float gate_s[kEpiWarps][kEpiCols];   // kEpiGateRes: each epilogue warp's gate values
-  // BF16 epilogues: each epilogue warp's 32 x 32 output block (64-byte swizzle),
-  // the source of its TMA stores
+  // each epilogue warp's output box (BF16 32 x 32 with a 64-byte swizzle, or 32
+  // rows of 48 code bytes), the source of its TMA stores
   alignas(1024) uint8_t out_stage[kEpiWarps][kOutStageBytes];
 };
 constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;
@@ -475,13 +478,6 @@ __device__ __forceinline__ void silu_mul2(uint64_t g, uint64_t u, float& h0, flo
   f2_unpack(f2_mul(f2_mul(g, f2_pack(rcp_approx(d0), rcp_approx(d1))), u), h0, h1);
 }
 
-__device__ __forceinline__ void store_block_codes(uint8_t* dst_bytes, const uint32_t (&w)[6]) {
-  uint2* dst = reinterpret_cast<uint2*>(dst_bytes);
-  dst[0] = make_uint2(w[0], w[1]);
-  dst[1] = make_uint2(w[2], w[3]);
-  dst[2] = make_uint2(w[4], w[5]);
-}
-
 __device__ __forceinline__ void store_dbg32(float* d, const float (&g)[32]) {
   float4* p = reinterpret_cast<float4*>(d);
 #pragma unroll
@@ -554,7 +550,8 @@ struct EpiCtx {
   uint32_t tmem, tmem_empty_leader;
   float* bw;
   float* gw;
-  const CUtensorMap* tmap_out;   // BF16 epilogues: the output, box 32 x 32, 64-byte swizzle
+  const CUtensorMap* tmap_out;   // the output: BF16 boxes of 32 x 32 (64-byte swizzle) or
+                                 // 6-bit codes in boxes of 32 rows x 48 bytes
   uint8_t* ostage;               // this warp's TMA store source
 };
 
@@ -666,8 +663,9 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
   } else {
     // MXFP6 requantization along the output columns, one 32-column block at a time
     constexpr int kBlocks = (EPI == kEpiSwiglu) ? kEpiChunks / 2 : kEpiChunks;
-    uint8_t* codes = static_cast<uint8_t*>(out);
+    static_assert(kBlocks % 2 == 0, "codes leave in boxes of two 32-column blocks");
     uint32_t scale_word = 0;
+    uint32_t wprev[6];   // the codes of the first block of each pair
 #pragma unroll
     for (int c = 0; c < kBlocks; ++c) {
       const int n = col0 + 32 * c;
@@ -695,8 +693,28 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
       }
       uint32_t w[6];
       const uint32_t sc = quant_block32(g, w);
-      if (live) store_block_codes(codes + row * (n_out / 4 * 3) + n / 4 * 3, w);
       scale_word |= sc << (8 * c);
+      if ((c & 1) == 0) {
+#pragma unroll
+        for (int i = 0; i < 6; ++i) wprev[i] = w[i];
+        continue;
+      }
+      // two blocks' codes (48 bytes of the row) into the warp's slot, 48-byte rows:
+      // 16-byte group 3 lane + j of the slot, distinct for eight consecutive lanes,
+      // so the writes take the minimum wavefronts; then one TMA store of the
+      // 32-row x 48-byte box
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      uint4* srow = reinterpret_cast<uint4*>(e.ostage + lane * kCodesBoxBytes);
+      srow[0] = make_uint4(wprev[0], wprev[1], wprev[2], wprev[3]);
+      srow[1] = make_uint4(wprev[4], wprev[5], w[0], w[1]);
+      srow[2] = make_uint4(w[2], w[3], w[4], w[5]);
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0 && row0 < m_total) {
+        tma_store_2d(e.tmap_out, e.ostage, (n - 32) / 4 * 3, static_cast<int32_t>(row0));
+        bulk_commit_group();
+      }
     }
     // padding rows of the last row tile get zero scales; a row tile past the
     // last one (second half of the last pair) has no scale storage at all
@@ -810,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmap_b);
     prefetch_tensormap(&tmap_sa);
     prefetch_tensormap(&tmap_sb);
-    if constexpr (EPI == kEpiBf16 || EPI == kEpiGateRes) prefetch_tensormap(&tmap_out);
+    prefetch_tensormap(&tmap_out);
   }
   // both CTAs' barriers and tensor memory exist before either touches the other's
   cluster_sync();
@@ -835,9 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   gate, residual, out, out_scales, dbg, abort_flag);
     // the stores' writes are complete (and their shared sources read) before the
     // CTA leaves, also after a wait gave up
-    if constexpr (EPI == kEpiBf16 || EPI == kEpiGateRes) {
-      if (lane == 0) bulk_wait_all();
-    }
+    if (lane == 0) bulk_wait_all();
   }
   __syncwarp();
   tc_fence_before();
@@ -929,6 +945,22 @@ static bool make_bf16_out_map(CUtensorMap* map, void* out, int64_t m, int64_t n)
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over packed 6-bit output codes [m][w] (3 w / 4 bytes a row) for the
+// requantizing epilogues' TMA stores: box 48 bytes (two MX blocks) x 32 rows.
+static bool make_codes_out_map(CUtensorMap* map, void* codes, int64_t m, int64_t w) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  std::memset(map, 0, sizeof(*map));
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(w / 4 * 3), static_cast<cuuint64_t>(m)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(w / 4 * 3)};
+  cuuint32_t box[2] = {kCodesBoxBytes, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, codes, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Per-device caches of the kernel attribute and of the co-resident cluster count,
 // filled on a device's first call (any thread may fill them).
 template <int EPI, bool DBG, bool SPLIT>
@@ -1009,12 +1041,12 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, bool* encode_failed) {
   *encode_failed = false;
   CUtensorMap ta, tb, tsa, tsb, tout;
-  std::memset(&tout, 0, sizeof(tout));   // read only by the BF16 epilogues
   const bool bf16_out = a.epilogue == kEpiBf16 || a.epilogue == kEpiGateRes;
+  const int64_t w_out = a.epilogue == kEpiSwiglu ? a.n / 2 : a.n;
   if (!make_codes_map(&ta, a.a_codes, a.m, a.k, BM) ||
       !make_codes_map(&tb, a.b_codes, a.n, a.k, kBHalfRows) ||
       !make_scale_maps(&tsa, &tsb, a.a_scales, a.b_scales, a.m, a.n, a.k, a.epilogue == kEpiSwiglu ? 1u : 2u) ||
-      (bf16_out && !make_bf16_out_map(&tout, a.out, a.m, a.n))) {
+      !(bf16_out ? make_bf16_out_map(&tout, a.out, a.m, a.n) : make_codes_out_map(&tout, a.out, a.m, w_out))) {
     *encode_failed = true;
     return cudaSuccess;
   }
