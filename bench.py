@@ -96,12 +96,12 @@ S_OUT = "out-proj GEMM+bias+gate+residual"
 # capture of the current kernel exists. Source summaries live in profiles/.
 # Written by hand from profiles/*_full_mlp.md and profiles/*_dit_block_swiglu.md.
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", "K1 quantize"): 125853952 + 19825152,
-    ("full_mlp", "K3 up GEMM+GELU+requant"): None,   # kernel changed since the last capture
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 248584704 + 108426752,
-    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125878528 + 21619200,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): None,   # kernel changed since the last capture
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 278013440 + 105329408,
+    ("full_mlp", "K1 quantize"): 125856512 + 19715328,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 79952128 + 152724224,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 247360512 + 107715072,
+    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125880320 + 21430272,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89568256 + 105759232,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 278096640 + 104801792,
 }
 
 
