@@ -82,3 +82,22 @@ def test_cpu_model_names_the_host():
     name = bench._cpu_model()
     assert isinstance(name, str) and name
     assert platform.machine() in name
+
+
+def test_reference_arm_prints_one_contract_line(capsys):
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON line
+    with the contract's keys, a cpu_baseline describing the run and a zero-copy e2e."""
+    import json
+
+    bench.main(["--impl", "reference", "--config", "pr1", "--steps", "1", "--warmup", "3", "--cpu-budget", "0.2"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 3 and d["value"] > 0
+    assert d["config"]["workload"] == bench.CONFIGS["pr1"]["workload"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
