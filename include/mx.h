@@ -179,9 +179,9 @@ mx_status mx_gemm(const void* a_codes, const void* a_scales, const void* b_codes
  *              aligned, or NULL for a gate of 1 (plain residual add)
  *   residual : device BF16 [M][N] row-major, 16-byte aligned; required
  *   out      : device BF16 [M][N] row-major, 16-byte aligned (written). It may be
- *              residual itself (in-place update: each element is read before it
- *              is written, by the same thread); any other overlap returns
- *              MX_ERR_INVALID_ARG.
+ *              residual itself (in-place update: the warp that reads a block of
+ *              the residual issues that block's store only after its loads); any
+ *              other overlap returns MX_ERR_INVALID_ARG.
  *   workspace, workspace_bytes : the optional split-tail scratch, as mx_gemm.
  */
 mx_status mx_gemm_gate_residual(const void* a_codes, const void* a_scales, const void* b_codes,
