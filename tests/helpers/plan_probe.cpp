@@ -1,0 +1,20 @@
+// Prints the GEMM launch plan (pair tiles, CTA pairs, leading tiles divided along K)
+// and the split-tail workspace size for shapes read from standard input, one
+// "m n k max_clusters workspace_bytes" per line (workspace_bytes < 0: no workspace).
+// Host code only: the plan is inline in the library's internal header.
+#include <cstdio>
+
+#include "internal.h"
+
+int main() {
+  long long m, n, k, ws;
+  int clusters;
+  static unsigned char dummy[1];
+  while (std::scanf("%lld %lld %lld %d %lld", &m, &n, &k, &clusters, &ws) == 5) {
+    const mxk::GemmPlan p = mxk::plan_gemm(m, n, k, clusters, ws < 0 ? nullptr : dummy,
+                                           ws < 0 ? 0 : static_cast<size_t>(ws));
+    std::printf("%lld %d %d %zu\n", static_cast<long long>(p.tiles), p.clusters, p.sk_tiles,
+                mxk::split_workspace_bytes(m, n, k));
+  }
+  return 0;
+}

@@ -1,0 +1,80 @@
+"""The GEMM's launch plan on the host, without a GPU: how many CTA pairs launch,
+and when the nearly empty last round of tiles is divided along K (the split
+tail). The rule: split when a workspace of the full size is given, the tiles do
+not fit one round, the leftover round is at most a quarter full, and each tile has
+at least 32 K-steps of 128 (K >= 4096); the first pairs + leftover tiles are then
+divided. The workspace holds 10240 bytes of arrival counters plus two 256 KB
+partial-sum slots per pair, for at most 80 pairs."""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "microscaled_precision_gemm_gb300", "csrc")
+COUNTERS = 10240
+SLOT = 2 * 128 * 256 * 4
+
+
+@pytest.fixture(scope="module")
+def plan(tmp_path_factory):
+    cxx = shutil.which("g++")
+    cuda_inc = "/usr/local/cuda/include"
+    if cxx is None or not os.path.isdir(cuda_inc):
+        pytest.skip("g++ or the CUDA headers are not available")
+    exe = str(tmp_path_factory.mktemp("plan") / "plan_probe")
+    subprocess.run([cxx, "-std=c++17", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", CSRC,
+                    "-I", cuda_inc, os.path.join(ROOT, "tests", "helpers", "plan_probe.cpp"), "-o", exe], check=True)
+
+    def run(m, n, k, clusters=76, ws=None):
+        full = COUNTERS + 2 * min(80, max(1, ((m + 255) // 256) * (n // 256) - 1)) * SLOT
+        ws_bytes = full if ws is None else ws
+        out = subprocess.run([exe], input=f"{m} {n} {k} {clusters} {ws_bytes}\n", capture_output=True, text=True,
+                             check=True).stdout.split()
+        return tuple(int(v) for v in out)
+
+    return run
+
+
+def test_dit_down_projection_splits_its_leftover_round(plan):
+    # 64 x 12 = 768 pair tiles on 76 pairs: 10 rounds + 8; K = 12288 is 96 K-steps
+    assert plan(16384, 3072, 12288) == (768, 76, 76 + 8, COUNTERS + 2 * 80 * SLOT)
+
+
+def test_full_leftover_rounds_stay_whole(plan):
+    assert plan(20480, 12288, 3072)[:3] == (3840, 76, 0)    # 40 left over > 76 / 4
+    assert plan(20480, 3072, 12288)[:3] == (960, 76, 0)     # 48 left over
+
+
+def test_short_tiles_never_split(plan):
+    # M = 4096 up-projection: 768 tiles, 8 left over, but 24 K-steps per tile
+    tiles, pairs, split, ws = plan(4096, 12288, 3072)
+    assert (tiles, pairs, split, ws) == (768, 76, 0, 0)
+    assert plan(16384, 3072, 3968)[2] == 0                  # 31 K-steps
+    assert plan(16384, 3072, 4096)[2] == 76 + 8             # 32 K-steps
+
+
+def test_workspace_decides(plan):
+    assert plan(16384, 3072, 12288, ws=-1)[2] == 0                            # none given
+    assert plan(16384, 3072, 12288, ws=COUNTERS + 2 * 76 * SLOT - 1)[2] == 0  # one byte short
+    assert plan(16384, 3072, 12288, ws=COUNTERS + 2 * 76 * SLOT)[2] == 84     # enough for 76 pairs
+
+
+def test_pairs_never_exceed_tiles_or_residency(plan):
+    assert plan(256, 256, 8192)[:3] == (1, 1, 0)
+    assert plan(300, 512, 8192)[:3] == (4, 4, 0)            # ragged M: 2 row tiles x 2
+    assert plan(20480, 3072, 12288, clusters=10)[:2] == (960, 10)
+    # leftover 0 (tiles a multiple of the pairs): nothing to split
+    assert plan(256 * 76, 256, 8192)[:3] == (76, 76, 0)
+    assert plan(256 * 152, 256, 8192)[:3] == (152, 76, 0)
+    # leftover 1 of 76: split the first 77 tiles
+    assert plan(256 * 153, 256, 8192)[:3] == (153, 76, 77)
+
+
+def test_workspace_bytes_query(plan):
+    assert plan(16384, 3072, 3072)[3] == 0                  # K < 4096
+    assert plan(256, 256, 8192)[3] == 0                     # one tile
+    assert plan(512, 256, 8192)[3] == COUNTERS + 2 * 1 * SLOT
+    assert plan(20480, 3072, 12288)[3] == COUNTERS + 2 * 80 * SLOT
