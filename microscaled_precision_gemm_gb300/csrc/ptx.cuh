@@ -1,4 +1,4 @@
-// Inline-PTX wrappers for sm_103a: mbarriers, TMA tensor loads, tcgen05 (tensor
+// Inline-PTX wrappers for sm_103a: mbarriers, TMA tensor loads and stores, tcgen05 (tensor
 // memory, block-scaled pair MMA, scale-factor copies), clusters, programmatic
 // dependent launch, conversions and packed fp32 pairs. Every instruction here is
 // documented in the public PTX ISA (tcgen05, cp.async.bulk.tensor, mbarrier,
