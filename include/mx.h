@@ -288,9 +288,13 @@ mx_status mx_dit_mlp_block(const void* x, int64_t M, int64_t d, int64_t ff, cons
  *   The call allocates nothing. Sizes whose MXFP6 x and h exceed that capacity
  *   return MX_ERR_WORKSPACE_TOO_SMALL before anything is launched (for d = 3072,
  *   ff = 12288 that is M > 5590 tokens).
+ *   Argument checks run in mx_mlp's order (shape rules first, then M == 0 is a
+ *   no-op, then the capacity, then null pointers), all before any launch.
  *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   (cudaGetSymbolAddress) with that device current, and so does the first call
+ *   in a new context of the device (cudaDeviceReset recreates the context, and
+ *   the array may then sit elsewhere); make such a first call before any stream
+ *   capture.
  *   Every call on a device shares the one array, and the kernels write all of it
  *   that they read before reading it (the first kernel zeroes the split-tail
  *   counters), so nothing needs clearing between calls; but calls whose

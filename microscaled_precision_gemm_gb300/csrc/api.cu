@@ -1,10 +1,12 @@
 // C ABI (include/mx.h): argument validation, device checks and the three-launch
 // MLP orchestration. Everything here is host code; the arithmetic lives in the
 // kernels (quantize.cu, gemm.cu).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "mx.h"
@@ -152,11 +154,9 @@ mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_c
 mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, const void* w_up_codes,
                    const void* w_up_scales, const void* b_up, const void* w2_codes, const void* w2_scales,
                    const void* b2, void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (M < 0 || d < 0 || ff < 0) return MX_ERR_INVALID_ARG;
+  mx_status st = mxk::mlp_check_shape(M, d, ff, up_epi == MX_EPI_BIAS_SWIGLU_MXFP6);
+  if (st != MX_OK) return st;
   const int64_t n_up = up_epi == MX_EPI_BIAS_SWIGLU_MXFP6 ? 2 * ff : ff;
-  if (d == 0 || ff == 0 || d % 256 != 0 || ff % 128 != 0 || n_up % 256 != 0 || M > kMaxDim || d > kMaxDim ||
-      n_up > kMaxDim)
-    return MX_ERR_UNSUPPORTED_SHAPE;
   if (M == 0) return MX_OK;
   if (x == nullptr || w_up_codes == nullptr || w_up_scales == nullptr || w2_codes == nullptr ||
       w2_scales == nullptr || y == nullptr || workspace == nullptr)
@@ -174,7 +174,7 @@ mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, 
   const size_t sbytes = sw != nullptr ? workspace_bytes - l.split : 0;
   unsigned* zero = static_cast<unsigned*>(sw);
   const int nzero = static_cast<int>(mxk::kArrivalsBytes / sizeof(unsigned));
-  mx_status st = check_quantize(x, M, d, d, xq, xs);
+  st = check_quantize(x, M, d, d, xq, xs);
   if (st != MX_OK) return st;
   st = check_gemm(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr);
   if (st != MX_OK) return st;
@@ -201,9 +201,8 @@ mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const 
   if (activation != MX_ACT_GELU_TANH && activation != MX_ACT_SWIGLU) return MX_ERR_INVALID_ARG;
   const int up_epi = activation == MX_ACT_SWIGLU ? MX_EPI_BIAS_SWIGLU_MXFP6 : MX_EPI_BIAS_GELU_MXFP6;
   const int64_t n_up = activation == MX_ACT_SWIGLU ? 2 * ff : ff;
-  if (d == 0 || ff == 0 || d % 256 != 0 || ff % 128 != 0 || n_up % 256 != 0 || M > kMaxDim || d > kMaxDim ||
-      n_up > kMaxDim)
-    return MX_ERR_UNSUPPORTED_SHAPE;
+  mx_status st = mxk::mlp_check_shape(M, d, ff, activation == MX_ACT_SWIGLU);
+  if (st != MX_OK) return st;
   if (M == 0) return MX_OK;
   if (x == nullptr || w_up_codes == nullptr || w_up_scales == nullptr || w2_codes == nullptr ||
       w2_scales == nullptr || y == nullptr || workspace == nullptr)
@@ -220,7 +219,7 @@ mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const 
   const size_t sbytes = sw != nullptr ? workspace_bytes - l.split : 0;
   unsigned* zero = static_cast<unsigned*>(sw);
   const int nzero = static_cast<int>(mxk::kArrivalsBytes / sizeof(unsigned));
-  mx_status st = check_norm_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr);
+  st = check_norm_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr);
   if (st != MX_OK) return st;
   st = check_gemm(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr);
   if (st != MX_OK) return st;
@@ -245,9 +244,42 @@ mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const 
 }  // namespace
 
 namespace mxk {
+mx_status mlp_check_shape(int64_t M, int64_t d, int64_t ff, bool swiglu) {
+  if (M < 0 || d < 0 || ff < 0) return MX_ERR_INVALID_ARG;
+  const int64_t n_up = swiglu ? 2 * ff : ff;
+  if (d == 0 || ff == 0 || d % 256 != 0 || ff % 128 != 0 || n_up % 256 != 0 || M > kMaxDim || d > kMaxDim ||
+      n_up > kMaxDim)
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  return MX_OK;
+}
+
 size_t mlp_min_workspace_bytes(int64_t M, int64_t d, int64_t ff) {
   if (M < 0 || d < 0 || ff < 0) return 0;
   return mlp_layout(M, d, ff).base;
+}
+
+bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+  typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    void* q = nullptr;
+    cudaDriverEntryPointQueryResult r1, r2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r1) == cudaSuccess &&
+        r1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) == cudaSuccess &&
+        r2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+      get_id = reinterpret_cast<CtxGetIdFn>(q);
+    }
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
 }
 }  // namespace mxk
 

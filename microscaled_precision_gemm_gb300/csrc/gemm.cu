@@ -962,18 +962,21 @@ static bool make_codes_out_map(CUtensorMap* map, void* codes, int64_t m, int64_t
 }
 
 // Per-device caches of the kernel attribute and of the co-resident cluster count,
-// filled on a device's first call (any thread may fill them).
+// filled on a device's first call (any thread may fill them). The attribute belongs
+// to the context, so it is set again when the device's context has changed (a new
+// primary context after cudaDeviceReset).
 template <int EPI, bool DBG, bool SPLIT>
 static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) {
   auto kern = mx_gemm_kernel<EPI, DBG, SPLIT>;
-  static std::atomic<bool> configured[64];
+  static std::atomic<unsigned long long> configured[64];   // context ID + 1 the attribute was set in; 0: none
   static std::atomic<int> cached[64];
   const bool cacheable = dev >= 0 && dev < 64;
-  if (!cacheable || !configured[dev].load(std::memory_order_acquire)) {
+  unsigned long long ctx = 0;
+  if (!cacheable || !current_context_id(&ctx) || configured[dev].load(std::memory_order_acquire) != ctx + 1) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    if (cacheable) configured[dev].store(true, std::memory_order_release);
+    if (cacheable && current_context_id(&ctx)) configured[dev].store(ctx + 1, std::memory_order_release);
   }
   int n = cacheable ? cached[dev].load(std::memory_order_relaxed) : 0;
   if (n == 0) {

@@ -123,9 +123,22 @@ struct GemmArgs {
 // tensor-map encoder rejected the operands.
 cudaError_t launch_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream, bool* encode_failed);
 
+// Shape rules shared by mx_mlp, mx_gated_mlp, mx_dit_mlp_block and mx_mlp_noalloc:
+// MX_ERR_INVALID_ARG for a negative size, MX_ERR_UNSUPPORTED_SHAPE for d or ff of 0,
+// d % 256, ff % 128, an up-projection width (ff, or 2 ff for the stacked SwiGLU
+// weight) % 256, or a size of 2^31 or more; MX_OK otherwise (M == 0 included).
+mx_status mlp_check_shape(int64_t M, int64_t d, int64_t ff, bool swiglu);
+
 // Smallest workspace mx_mlp / mx_gated_mlp / mx_dit_mlp_block run with: the MXFP6
 // activations and intermediate, without the split-tail region.
 size_t mlp_min_workspace_bytes(int64_t M, int64_t d, int64_t ff);
+
+// Unique ID of the calling thread's current CUDA context (cuCtxGetId); false when
+// no context is current or the driver cannot say. A device's primary context gets
+// a new ID when cudaDeviceReset destroys and recreates it, so caches of
+// context-bound state (a device symbol's address, a kernel's shared-memory
+// attribute) are kept per context ID rather than per device.
+bool current_context_id(unsigned long long* id);
 
 // Co-resident CTA pairs of the GEMM kernel on the current device (cached per device).
 cudaError_t gemm_max_clusters(int* clusters);

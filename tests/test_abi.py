@@ -279,3 +279,28 @@ def test_gemm_workspace_bytes(lib):
     assert lib.mx_gemm_workspace_bytes(256, 256, 8192) == 0       # one tile
     assert lib.mx_gemm_workspace_bytes(256, 384, 8192) == 0       # unsupported N
     assert lib.mx_gemm_workspace_bytes(0, 256, 8192) == 0
+
+
+def test_noalloc_checks_shape_then_capacity_on_the_host(lib):
+    """mx_mlp_noalloc answers in mx_mlp's order, all before any device call: a bad
+    shape as mx_mlp does (also with M = 0), then the capacity of its 64 MiB static
+    scratch, then null pointers. At d = 3072, ff = 12288 the MXFP6 x and h of 5590
+    tokens fit (the call gets as far as the null-pointer check) and of 5591 do not."""
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    fn = ctypes.CFUNCTYPE(ctypes.c_int, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp)(
+        ("mx_mlp_noalloc", lib))
+
+    def call(M, d=3072, ff=12288, x=None):
+        return fn(x, M, d, ff, None, None, None, None, None, None, None, None)
+
+    cap = 64 << 20
+    assert _mlp_base(lib, 5590, 3072, 12288) <= cap < _mlp_base(lib, 5591, 3072, 12288)
+    assert call(5590) == INVALID
+    assert call(5591) == WS_SMALL
+    assert call(-1) == INVALID
+    assert call(0, d=100) == SHAPE                 # mx_mlp's answer for d % 256, even with M = 0
+    assert call(1 << 20, d=100) == SHAPE           # a bad shape is not reported as a capacity problem
+    assert call(8, ff=640) == SHAPE                # GELU up-projection width % 256
+    assert call(1 << 31) == SHAPE
+    assert call(0) == OK
+    assert lib.mx_mlp(None, 0, 100, 12288, None, None, None, None, None, None, None, None, 0, None) == SHAPE
