@@ -105,6 +105,14 @@ NCU_TRAFFIC_BYTES: dict = {
 }
 
 
+# sm__pipe_tensor_cycles_active as a fraction of elapsed cycles, from one ncu capture
+# of the current kernel (profiles/); None where no capture of the current kernel exists.
+NCU_TENSOR_PIPE_ACTIVE: dict = {
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 0.813,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 0.853,
+}
+
+
 def load_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -160,6 +168,7 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.proc = None
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "25"]
+        self.rows = []
         bus = _pci_bus_id(device_index)
         if bus:
             cmd += ["-i", bus]
@@ -168,39 +177,60 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
     def stop(self, window: tuple[float, float] | None = None) -> dict:
-        """Summary of the samples taken inside `window` (wall-clock seconds, the timed
-        region), or of all samples when none fell inside it."""
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        rows = []
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
+        """Ends the sampling; returns the summary of `window` (see summary())."""
+        self.rows = []
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                vals = (float(parts[1]), float(parts[2]), float(parts[3]))
-            except ValueError:
-                continue
-            active = {name for name, val in zip(names, parts[4:8]) if val.lower().startswith("active")}
-            rows.append((t, vals, active))
-        inside = [r for r in rows if window is not None and window[0] <= r[0] <= window[1]]
-        use = inside or rows
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            for line in out.strip().splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    vals = (float(parts[1]), float(parts[2]), float(parts[3]))
+                except ValueError:
+                    continue
+                active = {name for name, val in zip(self.NAMES, parts[4:8]) if val.lower().startswith("active")}
+                self.rows.append((t, vals, active))
+        return self.summary(window)
+
+    def summary(self, window: tuple[float, float] | None, min_samples: int = 3, max_pad_s: float = 0.1) -> dict:
+        """Median SM clock, maximum clock and power, and throttle reasons of the samples
+        taken inside `window` (wall-clock seconds). A window shorter than the sampling
+        interval may hold fewer than `min_samples`: it is then widened on both sides in
+        25 ms steps, up to `max_pad_s`, and the record says by how much. Without any
+        sample near the window, all samples are summarised ("whole sampling run")."""
+        rows = getattr(self, "rows", [])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "no samples"}
+        use, label = [], "whole sampling run"
+        if window is not None:
+            pad = 0.0
+            while True:
+                use = [r for r in rows if window[0] - pad <= r[0] <= window[1] + pad]
+                if len(use) >= min_samples or pad >= max_pad_s - 1e-9:
+                    break
+                pad += 0.025
+            if use:
+                label = "timed region" if pad == 0.0 else (
+                    f"timed region widened by +-{pad * 1e3:.0f} ms (the region is shorter than the sampling "
+                    f"interval; the neighbouring samples are of the same back-to-back steps)")
+        if not use:
+            use, label = rows, "whole sampling run"
         sm = [r[1][0] for r in use]
         smax = [r[1][1] for r in use]
         power = [r[1][2] for r in use]
-        reasons = set().union(*(r[2] for r in use)) if use else set()
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None,
-                "window": "timed region" if inside else "whole sampling run"}
+        reasons = set().union(*(r[2] for r in use))
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power), "window": label}
 
 
 def _pci_bus_id(device_index: int) -> str | None:
@@ -490,8 +520,29 @@ def run_gpu(args) -> dict | None:
     torch.cuda.synchronize()
     t_region1 = time.time()
     barrier(world)
-    clk = clocks.stop(window=(t_region0, t_region1))
     total_ms = max_over_ranks(start.elapsed_time(stop), world)
+
+    # sustained leg: the same rotation of steps, back to back for a few seconds right
+    # after the timed region, so the power cap has settled and the clock sampler
+    # (every 25 ms) has many samples inside its window
+    sustained = None
+    if args.sustain_s > 0:
+        n_sus = max(1, int(args.sustain_s / max(total_ms / args.steps * 1e-3, 1e-6)))
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        t_sus0 = time.time()
+        s0.record(stream)
+        for i in range(n_sus):
+            for _, fn in launches[i % len(launches)]:
+                fn()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        t_sus1 = time.time()
+        barrier(world)
+        sustained = {"steps": n_sus, "ms_per_step": max_over_ranks(s0.elapsed_time(s1), world) / n_sus,
+                     "seconds": t_sus1 - t_sus0, "window": (t_sus0, t_sus1)}
+    clk = clocks.stop(window=(t_region0, t_region1))
     per_stage = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in probe) / len(probe) for j in range(n_st)]
     if mx.mx_device_error() != 0:
         raise RuntimeError("a kernel reported a device-side wait timeout in the timed region")
@@ -526,7 +577,9 @@ def run_gpu(args) -> dict | None:
                 "unit": "TFLOP/s", "frac": stage_report[dom]["tflops"] / fp6_peak,
                 "peak_basis": f"2 x {peaks['source']} {basis_name} bf16 cuBLAS ({bf16_basis} TFLOP/s): "
                               f"dense FP6/FP8 rate = 2 x BF16 (of {peaks['source']})",
-                "traffic": NCU_TRAFFIC_BYTES.get((args.config, dom))}
+                "traffic": NCU_TRAFFIC_BYTES.get((args.config, dom)),
+                "frac_spec_5pf": stage_report[dom]["tflops"] / FP6_SPEC_PEAK_TFLOPS,
+                "tensor_pipe_active_ncu": NCU_TENSOR_PIPE_ACTIVE.get((args.config, dom))}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": stage_report[dom]["gbs"], "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": stage_report[dom]["gbs"] / peaks["hbm_gbs"],
@@ -605,6 +658,21 @@ def run_gpu(args) -> dict | None:
             line["quantize_isolated"] = k1_isolated
     if bf16_ctx is not None:
         line["bf16_context"] = bf16_ctx
+    if sustained is not None:
+        sclk = clocks.summary(sustained.pop("window"))
+        sms = sustained["ms_per_step"]
+        sustained.update({
+            "value": step_flops / (sms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "pct_fp6_peak_spec_5pf": step_flops / (sms * 1e-3) / 1e12 / FP6_SPEC_PEAK_TFLOPS,
+            "clocks": sclk,
+            # time x clock: comparable between runs at different SM clocks (us * MHz)
+            "time_x_mhz": sms * 1e3 * sclk["sm_mhz"] if sclk.get("sm_mhz") else None,
+            "note": "the timed region's rotation of steps, back to back right after it, with no events "
+                    "between kernels; clocks from the samples inside this leg's own window"})
+        line["sustained"] = sustained
+    if clk.get("sm_mhz"):
+        line["time_x_mhz"] = ms_step * 1e3 * clk["sm_mhz"]
+        roof["kernel_time_x_mhz"] = stage_report[dom]["ms"] * 1e3 * clk["sm_mhz"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=args.cpu_budget)
     return line
@@ -833,16 +901,34 @@ def _grow_sample(ow, rng, M: int, target_s: float):
 
 
 def cpu_baseline(cfg: dict, budget_s: float) -> dict:
-    """The oracle, as it stands, on a bounded row sample of the same workload."""
+    """The oracle, as it stands. The single-GEMM workload and the M = 4096
+    up-projection are timed whole; the larger workloads on a bounded row sample,
+    whose time is extrapolated linearly in M to the whole workload (the oracle's
+    cost per token row is constant once its weights are quantized) and labelled so."""
     ow = OracleWorkload(cfg, sample_rows=64)
     rng = np.random.default_rng(0)
     M = cfg["M"]
     ow.step(rng.integers(0, M, 8))   # warm the thread pools
-    rows, dt, flops = _grow_sample(ow, rng, M, budget_s)
+    whole = cfg["kind"] in ("gemm", "up")
+    if whole:
+        rows = np.arange(M)
+        t0 = time.perf_counter()
+        flops = ow.step(rows)
+        dt = time.perf_counter() - t0
+    else:
+        rows, dt, flops = _grow_sample(ow, rng, M, budget_s)
     n = len(rows)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "cpu_model": _cpu_model(),
-            "kind": "oracle", "seconds": dt, "sample": f"{n} of {M} token rows of the same workload (weights quantized by the "
-                                     f"oracle beforehand, untimed); fp64 numpy + brute-force E2M3 search"}
+    out = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "cpu_model": _cpu_model(),
+           "kind": "oracle", "seconds": dt,
+           "sample": (f"all {M} token rows of the workload" if whole else f"{n} of {M} token rows of the same "
+                      f"workload") + " (weights quantized by the oracle beforehand, untimed); fp64 numpy + "
+                                     "brute-force E2M3 search",
+           "extrapolated": not whole,
+           "full_workload_s": dt * M / n}
+    if not whole:
+        out["rule"] = (f"full_workload_s = seconds x {M} / {n}: linear in the token count M; value is the "
+                       f"sample's own rate")
+    return out
 
 
 def run_reference(args) -> dict | None:
@@ -898,6 +984,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-split", action="store_true",
                     help="run the GEMMs without the split tail (the same work, tiles whole; for comparison)")
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps after the timed region (the sustained leg; 0: none)")
     ap.add_argument("--copies", type=int, default=2,
                     help="independent input copies rotated between steps (2 keeps L2 cold; 1 for profiling)")
     args = ap.parse_args(argv)

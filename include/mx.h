@@ -96,6 +96,34 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, void
                       cudaStream_t stream);
 
 /*
+ * mx_quantize_stacked -- K1 over several BF16 matrices with the same K into one
+ * stacked MXFP6 tensor of R = sum(part_rows) rows: the weights that one GEMM reads
+ * as a single B operand ("Optimizing Krea 3 on AMD Instinct MI355X", section
+ * "Fusion cut intermediate memory traffic": the stacked projections are quantized
+ * and read once) -- [W_g; W_u] for MX_EPI_BIAS_SWIGLU_MXFP6 / mx_gated_mlp, or the
+ * query/key/value/gate weights of one projection. Rows are quantized independently,
+ * so the result equals mx_quantize of the concatenated matrix.
+ * Scale-atom offset rule: part i starts at stacked row R_i = part_rows[0] + ... +
+ * part_rows[i-1]; its codes at byte mx_codes_bytes(R_i, K) of `codes` and its
+ * scales at byte mx_scales_bytes(R_i, K) of `scales`. That is where its own
+ * mx_quantize output would go, because every part but the last has a multiple of
+ * 128 rows, so each part's tiled scales begin on a 512-byte atom.
+ *   x_parts   : host array of n_parts device pointers; part i is BF16
+ *               [part_rows[i]][K] with row stride ld_x[i], 16-byte aligned
+ *   part_rows : host array of n_parts row counts >= 0; all but the last % 128 == 0
+ *   ld_x      : host array of n_parts row strides (>= K, % 8 == 0), or NULL for K
+ *   n_parts   : >= 1
+ *   K         : as mx_quantize
+ *   codes, scales : the stacked tensor, mx_codes_bytes(R, K) and mx_scales_bytes(R, K)
+ *               bytes (32- and 16-byte aligned), written
+ * Every part is checked on the host before the first launch (one launch per part,
+ * in order, on `stream`); a bad part returns its mx_quantize status and nothing is
+ * written. R < 2^31.
+ */
+mx_status mx_quantize_stacked(const void* const* x_parts, const int64_t* part_rows, const int64_t* ld_x, int n_parts,
+                              int64_t K, void* codes, void* scales, cudaStream_t stream);
+
+/*
  * mx_quantize_rmsnorm_modulate -- K1 with the step before it fused in: row-wise
  * RMS normalisation, modulation, then MXFP6 quantization of the result
  * ("Optimizing Krea 3 on AMD Instinct MI355X", section "Fusion cut intermediate

@@ -88,6 +88,7 @@ EXPORTED_SYMBOLS = (
     "mx_dit_mlp_block",
     "mx_gemm_workspace_bytes",
     "mx_gemm_launch_plan",
+    "mx_quantize_stacked",
 )
 
 _lib = None
@@ -125,6 +126,8 @@ def load():
             "mx_codes_bytes": (sz, [i64, i64]),
             "mx_scales_bytes": (sz, [i64, i64]),
             "mx_quantize": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp]),
+            "mx_quantize_stacked": (ctypes.c_int, [ctypes.POINTER(vp), ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                                   ctypes.c_int, i64, vp, vp, vp]),
             "mx_gemm": (ctypes.c_int, [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, sz, vp]),
             "mx_gemm_workspace_bytes": (sz, [i64, i64, i64]),
             "mx_gemm_launch_plan": (ctypes.c_int, [i64, i64, i64, sz, ctypes.POINTER(ctypes.c_int),
@@ -342,27 +345,34 @@ def mx_quantize_rmsnorm_modulate(x, shift=None, scale=None, eps: float = 1e-6, o
 
 
 def mx_quantize_stacked(parts, stream=None) -> MxTensor:
-    """Quantize BF16 matrices [R_i][K] into one stacked MXFP6 tensor [sum R_i][K].
+    """Quantize BF16 matrices [R_i][K] into one stacked MXFP6 tensor [sum R_i][K]
+    (the C entry point mx_quantize_stacked).
 
     Rows are quantized independently, so the result is the concatenation of the
     parts' MXFP6 forms; every part but the last needs R_i % 128 == 0 (its tiled
     scales then end on an atom boundary). Builds the [W_g; W_u] weight of
     mx_gated_mlp and the stacked query/key/value/gate weight of one projection.
     """
+    torch = _torch()
     lib = load()
+    if not parts:
+        raise ValueError("mx_quantize_stacked needs at least one part")
+    dev = parts[0].device
+    for i, p in enumerate(parts):
+        if p.dtype != torch.bfloat16 or p.dim() != 2 or not p.is_cuda or p.stride(1) != 1 or p.device != dev:
+            raise ValueError(f"part {i} must be a CUDA bfloat16 [rows][K] tensor with unit column stride on {dev}")
     k = parts[0].shape[1]
     rows = sum(int(p.shape[0]) for p in parts)
-    if any(p.shape[1] != k for p in parts) or any(p.shape[0] % 128 for p in parts[:-1]):
-        raise ValueError("parts need equal K and all but the last a multiple of 128 rows")
-    dev = parts[0].device
+    if any(p.shape[1] != k for p in parts):
+        raise ValueError("parts need equal K")
     codes = _empty_u8(lib.mx_codes_bytes(rows, k), dev).view(rows, -1)
     scales = _empty_u8(lib.mx_scales_bytes(rows, k), dev)
-    r0 = 0
-    for p in parts:
-        r = int(p.shape[0])
-        s0 = lib.mx_scales_bytes(r0, k)
-        mx_quantize(p, MxTensor(codes[r0:r0 + r], scales[s0:s0 + lib.mx_scales_bytes(r, k)], r, k), stream)
-        r0 += r
+    n = len(parts)
+    ptrs = (ctypes.c_void_p * n)(*[_ptr(p) for p in parts])
+    prow = (ctypes.c_int64 * n)(*[int(p.shape[0]) for p in parts])
+    lds = (ctypes.c_int64 * n)(*[int(p.stride(0)) for p in parts])
+    st = lib.mx_quantize_stacked(ptrs, prow, lds, n, k, _ptr(codes), _ptr(scales), _stream_handle(stream))
+    _check(st, "mx_quantize_stacked")
     return MxTensor(codes, scales, rows, k)
 
 

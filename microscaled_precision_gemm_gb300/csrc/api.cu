@@ -305,6 +305,40 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, void
                                                                                                 : MX_ERR_CUDA;
 }
 
+mx_status mx_quantize_stacked(const void* const* x_parts, const int64_t* part_rows, const int64_t* ld_x, int n_parts,
+                              int64_t K, void* codes, void* scales, cudaStream_t stream) {
+  if (x_parts == nullptr || part_rows == nullptr || n_parts < 1) return MX_ERR_INVALID_ARG;
+  // every part is checked before anything is launched
+  int64_t total = 0;
+  for (int i = 0; i < n_parts; ++i) {
+    const int64_t r = part_rows[i];
+    const int64_t ld = ld_x != nullptr ? ld_x[i] : K;
+    if (r < 0) return MX_ERR_INVALID_ARG;
+    if (i + 1 < n_parts && r % 128 != 0) return MX_ERR_UNSUPPORTED_SHAPE;   // parts start on a scale atom
+    if (total > kMaxDim - r) return MX_ERR_UNSUPPORTED_SHAPE;
+    // the part's own checks, at its place in the stacked buffers (32-byte aligned
+    // codes: a row offset that is a multiple of 128 keeps the stacked base's alignment)
+    const mx_status st = check_quantize(x_parts[i], r, K, ld, codes, scales);
+    if (st != MX_OK) return st;
+    total += r;
+  }
+  mx_status st = check_quantize(x_parts[0], total, K, K, codes, scales);
+  if (st != MX_OK || total == 0) return st;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  int64_t r0 = 0;
+  for (int i = 0; i < n_parts; ++i) {
+    const int64_t r = part_rows[i];
+    const int64_t ld = ld_x != nullptr ? ld_x[i] : K;
+    if (r > 0 && mxk::launch_quantize_bf16(x_parts[i], r, K, ld, static_cast<uint8_t*>(codes) + mxk::codes_bytes(r0, K),
+                                           static_cast<uint8_t*>(scales) + mxk::scales_bytes(r0, K), sms,
+                                           stream) != cudaSuccess)
+      return MX_ERR_CUDA;
+    r0 += r;
+  }
+  return MX_OK;
+}
+
 mx_status mx_quantize_rmsnorm_modulate(const void* x, int64_t rows, int64_t K, int64_t ld_x, const void* shift,
                                        const void* scale, float eps, void* codes, void* scales, float* debug_y,
                                        cudaStream_t stream) {

@@ -304,3 +304,26 @@ def test_noalloc_checks_shape_then_capacity_on_the_host(lib):
     assert call(1 << 31) == SHAPE
     assert call(0) == OK
     assert lib.mx_mlp(None, 0, 100, 12288, None, None, None, None, None, None, None, None, 0, None) == SHAPE
+
+
+def test_quantize_stacked_rejects_bad_arguments(lib):
+    """Every part is checked on the host before the first launch."""
+    def call(rows, k=256, lds=None, ptrs=None, codes=A32b, scales=A32c, n=None):
+        n = len(rows) if n is None else n
+        p = (ctypes.c_void_p * max(1, len(rows)))(*(ptrs or [A32 + 0x100000 * i for i in range(len(rows))]))
+        r = (ctypes.c_int64 * max(1, len(rows)))(*rows)
+        ld = None if lds is None else (ctypes.c_int64 * len(lds))(*lds)
+        return lib.mx_quantize_stacked(p, r, ld, n, k, codes, scales, None)
+
+    assert call([128, 64], n=0) == INVALID
+    assert lib.mx_quantize_stacked(None, None, None, 1, 256, A32b, A32c, None) == INVALID
+    assert call([100, 64]) == SHAPE                    # a part before the last not a multiple of 128 rows
+    assert call([128, -1]) == INVALID
+    assert call([128, 64], k=100) == SHAPE
+    assert call([128, 64], lds=[256, 128]) == INVALID  # ld_x < K
+    assert call([128, 64], lds=[256, 260]) == MISALIGNED
+    assert call([128, 64], ptrs=[A32, A32 + 8]) == MISALIGNED
+    assert call([128, 64], ptrs=[A32, 0]) == INVALID
+    assert call([128, 64], codes=A32b + 16) == MISALIGNED
+    assert call([128, 1 << 31]) == SHAPE
+    assert call([0, 0], ptrs=[0, 0], codes=0, scales=0) == OK   # nothing to quantize
