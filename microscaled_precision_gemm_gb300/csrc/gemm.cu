@@ -610,9 +610,10 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
       if constexpr (EPI == kEpiGateRes) {
         uint4 res[4] = {};
         if (live) {
+          // coherent loads: the output may be this very residual (in-place update)
           const uint4* src = reinterpret_cast<const uint4*>(residual + row * n_total + n);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) res[j] = __ldg(src + j);
+          for (int j = 0; j < 4; ++j) res[j] = ld_global_na_v4(src + j);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -109,14 +109,22 @@ def assert_codes_equal(gpu_codes, ref_codes, gpu_scales, ref_scales, what=""):
                              f"oracle {[hex(v) for v in rc[tuple(idx.T)].tolist()]}")
 
 
-def assert_swiglu_close(h_gpu, c_ref, what):
-    """h_gpu [M][F] against the oracle's stacked accumulators c_ref [M][2F] (bias included)."""
+def swiglu_bound(c_ref):
+    """The bound on |h_gpu - silu(g) u| that follows from the GEMM tolerance on the
+    stacked accumulators c_ref = [g | u] [M][2F] (bias included)."""
     f = c_ref.shape[1] // 2
     g, u = c_ref[:, :f], c_ref[:, f:]
     tg = REL_TOL * np.abs(g) + RMS_TOL * np.sqrt(np.mean(g * g))
     tu = REL_TOL * np.abs(u) + RMS_TOL * np.sqrt(np.mean(u * u))
     ref = O.silu(g) * u
-    bound = SILU_LIP * tg * (np.abs(u) + tu) + np.abs(O.silu(g)) * tu + 1e-6 * np.abs(ref) + 1e-30
+    return SILU_LIP * tg * (np.abs(u) + tu) + np.abs(O.silu(g)) * tu + 1e-6 * np.abs(ref) + 1e-30
+
+
+def assert_swiglu_close(h_gpu, c_ref, what):
+    """h_gpu [M][F] against the oracle's stacked accumulators c_ref [M][2F] (bias included)."""
+    f = c_ref.shape[1] // 2
+    ref = O.silu(c_ref[:, :f]) * c_ref[:, f:]
+    bound = swiglu_bound(c_ref)
     err = np.abs(np.asarray(h_gpu, np.float64) - ref)
     bad = np.argwhere(err > bound)
     assert bad.size == 0, (f"{what}: {len(bad)} of {err.size} outside, first {bad[:4].tolist()}, "
@@ -155,3 +163,53 @@ def graph_replays_match(lib, fn_into, make_input, x_buf, y_buf, n=3):
         torch.cuda.synchronize()
         assert torch.equal(y_buf, y_eager), f"replay {i} differs from the eager call"
     assert lib.mx_device_error() == 0
+
+
+def near_rounding_boundary(v, tol) -> np.ndarray:
+    """Per element of v (fp32 values about to be MXFP6-encoded, [rows][K]): True where
+    some value within `tol` (same shape, >= 0) of v could encode differently -- a
+    rounding boundary between two E2M3 codes (the midpoint of adjacent magnitudes at
+    the block's scale, or zero, where the sign bit changes) lies within tol, or the
+    block's amax could fall on the other side of a power of two (the shared exponent
+    could change, moving every code of the block). Two encoders whose inputs differ
+    by at most tol can only disagree on such elements, which bounds the number of
+    legitimate code differences."""
+    v = np.asarray(v, dtype=np.float64)
+    tol = np.broadcast_to(np.asarray(tol, dtype=np.float64), v.shape)
+    rows, k = v.shape
+    vb = np.abs(v).reshape(rows, k // O.BLOCK, O.BLOCK)
+    tb = tol.reshape(rows, k // O.BLOCK, O.BLOCK)
+    amax = vb.max(axis=-1)
+    # the other encoder's amax lies in [max(|v| - t), max(|v| + t)]
+    lo = np.maximum((vb - tb).max(axis=-1), np.finfo(np.float64).tiny)
+    hi = (vb + tb).max(axis=-1)
+    near_scale = np.floor(np.log2(lo)) != np.floor(np.log2(hi))
+    s = O.shared_exponent(amax).astype(np.float64)
+    t = vb * np.exp2(-s)[..., None]
+    tt = tb * np.exp2(-s)[..., None]
+    mags = np.unique(np.abs(np.asarray(O.E2M3_TABLE, dtype=np.float64)))
+    mids = (mags[:-1] + mags[1:]) / 2.0
+    j = np.clip(np.searchsorted(mids, t), 1, len(mids) - 1)
+    dist = np.minimum(np.minimum(np.abs(t - mids[j - 1]), np.abs(t - mids[j])), t)
+    near = (dist <= tt) | near_scale[..., None]
+    return near.reshape(rows, k)
+
+
+def requant_flip_report(gpu_codes, gpu_scales, ref_codes, ref_scales, ref_values, tol) -> dict:
+    """Differences between the GPU's MXFP6 encoding and an independent oracle's of
+    the same rows: differing codes (elements of blocks whose scales differ count as
+    differing), rows touched, and the derived bound -- the number of elements near a
+    rounding boundary of the oracle's values within the tolerance that the two
+    pre-quantization values were held to. Asserts the differences stay within it."""
+    gc, rc = np.asarray(gpu_codes), np.asarray(ref_codes)
+    gs, rs = np.asarray(gpu_scales), np.asarray(ref_scales)
+    scale_diff = np.repeat(gs != rs, O.BLOCK, axis=1)
+    differ = (gc != rc) | scale_diff
+    # the oracle encodes its fp64 values rounded to fp32: half an fp32 ulp more
+    ref = np.asarray(ref_values, dtype=np.float64)
+    near = near_rounding_boundary(ref, np.asarray(tol, dtype=np.float64) + 2.0 ** -24 * np.abs(ref))
+    rep = {"elements": int(differ.size), "differing": int(differ.sum()), "near_boundary": int(near.sum()),
+           "differing_not_near": int((differ & ~near).sum()), "rows_touched": int(differ.any(axis=1).sum()),
+           "rows": int(differ.shape[0])}
+    assert rep["differing_not_near"] == 0, f"codes differ away from any rounding boundary: {rep}"
+    return rep, differ

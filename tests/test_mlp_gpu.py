@@ -6,7 +6,9 @@ the GEMM tolerance; requantized intermediate bit-exact given the kernel's fp32
 GELU values; down-projection within the tolerance given the GPU's intermediate.
 End to end, against a fully independent oracle run, requantization may flip a
 code where the GPU's fp32 value and the oracle's fp64 value sit on two sides of
-a rounding boundary, so that comparison asserts a 99.9% element pass rate.
+a rounding boundary; every differing code must be within the stage-2 tolerance of
+such a boundary, and the output must stay within the GEMM tolerance plus the
+exact contribution of the differing codes.
 """
 
 import numpy as np
@@ -14,8 +16,8 @@ import pytest
 
 import oracle as O
 import synth
-from mxutil import (assert_codes_equal, assert_gemm_close, bf16_from_device, bf16_to_device, f32_from_bf16_bits,
-                    gemm_tolerance_report, mx_rows_to_host, sample_rows)
+from mxutil import (REL_TOL, RMS_TOL, assert_codes_equal, assert_gemm_close, bf16_from_device, bf16_to_device,
+                    f32_from_bf16_bits, gemm_tolerance_report, mx_rows_to_host, requant_flip_report, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,11 +58,28 @@ def _run(lib, w, rows):
     # stage 4: down-projection given the GPU's verified intermediate
     got = f32_from_bf16_bits(bf16_from_device(y[idx])).astype(np.float64)
     assert_gemm_close(got, O.down_projection(ghq, ghs, r_w2q, r_w2s, w["b2"]), "y")
-    # end to end against the independent oracle
-    y_ref, _ = O.mlp(w["x"][rows], r_w1q, r_w1s, w["b1"], r_w2q, r_w2s, w["b2"])
+    # End to end against the independent oracle, which encodes its own fp64 GELU
+    # values (rounded to fp32) where the GPU encodes its fp32 ones. Two encodings of
+    # values held to the stage-2 tolerance can differ only at elements within that
+    # tolerance of a rounding boundary: requant_flip_report counts the differing
+    # codes and asserts each is such an element (a bound derived from the oracle's
+    # values, not a fixed pass rate). The output's deviation then splits exactly into
+    # the down-projection's rounding (stage 4's tolerance, given the GPU's
+    # intermediate) and the contribution of the differing codes, computed in fp64.
+    y_ref, mid = O.mlp(w["x"][rows], r_w1q, r_w1s, w["b1"], r_w2q, r_w2s, w["b2"])
+    g_ref = mid["g"]
+    g_tol = REL_TOL * np.abs(g_ref) + RMS_TOL * np.sqrt(np.mean(g_ref ** 2))   # stage 2's bound
+    flips, differ = requant_flip_report(ghq, ghs, mid["hq"], mid["hs"], g_ref.astype(np.float32), g_tol)
+    c_gpu = O.down_projection(ghq, ghs, r_w2q, r_w2s, w["b2"])
+    contrib = np.abs(c_gpu - y_ref)              # exact: the bias cancels
+    bound = REL_TOL * np.abs(c_gpu) + RMS_TOL * np.sqrt(np.mean(c_gpu ** 2)) + contrib
     rep = gemm_tolerance_report(got, y_ref)
+    rep.update(flips)
+    rep["n_outside_derived_bound"] = int((np.abs(got - y_ref) > bound).sum())
     print(f"end-to-end vs independent oracle: {rep}")
-    assert rep["frac_ok"] >= 0.999, rep
+    assert rep["n_outside_derived_bound"] == 0, rep
+    clean = ~differ.any(axis=1)
+    assert np.array_equal(c_gpu[clean], y_ref[clean])   # same intermediate codes: the same oracle output
     assert lib.mx_device_error() == 0
     return rep
 

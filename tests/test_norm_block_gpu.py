@@ -25,7 +25,8 @@ import pytest
 import oracle as O
 import synth
 from mxutil import (REL_TOL, RMS_TOL, assert_codes_equal, assert_gemm_close, assert_swiglu_close,
-                    bf16_from_device, bf16_to_device, f32_from_bf16_bits, mx_rows_to_host, mx_to_host, sample_rows)
+                    bf16_from_device, bf16_to_device, f32_from_bf16_bits, mx_rows_to_host, mx_to_host,
+                    requant_flip_report, sample_rows, swiglu_bound)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,9 +38,14 @@ def _norm_ref_parts(x_bits, shift_bits, scale_bits, eps):
     return np.abs(x * rstd * opp[None, :])
 
 
-def assert_norm_close(y_gpu, x_bits, shift_bits, scale_bits, eps, what):
+def norm_bound(x_bits, shift_bits, scale_bits, eps):
+    """(oracle y, the per-element bound the kernel's fp32 y is held to)."""
     ref = O.rms_norm_modulate(x_bits, shift_bits, scale_bits, eps)
-    bound = 5e-6 * _norm_ref_parts(x_bits, shift_bits, scale_bits, eps) + 2.0 ** -23 * np.abs(ref) + 1e-30
+    return ref, 5e-6 * _norm_ref_parts(x_bits, shift_bits, scale_bits, eps) + 2.0 ** -23 * np.abs(ref) + 1e-30
+
+
+def assert_norm_close(y_gpu, x_bits, shift_bits, scale_bits, eps, what):
+    ref, bound = norm_bound(x_bits, shift_bits, scale_bits, eps)
     err = np.abs(np.asarray(y_gpu, np.float64) - ref)
     bad = np.argwhere(err > bound)
     assert bad.size == 0, f"{what}: {len(bad)} outside, first {bad[:4].tolist()}, worst {float((err / bound).max())}"
@@ -185,9 +191,13 @@ def _run_block(lib, w, rows, in_place=False):
     # stage 2: up-projection + activation, given the GPU's xq
     h = hdbg[idx].cpu().numpy()
     if w["activation"] == "gelu":
-        assert_gemm_close(h, O.up_projection(gxq, gxs, r_wq, r_ws, w["b_up"]), "gelu")
+        h_ref2 = O.up_projection(gxq, gxs, r_wq, r_ws, w["b_up"])
+        assert_gemm_close(h, h_ref2, "gelu")
+        h_tol = REL_TOL * np.abs(h_ref2) + RMS_TOL * np.sqrt(np.mean(h_ref2 ** 2))   # the bound just checked
     else:
-        assert_swiglu_close(h, O.gemm(gxq, gxs, r_wq, r_ws, w["b_up"]), "swiglu")
+        c_up2 = O.gemm(gxq, gxs, r_wq, r_ws, w["b_up"])
+        assert_swiglu_close(h, c_up2, "swiglu")
+        h_tol = swiglu_bound(c_up2)
     ghq, ghs = mx_rows_to_host(hq, rows)
     rhq, rhs = O.quantize_f32(h)
     assert_codes_equal(ghq, rhq, ghs, rhs, "hq")
@@ -197,19 +207,30 @@ def _run_block(lib, w, rows, in_place=False):
     gate_f = f32_from_bf16_bits(w["gate"]).astype(np.float64)
     rep = _gate_res_report(got, c, gate_f, O.gate_residual(c, w["gate"], xr))
     assert rep["n_bad"] == 0, rep
-    # the whole block against an independent oracle run. The normalised activations
-    # are rounded to fp32 before quantization on both sides, in different operation
-    # orders, so a code may legitimately differ where a value sits within an ulp of a
-    # rounding boundary; one such code moves a whole output row. Those rows are
-    # counted (both results are correct) and the rest are compared element-wise.
+    # The whole block against an independent oracle run, which encodes its own fp64
+    # values (rounded to fp32) where the GPU encodes its fp32 ones. Two encodings of
+    # values held to a tolerance can differ only at elements within that tolerance of
+    # a rounding boundary: requant_flip_report counts the differing codes and asserts
+    # each is such an element (the bound is derived from the oracle's values, not a
+    # fixed rate). A differing activation code changes its whole row downstream; those
+    # rows are correct given the GPU's activations (stages 2-3 above). In the other
+    # rows the output's deviation splits exactly into the down-projection's rounding
+    # (stage 3's tolerance, given the GPU's intermediate) and the contribution of the
+    # differing intermediate codes, which the oracle computes exactly.
     y_ref, mid = O.dit_mlp_block(xr, w["shift"], w["scale"], w["gate"], w["eps"], r_wq, r_ws, w["b_up"],
                                  r_w2q, r_w2s, w["b2"], activation=w["activation"])
-    same = np.all(mid["xq"] == gxq, axis=1) & np.all(mid["xs"] == gxs, axis=1)
-    assert (~same).sum() <= max(2, 0.01 * len(rows)), f"{(~same).sum()} rows with a differing activation code"
-    rep = _gate_res_report(got[same], mid["c"][same], gate_f, y_ref[same])
-    rep["rows_with_differing_xq"] = int((~same).sum())
+    a_ref, a_tol = norm_bound(xr, w["shift"], w["scale"], w["eps"])
+    xrep, xdiff = requant_flip_report(gxq, gxs, mid["xq"], mid["xs"], mid["a"].astype(np.float32), a_tol)
+    same = ~xdiff.any(axis=1)   # rows whose activations the two sides encoded alike
+    hrep, _ = requant_flip_report(ghq[same], ghs[same], mid["hq"][same], mid["hs"][same],
+                                  mid["h"][same].astype(np.float32), h_tol[same])
+    contrib = np.abs(gate_f)[None, :] * np.abs(c[same] - mid["c"][same])   # exact, bias cancels
+    err = np.abs(got[same] - y_ref[same])
+    bound = (np.abs(gate_f)[None, :] * (REL_TOL * np.abs(c[same]) + RMS_TOL * np.sqrt(np.mean(c ** 2))) +
+             2.0 ** -8 * np.abs(y_ref[same]) + contrib + 1e-30)
+    rep = {"xq": xrep, "hq": hrep, "n_bad": int((err > bound).sum())}
     print(f"DiT block ({w['activation']}) end-to-end vs independent oracle: {rep}")
-    assert rep["frac_ok"] >= 0.999, rep
+    assert rep["n_bad"] == 0, rep
     assert lib.mx_device_error() == 0
 
 
