@@ -205,9 +205,11 @@ class ClockSampler:
     def summary(self, window: tuple[float, float] | None, min_samples: int = 3, max_pad_s: float = 0.1) -> dict:
         """Median SM clock, maximum clock and power, and throttle reasons of the samples
         taken inside `window` (wall-clock seconds). A window shorter than the sampling
-        interval may hold fewer than `min_samples`: it is then widened on both sides in
-        25 ms steps, up to `max_pad_s`, and the record says by how much. Without any
-        sample near the window, all samples are summarised ("whole sampling run")."""
+        interval may hold fewer than `min_samples`: its end is then moved later in 25 ms
+        steps, up to `max_pad_s` (into the back-to-back steps that follow the timed
+        region; never earlier, where the GPU idled before it), and the record says by
+        how much. Without any sample near the window, all samples are summarised
+        ("whole sampling run")."""
         rows = getattr(self, "rows", [])
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "no samples"}
@@ -215,14 +217,14 @@ class ClockSampler:
         if window is not None:
             pad = 0.0
             while True:
-                use = [r for r in rows if window[0] - pad <= r[0] <= window[1] + pad]
+                use = [r for r in rows if window[0] <= r[0] <= window[1] + pad]
                 if len(use) >= min_samples or pad >= max_pad_s - 1e-9:
                     break
                 pad += 0.025
             if use:
                 label = "timed region" if pad == 0.0 else (
-                    f"timed region widened by +-{pad * 1e3:.0f} ms (the region is shorter than the sampling "
-                    f"interval; the neighbouring samples are of the same back-to-back steps)")
+                    f"timed region and the {pad * 1e3:.0f} ms after it (the region is shorter than the sampling "
+                    f"interval; the samples after it are of the same steps, continued back to back)")
         if not use:
             use, label = rows, "whole sampling run"
         sm = [r[1][0] for r in use]
@@ -670,6 +672,10 @@ def run_gpu(args) -> dict | None:
             "note": "the timed region's rotation of steps, back to back right after it, with no events "
                     "between kernels; clocks from the samples inside this leg's own window"})
         line["sustained"] = sustained
+        if sustained["time_x_mhz"]:
+            # the clock at which the sustained leg's cycles per step give the timed region's
+            # step time: the timed region's effective SM clock, whatever the samples say
+            line["sm_mhz_effective"] = sustained["time_x_mhz"] / (ms_step * 1e3)
     if clk.get("sm_mhz"):
         line["time_x_mhz"] = ms_step * 1e3 * clk["sm_mhz"]
         roof["kernel_time_x_mhz"] = stage_report[dom]["ms"] * 1e3 * clk["sm_mhz"]

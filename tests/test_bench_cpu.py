@@ -69,6 +69,16 @@ def test_clock_record_outside_the_window_ignores_its_reasons():
     assert clk["samples"] == 5 and clk["reasons"] == []
 
 
+def test_clock_record_of_a_short_region_extends_only_forward():
+    t0 = 1_700_000_000.0
+    # region between samples 4 and 5 (+100, +125 ms): no sample inside; the samples
+    # after it (5, 6, 7) are taken, never the ones before it (the GPU idled then)
+    clk = _sampler(_FakeSmi(t0, cap_at=3)).stop(window=(t0 + 0.105, t0 + 0.12))
+    assert clk["samples"] == 3 and clk["reasons"] == []
+    assert clk["sm_mhz"] == pytest.approx(1460)
+    assert clk["window"].startswith("timed region and the 75 ms after it")
+
+
 def test_clock_record_without_samples_in_the_window_falls_back_to_all():
     t0 = 1_700_000_000.0
     clk = _sampler(_FakeSmi(t0, cap_at=2)).stop(window=(t0 + 10.0, t0 + 11.0))
