@@ -524,9 +524,41 @@ def run_gpu(args) -> dict | None:
     barrier(world)
     total_ms = max_over_ranks(start.elapsed_time(stop), world)
 
-    # sustained leg: the same rotation of steps, back to back for a few seconds right
-    # after the timed region, so the power cap has settled and the clock sampler
-    # (every 25 ms) has many samples inside its window
+    per_stage = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in probe) / len(probe) for j in range(n_st)]
+    if mx.mx_device_error() != 0:
+        raise RuntimeError("a kernel reported a device-side wait timeout in the timed region")
+
+    ms_step = total_ms / args.steps
+    work = stage_work(cfg, hi - lo)
+    step_flops = sum(w["flops"] for w in work.values()) * world
+    value = step_flops / (ms_step * 1e-3) / 1e12
+    # the quantizer alone, back to back over the copies with no event between launches
+    # (inside a step its event window also holds the launch gap after the previous kernel)
+    k1_isolated = None
+    k1_name = S_K1 if S_K1 in stage_names else (S_K1N if S_K1N in stage_names else None)
+    if k1_name is not None:
+        k1_fns = [dict(c.stages(mx))[k1_name] for c in copies]
+        for i in range(4):
+            k1_fns[i % len(k1_fns)]()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        n_iso = 50
+        a.record(stream)
+        for i in range(n_iso):
+            k1_fns[i % len(k1_fns)]()
+        b.record(stream)
+        torch.cuda.synchronize()
+        iso_ms = a.elapsed_time(b) / n_iso
+        k1_isolated = {"kernel": k1_name, "us": iso_ms * 1e3,
+                       "gbs": work[k1_name]["bytes"] / (iso_ms * 1e-3) / 1e9,
+                       "launches": n_iso, "note": "back-to-back launches over the input copies, outside the timed region"}
+
+    # sustained leg: the same rotation of steps, back to back for a few seconds after
+    # the timed region (and after the quantizer's isolated timing, which would
+    # otherwise run at the power-capped clock the leg leaves behind), so the power
+    # cap has settled and the clock sampler (every 25 ms) has many samples inside
+    # its window
     sustained = None
     if args.sustain_s > 0:
         n_sus = max(1, int(args.sustain_s / max(total_ms / args.steps * 1e-3, 1e-6)))
@@ -545,14 +577,6 @@ def run_gpu(args) -> dict | None:
         sustained = {"steps": n_sus, "ms_per_step": max_over_ranks(s0.elapsed_time(s1), world) / n_sus,
                      "seconds": t_sus1 - t_sus0, "window": (t_sus0, t_sus1)}
     clk = clocks.stop(window=(t_region0, t_region1))
-    per_stage = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in probe) / len(probe) for j in range(n_st)]
-    if mx.mx_device_error() != 0:
-        raise RuntimeError("a kernel reported a device-side wait timeout in the timed region")
-
-    ms_step = total_ms / args.steps
-    work = stage_work(cfg, hi - lo)
-    step_flops = sum(w["flops"] for w in work.values()) * world
-    value = step_flops / (ms_step * 1e-3) / 1e12
     peaks = load_peaks()
     # The driver measured cuBLAS bf16 both as a burst and as a seconds-long loop under
     # the power cap; take the sustained figure when the power cap acted in our timed
@@ -587,27 +611,6 @@ def run_gpu(args) -> dict | None:
                 "unit": "GB/s", "frac": stage_report[dom]["gbs"] / peaks["hbm_gbs"],
                 "traffic": NCU_TRAFFIC_BYTES.get((args.config, dom))}
 
-    # the quantizer alone, back to back over the copies with no event between launches
-    # (inside a step its event window also holds the launch gap after the previous kernel)
-    k1_isolated = None
-    k1_name = S_K1 if S_K1 in stage_names else (S_K1N if S_K1N in stage_names else None)
-    if k1_name is not None:
-        k1_fns = [dict(c.stages(mx))[k1_name] for c in copies]
-        for i in range(4):
-            k1_fns[i % len(k1_fns)]()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        n_iso = 50
-        a.record(stream)
-        for i in range(n_iso):
-            k1_fns[i % len(k1_fns)]()
-        b.record(stream)
-        torch.cuda.synchronize()
-        iso_ms = a.elapsed_time(b) / n_iso
-        k1_isolated = {"kernel": k1_name, "us": iso_ms * 1e3,
-                       "gbs": work[k1_name]["bytes"] / (iso_ms * 1e-3) / 1e9,
-                       "launches": n_iso, "note": "back-to-back launches over the input copies, outside the timed region"}
 
     # end to end through the public API with host buffers (rank 0's view; all ranks run it)
     e2e = run_e2e(mx, copies, cfg, args, world)

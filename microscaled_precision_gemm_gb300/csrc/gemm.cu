@@ -610,10 +610,14 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
       if constexpr (EPI == kEpiGateRes) {
         uint4 res[4] = {};
         if (live) {
-          // coherent loads: the output may be this very residual (in-place update)
+          // plain coherent loads, not the read-only (non-coherent) path: the output
+          // may be this very residual, written by this kernel (in-place update).
+          // They allocate in L1, so the four 16-byte loads of a thread's 64 bytes
+          // share their two 32-byte sectors (loads that skip L1 fetch each sector
+          // twice: 77% slower at K = 3072)
           const uint4* src = reinterpret_cast<const uint4*>(residual + row * n_total + n);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) res[j] = ld_global_na_v4(src + j);
+          for (int j = 0; j < 4; ++j) res[j] = src[j];
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -120,18 +120,6 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// Coherent 16-byte global load that does not allocate in L1 (each byte is read
-// once). Unlike ld.global.nc it stays valid for memory that the same kernel also
-// writes, such as a residual updated in place.
-__device__ __forceinline__ uint4 ld_global_na_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
-}
-
 // ------------------------------------------------------------------ TMA tensor stores
 
 // Shared-memory writes of the generic proxy become visible to the async proxy
