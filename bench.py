@@ -93,20 +93,21 @@ S_OUT = "out-proj GEMM+bias+gate+residual"
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the current kernels, keyed by (config, kernel); None where no
-# capture of the current kernel exists. Source summaries live in profiles/.
-# Written by hand from profiles/*_full_mlp.md and profiles/*_dit_block_swiglu.md.
+# capture of the current kernel exists. Copied by hand from the ncu traffic
+# captures of the full DiT MLP block and of the SwiGLU DiT sub-block.
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", "K1 quantize"): 125856512 + 19715328,
-    ("full_mlp", "K3 up GEMM+GELU+requant"): 79952128 + 152724224,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 247360512 + 107715072,
-    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125880320 + 21430272,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89568256 + 105759232,
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 278096640 + 104801792,
+    ("full_mlp", "K1 quantize"): 125857280 + 22170112,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 80503296 + 152273408,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 256534016 + 108329472,
+    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125879040 + 24282368,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 91800320 + 104683520,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 284166656 + 104840960,
 }
 
 
 # sm__pipe_tensor_cycles_active as a fraction of elapsed cycles, from one ncu capture
-# of the current kernel (profiles/); None where no capture of the current kernel exists.
+# of the current kernel (its full-set capture); None where no capture of the current
+# kernel exists.
 NCU_TENSOR_PIPE_ACTIVE: dict = {
     ("full_mlp", "K3 up GEMM+GELU+requant"): 0.813,
     ("full_mlp", "K2 down GEMM+bias+BF16"): 0.853,
