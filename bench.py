@@ -109,8 +109,11 @@ NCU_TRAFFIC_BYTES: dict = {
 # of the current kernel (its full-set capture); None where no capture of the current
 # kernel exists.
 NCU_TENSOR_PIPE_ACTIVE: dict = {
-    ("full_mlp", "K3 up GEMM+GELU+requant"): 0.813,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 0.853,
+    ("full_mlp", "K3 up GEMM+GELU+requant"): 0.816,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 0.857,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 0.845,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 0.805,
+    ("attn_out", "out-proj GEMM+bias+gate+residual"): 0.663,
 }
 
 
