@@ -150,6 +150,38 @@ mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_c
   return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+// The MLP's workspace cut into its parts: MXFP6 x, MXFP6 h, and the split-tail
+// region when the workspace holds it (its first kernel zeroes the arrival counters).
+struct MlpWorkspace {
+  void* xq;
+  void* xs;
+  void* hq;
+  void* hs;
+  void* split;          // null: the GEMMs run unsplit
+  size_t split_bytes;
+  unsigned* zero;       // the counter words the first kernel zeroes (null with no split region)
+  int zero_count;
+};
+
+mx_status slice_mlp_workspace(int64_t M, int64_t d, int64_t ff, void* workspace, size_t workspace_bytes,
+                              MlpWorkspace* w) {
+  if (workspace == nullptr) return MX_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
+  const MlpLayout l = mlp_layout(M, d, ff);
+  if (workspace_bytes < l.base) return MX_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  w->xq = ws + l.xq;
+  w->xs = ws + l.xs;
+  w->hq = ws + l.hq;
+  w->hs = ws + l.hs;
+  // the split tail runs when the workspace holds its region (mx_mlp_workspace_bytes)
+  w->split = workspace_bytes >= l.total && l.total > l.base ? ws + l.split : nullptr;
+  w->split_bytes = w->split != nullptr ? workspace_bytes - l.split : 0;
+  w->zero = static_cast<unsigned*>(w->split);
+  w->zero_count = static_cast<int>(mxk::kArrivalsBytes / sizeof(unsigned));
+  return MX_OK;
+}
+
 // K1 -> up-projection (GELU, or SwiGLU on the stacked gate/up weight) -> K2.
 mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, const void* w_up_codes,
                    const void* w_up_scales, const void* b_up, const void* w2_codes, const void* w2_scales,
@@ -159,36 +191,26 @@ mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, 
   const int64_t n_up = up_epi == MX_EPI_BIAS_SWIGLU_MXFP6 ? 2 * ff : ff;
   if (M == 0) return MX_OK;
   if (x == nullptr || w_up_codes == nullptr || w_up_scales == nullptr || w2_codes == nullptr ||
-      w2_scales == nullptr || y == nullptr || workspace == nullptr)
+      w2_scales == nullptr || y == nullptr)
     return MX_ERR_INVALID_ARG;
-  if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
-  const MlpLayout l = mlp_layout(M, d, ff);
-  if (workspace_bytes < l.base) return MX_ERR_WORKSPACE_TOO_SMALL;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* xq = ws + l.xq;
-  void* xs = ws + l.xs;
-  void* hq = ws + l.hq;
-  void* hs = ws + l.hs;
-  // the split tail runs when the workspace holds its region (mx_mlp_workspace_bytes)
-  void* sw = workspace_bytes >= l.total && l.total > l.base ? ws + l.split : nullptr;
-  const size_t sbytes = sw != nullptr ? workspace_bytes - l.split : 0;
-  unsigned* zero = static_cast<unsigned*>(sw);
-  const int nzero = static_cast<int>(mxk::kArrivalsBytes / sizeof(unsigned));
-  st = check_quantize(x, M, d, d, xq, xs);
+  MlpWorkspace w;
+  if ((st = slice_mlp_workspace(M, d, ff, workspace, workspace_bytes, &w)) != MX_OK) return st;
+  st = check_quantize(x, M, d, d, w.xq, w.xs);
   if (st != MX_OK) return st;
-  st = check_gemm(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr);
+  st = check_gemm(w.xq, w.xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, w.hq, w.hs, nullptr);
   if (st != MX_OK) return st;
-  st = check_gemm(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr);
+  st = check_gemm(w.hq, w.hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr);
   if (st != MX_OK) return st;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
-  if (mxk::launch_quantize_bf16(x, M, d, d, xq, xs, sms, stream, zero, nzero) != cudaSuccess) return MX_ERR_CUDA;
-  st = gemm_launch(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr, sms, stream, sw,
-                   sbytes);
+  if (mxk::launch_quantize_bf16(x, M, d, d, w.xq, w.xs, sms, stream, w.zero, w.zero_count) != cudaSuccess)
+    return MX_ERR_CUDA;
+  st = gemm_launch(w.xq, w.xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, w.hq, w.hs, nullptr, sms, stream,
+                   w.split, w.split_bytes);
   if (st != MX_OK) return st;
   // the up-projection leaves the arrival counters at zero again
-  return gemm_launch(hq, hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr, sms,
-                     stream, sw, sbytes);
+  return gemm_launch(w.hq, w.hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr, sms,
+                     stream, w.split, w.split_bytes);
 }
 
 // The MLP half of a DiT block: fused norm quantizer -> up-projection -> down-projection
@@ -205,25 +227,15 @@ mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const 
   if (st != MX_OK) return st;
   if (M == 0) return MX_OK;
   if (x == nullptr || w_up_codes == nullptr || w_up_scales == nullptr || w2_codes == nullptr ||
-      w2_scales == nullptr || y == nullptr || workspace == nullptr)
+      w2_scales == nullptr || y == nullptr)
     return MX_ERR_INVALID_ARG;
-  if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
-  const MlpLayout l = mlp_layout(M, d, ff);
-  if (workspace_bytes < l.base) return MX_ERR_WORKSPACE_TOO_SMALL;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* xq = ws + l.xq;
-  void* xs = ws + l.xs;
-  void* hq = ws + l.hq;
-  void* hs = ws + l.hs;
-  void* sw = workspace_bytes >= l.total && l.total > l.base ? ws + l.split : nullptr;
-  const size_t sbytes = sw != nullptr ? workspace_bytes - l.split : 0;
-  unsigned* zero = static_cast<unsigned*>(sw);
-  const int nzero = static_cast<int>(mxk::kArrivalsBytes / sizeof(unsigned));
-  st = check_norm_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr);
+  MlpWorkspace w;
+  if ((st = slice_mlp_workspace(M, d, ff, workspace, workspace_bytes, &w)) != MX_OK) return st;
+  st = check_norm_quantize(x, M, d, d, shift, scale, eps, w.xq, w.xs, nullptr);
   if (st != MX_OK) return st;
-  st = check_gemm(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr);
+  st = check_gemm(w.xq, w.xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, w.hq, w.hs, nullptr);
   if (st != MX_OK) return st;
-  st = check_gemm(hq, hs, w2_codes, w2_scales, b2, M, d, ff, kEpiGateResidual, y, nullptr, nullptr);
+  st = check_gemm(w.hq, w.hs, w2_codes, w2_scales, b2, M, d, ff, kEpiGateResidual, y, nullptr, nullptr);
   if (st != MX_OK) return st;
   if (gate != nullptr && !aligned(gate, 16)) return MX_ERR_MISALIGNED;
   const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), y0 = reinterpret_cast<uintptr_t>(y);
@@ -231,14 +243,14 @@ mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const 
   if (x0 != y0 && x0 < y0 + bytes && y0 < x0 + bytes) return MX_ERR_INVALID_ARG;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
-  if (mxk::launch_norm_modulate_quantize(x, M, d, d, shift, scale, eps, xq, xs, nullptr, sms, stream, zero, nzero) !=
-      cudaSuccess)
+  if (mxk::launch_norm_modulate_quantize(x, M, d, d, shift, scale, eps, w.xq, w.xs, nullptr, sms, stream, w.zero,
+                                         w.zero_count) != cudaSuccess)
     return MX_ERR_CUDA;
-  st = gemm_launch(xq, xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, hq, hs, nullptr, sms, stream, sw,
-                   sbytes);
+  st = gemm_launch(w.xq, w.xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, w.hq, w.hs, nullptr, sms, stream,
+                   w.split, w.split_bytes);
   if (st != MX_OK) return st;
-  return gemm_launch(hq, hs, w2_codes, w2_scales, b2, M, d, ff, kEpiGateResidual, y, nullptr, nullptr, sms, stream,
-                     sw, sbytes, gate, x);
+  return gemm_launch(w.hq, w.hs, w2_codes, w2_scales, b2, M, d, ff, kEpiGateResidual, y, nullptr, nullptr, sms,
+                     stream, w.split, w.split_bytes, gate, x);
 }
 
 }  // namespace
