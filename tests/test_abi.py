@@ -327,3 +327,22 @@ def test_quantize_stacked_rejects_bad_arguments(lib):
     assert call([128, 64], codes=A32b + 16) == MISALIGNED
     assert call([128, 1 << 31]) == SHAPE
     assert call([0, 0], ptrs=[0, 0], codes=0, scales=0) == OK   # nothing to quantize
+
+
+def test_c_hot_path_program_compiles_and_links(mx, tmp_path):
+    """The C program the GPU test runs (tests/helpers/c_hot_path.c) is valid C11 against
+    include/mx.h and links against the library and the CUDA runtime."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc")
+    cuda = "/usr/local/cuda"
+    cuda_lib = next((p for p in (os.path.join(cuda, "lib64"), os.path.join(cuda, "lib"))
+                     if os.path.exists(os.path.join(p, "libcudart.so"))), None)
+    if cc is None or cuda_lib is None:
+        pytest.skip("gcc or the CUDA runtime is not available")
+    lib_dir = os.path.dirname(mx.library_path())
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I",
+                    os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "helpers", "c_hot_path.c"), "-o",
+                    str(tmp_path / "c_hot_path"), "-L", lib_dir, "-lmxfp6", "-L", cuda_lib, "-lcudart",
+                    "-Wl,-rpath," + lib_dir], check=True)

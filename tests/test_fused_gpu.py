@@ -102,6 +102,34 @@ def test_quantize_stacked_is_concatenation(lib):
     assert torch.equal(st.codes, whole.codes) and torch.equal(st.scales, whole.scales)
 
 
+def test_quantize_stacked_strided_parts_and_ragged_last(lib):
+    """Four parts (the query/key/value/gate layout) with their own row strides, the
+    last one ragged: equal to quantizing the concatenation, and to the oracle, code
+    for code; the padding rows' scales are zero."""
+    import torch
+
+    rng = np.random.default_rng(21)
+    k, rows = 384, [256, 128, 384, 100]
+    mats = [synth.bf16_round(rng.standard_normal((r, k)).astype(np.float32) * (0.5 + i)) for i, r in enumerate(rows)]
+    parts = []
+    for i, m in enumerate(mats):
+        pad = 8 * (i + 1)                               # row stride k + pad elements
+        buf = torch.zeros((m.shape[0], k + pad), dtype=torch.bfloat16, device="cuda")
+        buf[:, :k] = bf16_to_device(m)
+        parts.append(buf[:, :k])
+    st = lib.mx_quantize_stacked(parts)
+    cat = np.concatenate(mats)
+    whole = lib.mx_quantize(bf16_to_device(cat))
+    assert torch.equal(st.codes, whole.codes) and torch.equal(st.scales, whole.scales)
+    codes = O.unpack_codes(st.codes.cpu().numpy(), k)
+    scales = O.scales_tiled_to_plain(st.scales.cpu().numpy(), sum(rows), k)
+    rq, rs = O.quantize_bf16(cat)
+    assert_codes_equal(codes, rq, scales, rs, "stacked")
+    tiled = st.scales.cpu().numpy()
+    pad_rows = np.arange(sum(rows), (sum(rows) + 127) // 128 * 128)
+    assert np.all(tiled[[O._tiled_offset(r, b, k) for r in pad_rows for b in range(k // 32)]] == 0)
+
+
 def _run_gated_mlp(lib, w, rows):
     import torch
 
