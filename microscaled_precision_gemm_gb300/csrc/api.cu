@@ -334,8 +334,10 @@ mx_status mx_quantize_stacked(const void* const* x_parts, const int64_t* part_ro
     if (st != MX_OK) return st;
     total += r;
   }
-  mx_status st = check_quantize(x_parts[0], total, K, K, codes, scales);
-  if (st != MX_OK || total == 0) return st;
+  if (total == 0) return MX_OK;
+  // the stacked tensor's own size limit (the parts were each within it)
+  if (total * (K / 32) > (int64_t{1} << 32) - (int64_t{1} << 28)) return MX_ERR_UNSUPPORTED_SHAPE;
+  mx_status st = MX_OK;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
   int64_t r0 = 0;

@@ -327,6 +327,9 @@ def test_quantize_stacked_rejects_bad_arguments(lib):
     assert call([128, 64], codes=A32b + 16) == MISALIGNED
     assert call([128, 1 << 31]) == SHAPE
     assert call([0, 0], ptrs=[0, 0], codes=0, scales=0) == OK   # nothing to quantize
+    # an empty first part may have a null pointer; the call then goes on to the device
+    assert call([0, 64], ptrs=[0, A32]) not in (OK, INVALID, SHAPE, MISALIGNED)
+    assert call([1 << 23, 1 << 23], k=8192) == SHAPE          # each part fits the size limit, the stack does not
 
 
 def test_c_hot_path_program_compiles_and_links(mx, tmp_path):
