@@ -48,6 +48,7 @@ __all__ = [
     "mx_gemm",
     "mx_gemm_gate_residual",
     "mx_mlp",
+    "mx_mlp_noalloc",
     "mx_gated_mlp",
     "mx_dit_mlp_block",
     "MX_ACT_GELU_TANH",
@@ -134,6 +135,7 @@ def load():
                                                    ctypes.POINTER(ctypes.c_int)]),
             "mx_mlp_workspace_bytes": (sz, [i64, i64, i64]),
             "mx_mlp": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "mx_mlp_noalloc": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]),
             "mx_gated_mlp": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "mx_gemm_gate_residual": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, sz, vp]),
             "mx_quantize_rmsnorm_modulate": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, ctypes.c_float, vp, vp, vp,
@@ -443,6 +445,31 @@ def mx_mlp(x, w1: MxTensor, b1, w2: MxTensor, b2, y=None, workspace=None, stream
                     _ptr(w2.scales), _ptr(b2), _ptr(y), _ptr(workspace), workspace.numel(),
                     _stream_handle(stream))
     _check(st, "mx_mlp")
+    return y
+
+
+def mx_mlp_noalloc(x, w1: MxTensor, b1, w2: MxTensor, b2, y=None, stream=None):
+    """mx_mlp through the library's static scratch (mx_mlp_noalloc): no workspace is
+    allocated for the call. For callers that must not allocate device memory; sizes
+    beyond the scratch raise MxError(MX_ERR_WORKSPACE_TOO_SMALL). Calls that overlap
+    on the GPU share the scratch and race: order them on one stream."""
+    torch = _torch()
+    lib = load()
+    dev = _bf16_matrix(x, "x").device
+    m, d = x.shape
+    ff = w1.rows
+    if w1.k != d or w2.rows != d or w2.k != ff:
+        raise ValueError("weight shapes do not match x")
+    _mx_on(w1, dev, "w1", ff, d)
+    _mx_on(w2, dev, "w2", d, ff)
+    _vec(b1, dev, "b1", ff)
+    _vec(b2, dev, "b2", d)
+    if y is None:
+        y = torch.empty((m, d), dtype=torch.bfloat16, device=x.device)
+    _on(y, dev, "y", torch.bfloat16, m * d)
+    st = lib.mx_mlp_noalloc(_ptr(x), m, d, ff, _ptr(w1.codes), _ptr(w1.scales), _ptr(b1), _ptr(w2.codes),
+                            _ptr(w2.scales), _ptr(b2), _ptr(y), _stream_handle(stream))
+    _check(st, "mx_mlp_noalloc")
     return y
 
 

@@ -80,6 +80,19 @@ def test_noalloc_matches_mx_mlp_on_two_calls(lib):
     assert lib.mx_device_error() == 0
 
 
+def test_noalloc_binding_matches_mx_mlp(lib):
+    """The Python binding's mx_mlp_noalloc (argument marshalling only) gives mx_mlp's
+    result bit for bit, and a size beyond the scratch raises."""
+    import torch
+
+    w = synth.full_mlp(M=300, d=256, ff=512)
+    x = bf16_to_device(w["x"])
+    w1, w2 = lib.mx_quantize(bf16_to_device(w["w1"])), lib.mx_quantize(bf16_to_device(w["w2"]))
+    b1, b2 = bf16_to_device(w["b1"]), bf16_to_device(w["b2"])
+    assert torch.equal(lib.mx_mlp_noalloc(x, w1, b1, w2, b2), lib.mx_mlp(x, w1, b1, w2, b2))
+    assert lib.mx_device_error() == 0
+
+
 def test_noalloc_refuses_sizes_beyond_its_scratch(lib):
     fn = _noalloc_fn(lib)
     # 5591 tokens of a d=3072, ff=12288 block need more than the 64 MiB scratch;
