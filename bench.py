@@ -199,9 +199,14 @@ class ClockSampler:
                     continue
                 try:
                     t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    vals = (float(parts[1]), float(parts[2]), float(parts[3]))
+                    clk = (float(parts[1]), float(parts[2]))
                 except ValueError:
                     continue
+                try:
+                    power = float(parts[3])
+                except ValueError:   # "[N/A]" where the board does not report it
+                    power = None
+                vals = (clk[0], clk[1], power)
                 active = {name for name, val in zip(self.NAMES, parts[4:8]) if val.lower().startswith("active")}
                 self.rows.append((t, vals, active))
         return self.summary(window)
@@ -233,10 +238,10 @@ class ClockSampler:
             use, label = rows, "whole sampling run"
         sm = [r[1][0] for r in use]
         smax = [r[1][1] for r in use]
-        power = [r[1][2] for r in use]
+        power = [r[1][2] for r in use if r[1][2] is not None]
         reasons = set().union(*(r[2] for r in use))
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power), "window": label}
+                "samples": len(sm), "power_w_max": max(power) if power else None, "window": label}
 
 
 def _pci_bus_id(device_index: int) -> str | None:

@@ -79,6 +79,26 @@ def test_clock_record_of_a_short_region_extends_only_forward():
     assert clk["window"].startswith("timed region and the 75 ms after it")
 
 
+class _FakeSmiNoPower(_FakeSmi):
+    """As _FakeSmi, on a board that reports no power draw ("[N/A]")."""
+
+    def communicate(self, timeout=None):
+        out, err = super().communicate(timeout)
+        lines = []
+        for ln in out.strip().splitlines():
+            p = ln.split(", ")
+            p[3] = "[N/A]"
+            lines.append(", ".join(p))
+        return "\n".join(lines) + "\n", err
+
+
+def test_clock_record_without_power_readings():
+    t0 = 1_700_000_000.0
+    clk = _sampler(_FakeSmiNoPower(t0, cap_at=5)).stop(window=(t0 + 0.06, t0 + 0.16))
+    assert clk["samples"] == 4 and clk["power_w_max"] is None
+    assert clk["sm_mhz"] == pytest.approx((1440 + 1450) / 2)
+
+
 def test_clock_record_without_samples_in_the_window_falls_back_to_all():
     t0 = 1_700_000_000.0
     clk = _sampler(_FakeSmi(t0, cap_at=2)).stop(window=(t0 + 10.0, t0 + 11.0))
