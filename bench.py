@@ -563,6 +563,30 @@ def run_gpu(args) -> dict | None:
                        "gbs": work[k1_name]["bytes"] / (iso_ms * 1e-3) / 1e9,
                        "launches": n_iso, "note": "back-to-back launches over the input copies, outside the timed region"}
 
+    # every GEMM stage alone, back to back over the copies (its launches overlap one
+    # another's prologue and tail as consecutive launches of one kernel do), outside
+    # the timed region: the kernel's own rate, without the step's other kernels
+    gemms_isolated = {}
+    for name in stage_names:
+        if not work[name]["flops"]:
+            continue
+        fns = [dict(c.stages(mx))[name] for c in copies]
+        for i in range(3):
+            fns[i % len(fns)]()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        n_iso = 20
+        a.record(stream)
+        for i in range(n_iso):
+            fns[i % len(fns)]()
+        b.record(stream)
+        torch.cuda.synchronize()
+        g_ms = a.elapsed_time(b) / n_iso
+        tf = work[name]["flops"] / (g_ms * 1e-3) / 1e12
+        gemms_isolated[name] = {"us": g_ms * 1e3, "tflops": tf, "frac_fp6_peak_spec": tf / FP6_SPEC_PEAK_TFLOPS,
+                                "launches": n_iso}
+
     # sustained leg: the same rotation of steps, back to back for a few seconds after
     # the timed region (and after the quantizer's isolated timing, which would
     # otherwise run at the power-capped clock the leg leaves behind), so the power
@@ -670,6 +694,12 @@ def run_gpu(args) -> dict | None:
         if k1_isolated is not None:
             k1_isolated["frac_hbm"] = k1_isolated["gbs"] / peaks["hbm_gbs"]
             line["quantize_isolated"] = k1_isolated
+    if gemms_isolated:
+        for rep in gemms_isolated.values():
+            rep["frac_fp6_peak_measured"] = rep["tflops"] / fp6_peak
+        line["gemms_isolated"] = gemms_isolated
+        line["gemms_isolated_note"] = ("each GEMM stage launched alone 20 times back to back over the input copies, "
+                                       "outside the timed region")
     if bf16_ctx is not None:
         line["bf16_context"] = bf16_ctx
     if sustained is not None:

@@ -40,6 +40,8 @@ def test_bench_line_contract(lib):
     assert set(d["roofline"]) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
     assert d["sustained"]["steps"] >= 1 and d["sustained"]["ms_per_step"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    iso = d["gemms_isolated"]["K2 GEMM+bias+BF16"]
+    assert iso["us"] > 0 and iso["launches"] == 20
 
 
 def test_reference_arm_line(lib):
