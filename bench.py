@@ -90,6 +90,14 @@ S_DOWNR = "K2 down GEMM+bias+gate+residual"
 S_GEMM = "K2 GEMM+bias+BF16"
 S_QKV = "QKV+gate GEMM+bias+BF16"
 S_OUT = "out-proj GEMM+bias+gate+residual"
+# the quantizer fused into the GEMM (mx_quantize_gemm: the quantize kernel encodes the
+# rows of the first two rounds of tiles, the GEMM the rest while it runs): two launches
+S_QUP = "K1 lead rows + K3 up GEMM (in-kernel quantizer)+GELU+requant"
+S_QGU = "K1 lead rows + K3 gate/up GEMM (in-kernel quantizer)+SwiGLU+requant"
+S_QGEMM = "K1 lead rows + GEMM (in-kernel quantizer)+bias+BF16"
+S_QQKV = "K1 lead rows + QKV+gate GEMM (in-kernel quantizer)+bias+BF16"
+S_QOUT = "K1 lead rows + out-proj GEMM (in-kernel quantizer)+bias+gate+residual"
+FUSED_STAGES = (S_QUP, S_QGU, S_QGEMM, S_QQKV, S_QOUT)
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the current kernels, keyed by (config, kernel); None where no
@@ -265,10 +273,11 @@ def _bf16_dev(bits, dev):
 class Workload:
     """Device-resident inputs and outputs of one copy of the configuration."""
 
-    def __init__(self, mx, cfg: dict, seed: int, dev, m_rows: int, split: bool = True):
+    def __init__(self, mx, cfg: dict, seed: int, dev, m_rows: int, split: bool = True, fused: bool = True):
         import torch
 
         self.cfg = cfg
+        self.fused = fused
         kind = cfg["kind"]
         M, d, ff = m_rows, cfg["d"], cfg["ff"]
         self.M, self.d, self.ff = M, d, ff
@@ -355,33 +364,64 @@ class Workload:
         # (a workspace smaller than mx_gemm_workspace_bytes runs the GEMMs unsplit)
         self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
         self.split = split
+        # mx_quantize_gemm's workspace (MXFP6 activations + row-block counters)
+        self.qws = None
+        if kind in ("mlp", "gated_mlp", "up", "gemm", "qkv", "attn_out"):
+            self.qws = torch.empty(max(256, mx.mx_quantize_gemm_workspace_bytes(M, d)), dtype=torch.uint8,
+                                   device=dev)
         torch.cuda.synchronize()
+
+    def quantizer(self, mx):
+        """(name, callable) of the step's whole quantizer, launched on its own."""
+        kind = self.cfg["kind"]
+        if kind in ("block", "attn_in"):
+            return S_K1N, lambda: mx.mx_quantize_rmsnorm_modulate(self.x, self.shift, self.scale, self.eps,
+                                                                  out=self.xq)
+        if kind == "down":
+            return None, None
+        src = self.a if kind == "attn_out" else self.x
+        return S_K1, lambda: mx.mx_quantize(src, out=self.xq)
 
     def stages(self, mx):
         """The step's launches as (name, callable) in stream order."""
         kind = self.cfg["kind"]
         swiglu = kind == "gated_mlp" or (kind == "block" and self.cfg["activation"] == "swiglu")
+        epi_up = mx.MX_EPI_BIAS_SWIGLU_MXFP6 if swiglu else mx.MX_EPI_BIAS_GELU_MXFP6
         out = []
-        if kind in ("mlp", "gated_mlp", "up", "gemm", "qkv"):
-            out.append((S_K1, lambda: mx.mx_quantize(self.x, out=self.xq)))
+        if self.fused and kind in ("mlp", "gated_mlp", "up"):
+            out.append((S_QGU if swiglu else S_QUP,
+                        lambda: mx.mx_quantize_gemm(self.x, self.w1, self.b1, epi_up, out=self.hq, workspace=self.qws)))
+        elif self.fused and kind in ("gemm", "qkv"):
+            out.append((S_QQKV if kind == "qkv" else S_QGEMM,
+                        lambda: mx.mx_quantize_gemm(self.x, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y,
+                                                    workspace=self.qws)))
+        elif self.fused and kind == "attn_out":
+            out.append((S_QOUT, lambda: mx.mx_quantize_gemm(self.a, self.w2, self.b2, mx.MX_EPI_GATE_RESIDUAL_BF16,
+                                                            gate=self.gate, residual=self.x, out=self.y,
+                                                            workspace=self.qws)))
+        else:
+            if kind in ("mlp", "gated_mlp", "up", "gemm", "qkv"):
+                out.append((S_K1, lambda: mx.mx_quantize(self.x, out=self.xq)))
+            if kind == "attn_out":
+                out.append((S_K1, lambda: mx.mx_quantize(self.a, out=self.xq)))
+                out.append((S_OUT, lambda: mx.mx_gemm_gate_residual(self.xq, self.w2, self.b2, self.gate, self.x,
+                                                                    out=self.y, workspace=self.ws)))
+            if kind in ("mlp", "gated_mlp", "up"):
+                out.append((S_GU if swiglu else S_UP, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, epi_up,
+                                                                             out=self.hq, workspace=self.ws)))
+            if kind in ("gemm", "qkv"):
+                out.append((S_QKV if kind == "qkv" else S_GEMM,
+                            lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y,
+                                               workspace=self.ws)))
         if kind in ("block", "attn_in"):
             out.append((S_K1N, lambda: mx.mx_quantize_rmsnorm_modulate(self.x, self.shift, self.scale, self.eps,
                                                                        out=self.xq)))
         if kind == "attn_in":
             out.append((S_QKV, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y,
                                                      workspace=self.ws)))
-        if kind == "attn_out":
-            out.append((S_K1, lambda: mx.mx_quantize(self.a, out=self.xq)))
-            out.append((S_OUT, lambda: mx.mx_gemm_gate_residual(self.xq, self.w2, self.b2, self.gate, self.x,
-                                                                out=self.y, workspace=self.ws)))
-        if kind in ("mlp", "gated_mlp", "up", "block"):
-            epi = mx.MX_EPI_BIAS_SWIGLU_MXFP6 if swiglu else mx.MX_EPI_BIAS_GELU_MXFP6
-            out.append((S_GU if swiglu else S_UP, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, epi, out=self.hq,
+        if kind == "block":
+            out.append((S_GU if swiglu else S_UP, lambda: mx.mx_gemm(self.xq, self.w1, self.b1, epi_up, out=self.hq,
                                                                          workspace=self.ws)))
-        if kind in ("gemm", "qkv"):
-            out.append((S_QKV if kind == "qkv" else S_GEMM,
-                        lambda: mx.mx_gemm(self.xq, self.w1, self.b1, mx.MX_EPI_BIAS_BF16, out=self.y,
-                                                     workspace=self.ws)))
         if kind in ("mlp", "gated_mlp", "down"):
             out.append((S_DOWN, lambda: mx.mx_gemm(self.hq, self.w2, self.b2, mx.MX_EPI_BIAS_BF16, out=self.y,
                                                      workspace=self.ws)))
@@ -437,14 +477,23 @@ def bf16_context(shapes: list, dev, iters: int = 20) -> dict | None:
 
 
 def mlp_min_workspace_bytes(mx, M: int, d: int, ff: int) -> int:
-    """MLP workspace without the split-tail region: MXFP6 x and h, 256-byte aligned parts."""
-    parts = (mx.mx_codes_bytes(M, d), mx.mx_scales_bytes(M, d), mx.mx_codes_bytes(M, ff), mx.mx_scales_bytes(M, ff))
+    """MLP workspace without the split-tail region: MXFP6 x and h and a counter word
+    per 128 rows, 256-byte aligned parts."""
+    parts = (mx.mx_codes_bytes(M, d), mx.mx_scales_bytes(M, d), mx.mx_codes_bytes(M, ff), mx.mx_scales_bytes(M, ff),
+             4 * (-(-M // 128)))
     return sum(-(-n // 256) * 256 for n in parts)
 
 
-def stage_work(cfg: dict, M: int) -> dict:
-    """Algorithmic flops / bytes per launch of each stage (0.78125 = 0.75 code +
-    1/32 scale bytes per MXFP6 element)."""
+def quantizer_bytes(cfg: dict, M: int) -> float:
+    """Algorithmic bytes of quantizing the step's activations: BF16 in, MXFP6 out."""
+    return M * cfg["d"] * (2 + 0.78125)
+
+
+def stage_work(cfg: dict, M: int, fused: bool = False) -> dict:
+    """Algorithmic flops / bytes per launch of each stage of the step (0.78125 = 0.75
+    code + 1/32 scale bytes per MXFP6 element). fused: the quantizer runs inside the
+    GEMM that reads its output (Workload.stages with fused=True), and that stage does
+    both one's work."""
     d, ff = cfg["d"], cfg["ff"]
     kind = cfg["kind"]
     swiglu = kind == "gated_mlp" or (kind == "block" and cfg.get("activation") == "swiglu")
@@ -471,6 +520,13 @@ def stage_work(cfg: dict, M: int) -> dict:
         out[S_DOWN] = {"flops": 2.0 * M * d * ff, "bytes": M * ff * q + d * ff * q + M * d * 2}
     if kind == "block":
         out[S_DOWNR] = {"flops": 2.0 * M * d * ff, "bytes": M * ff * q + d * ff * q + M * d * 4}
+    if fused and kind in ("mlp", "gated_mlp", "up", "gemm", "qkv", "attn_out"):
+        # the quantizer stage folds into the GEMM stage that reads its output
+        k1 = out.pop(S_K1)
+        for merged, gemm in ((S_QUP, S_UP), (S_QGU, S_GU), (S_QGEMM, S_GEMM), (S_QQKV, S_QKV), (S_QOUT, S_OUT)):
+            if gemm in out:
+                g = out.pop(gemm)
+                out[merged] = {"flops": g["flops"], "bytes": g["bytes"] + k1["bytes"]}
     return out
 
 
@@ -492,7 +548,8 @@ def run_gpu(args) -> dict | None:
     M = cfg["M"]
     lo, hi = shard_rows(M, world, rank)
     # two independent copies; copy i uses seed (2*rank + i) so every rank's batch is its own
-    copies = [Workload(mx, cfg, seed=2 * rank + i, dev=dev, m_rows=hi - lo, split=not args.no_split)
+    copies = [Workload(mx, cfg, seed=2 * rank + i, dev=dev, m_rows=hi - lo, split=not args.no_split,
+                       fused=not args.unfused)
               for i in range(args.copies)]
     stream = torch.cuda.current_stream()
     stage_names = [n for n, _ in copies[0].stages(mx)]
@@ -538,15 +595,15 @@ def run_gpu(args) -> dict | None:
         raise RuntimeError("a kernel reported a device-side wait timeout in the timed region")
 
     ms_step = total_ms / args.steps
-    work = stage_work(cfg, hi - lo)
+    work = stage_work(cfg, hi - lo, fused=not args.unfused)
     step_flops = sum(w["flops"] for w in work.values()) * world
     value = step_flops / (ms_step * 1e-3) / 1e12
     # the quantizer alone, back to back over the copies with no event between launches
     # (inside a step its event window also holds the launch gap after the previous kernel)
     k1_isolated = None
-    k1_name = S_K1 if S_K1 in stage_names else (S_K1N if S_K1N in stage_names else None)
+    k1_name = copies[0].quantizer(mx)[0]
     if k1_name is not None:
-        k1_fns = [dict(c.stages(mx))[k1_name] for c in copies]
+        k1_fns = [c.quantizer(mx)[1] for c in copies]
         for i in range(4):
             k1_fns[i % len(k1_fns)]()
         torch.cuda.synchronize()
@@ -560,7 +617,7 @@ def run_gpu(args) -> dict | None:
         torch.cuda.synchronize()
         iso_ms = a.elapsed_time(b) / n_iso
         k1_isolated = {"kernel": k1_name, "us": iso_ms * 1e3,
-                       "gbs": work[k1_name]["bytes"] / (iso_ms * 1e-3) / 1e9,
+                       "gbs": quantizer_bytes(cfg, hi - lo) / (iso_ms * 1e-3) / 1e9,
                        "launches": n_iso, "note": "back-to-back launches over the input copies, outside the timed region"}
 
     # every GEMM stage alone, back to back over the copies (its launches overlap one
@@ -676,12 +733,14 @@ def run_gpu(args) -> dict | None:
                          "each step's working set exceeds the 129 MB L2, so no step reads operands the "
                          "previous step left in L2" if args.copies > 1 else "single copy (profiling run)",
                    "parallelism": f"token-sharded x{world}, weights replicated, no collective",
-                   "split_tail": not args.no_split},
+                   "split_tail": not args.no_split,
+                   "quantizer_in_gemm": not args.unfused},
         "ms_per_mlp": ms_step if cfg["kind"] in ("mlp", "gated_mlp", "block") else None,
         "stages": stage_report,
         "roofline": roof,
         "pct_fp6_peak_spec_5pf": value / FP6_SPEC_PEAK_TFLOPS,
-        "gpu_launches": args.steps * n_st,
+        # a fused stage is two launches (the quantize kernel, then the GEMM)
+        "gpu_launches": args.steps * sum(2 if n in FUSED_STAGES else 1 for n in stage_names),
         "clocks": clk,
         "gpu": {"name": torch.cuda.get_device_name(dev),
                 "sms": torch.cuda.get_device_properties(dev).multi_processor_count},
@@ -691,9 +750,16 @@ def run_gpu(args) -> dict | None:
     if k1 is not None:
         line["quantize_gbs"] = stage_report[k1]["gbs"]
         line["quantize_frac_hbm"] = stage_report[k1]["gbs"] / peaks["hbm_gbs"]
-        if k1_isolated is not None:
-            k1_isolated["frac_hbm"] = k1_isolated["gbs"] / peaks["hbm_gbs"]
-            line["quantize_isolated"] = k1_isolated
+    elif k1_isolated is not None:
+        # the step quantizes inside the GEMM: the standalone quantizer's rate, launched alone
+        line["quantize_gbs"] = k1_isolated["gbs"]
+        line["quantize_frac_hbm"] = k1_isolated["gbs"] / peaks["hbm_gbs"]
+        line["quantize_note"] = ("the timed step quantizes the activations inside the GEMM (the quantize kernel "
+                                 "encodes only the rows of the first two rounds of tiles); quantize_gbs is the "
+                                 "standalone quantizer over all rows, launched alone")
+    if k1_isolated is not None:
+        k1_isolated["frac_hbm"] = k1_isolated["gbs"] / peaks["hbm_gbs"]
+        line["quantize_isolated"] = k1_isolated
     if gemms_isolated:
         for rep in gemms_isolated.values():
             rep["frac_fp6_peak_measured"] = rep["tflops"] / fp6_peak
@@ -778,6 +844,9 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
         elif kind == "attn_in":
             mx.mx_quantize_rmsnorm_modulate(x_buf[slot], c.shift, c.scale, c.eps, out=c.xq, stream=s_comp)
             mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp, workspace=c.ws)
+        elif kind == "attn_out" and c.fused:
+            mx.mx_quantize_gemm(x_buf[slot], c.w2, c.b2, mx.MX_EPI_GATE_RESIDUAL_BF16, gate=c.gate, residual=c.x,
+                                out=y_buf[slot], workspace=c.qws, stream=s_comp)
         elif kind == "attn_out":
             mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
             mx.mx_gemm_gate_residual(c.xq, c.w2, c.b2, c.gate, c.x, out=y_buf[slot], stream=s_comp,
@@ -785,10 +854,17 @@ def run_e2e(mx, copies, cfg, args, world) -> dict:
         elif kind == "down":
             mx.mx_gemm(mx.MxTensor(x_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), c.w2, c.b2,
                        mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp, workspace=c.ws)
+        elif kind == "up" and c.fused:
+            mx.mx_quantize_gemm(x_buf[slot], c.w1, c.b1, mx.MX_EPI_BIAS_GELU_MXFP6,
+                                out=mx.MxTensor(y_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), workspace=c.qws,
+                                stream=s_comp)
         elif kind == "up":
             mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
             mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_GELU_MXFP6,
                        out=mx.MxTensor(y_buf[slot], c.hq.scales, c.hq.rows, c.hq.k), stream=s_comp, workspace=c.ws)
+        elif c.fused:
+            mx.mx_quantize_gemm(x_buf[slot], c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], workspace=c.qws,
+                                stream=s_comp)
         else:
             mx.mx_quantize(x_buf[slot], out=c.xq, stream=s_comp)
             mx.mx_gemm(c.xq, c.w1, c.b1, mx.MX_EPI_BIAS_BF16, out=y_buf[slot], stream=s_comp, workspace=c.ws)
@@ -1030,6 +1106,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU work for the baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="quantize all activations in their own kernel before the GEMM (the timed step's "
+                         "single-GEMM stages only; mx_mlp always quantizes inside its up-projection)")
     ap.add_argument("--no-split", action="store_true",
                     help="run the GEMMs without the split tail (the same work, tiles whole; for comparison)")
     ap.add_argument("--sustain-s", type=float, default=3.0,

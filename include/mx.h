@@ -64,7 +64,9 @@ typedef enum {
 typedef enum {
   MX_EPI_BIAS_BF16 = 0,          /* out = bf16_rne(acc + bias): the down-projection (K2)       */
   MX_EPI_BIAS_GELU_MXFP6 = 1,    /* out = MXFP6(gelu_tanh(acc + bias)): the up-projection (K3)  */
-  MX_EPI_BIAS_SWIGLU_MXFP6 = 2   /* stacked gate/up weight: out = MXFP6(silu(g) * u)            */
+  MX_EPI_BIAS_SWIGLU_MXFP6 = 2,  /* stacked gate/up weight: out = MXFP6(silu(g) * u)            */
+  MX_EPI_GATE_RESIDUAL_BF16 = 3  /* out = bf16(residual + gate * (acc + bias)): mx_quantize_gemm
+                                    only (mx_gemm_gate_residual is this epilogue on MXFP6 input) */
 } mx_epilogue;
 
 typedef enum {
@@ -240,24 +242,63 @@ mx_status mx_gemm_launch_plan(int64_t M, int64_t N, int64_t K, size_t workspace_
                               int* split_tiles);
 
 /*
+ * mx_quantize_gemm -- mx_quantize of BF16 activations fused with the GEMM that
+ * reads them ("Optimizing Krea 3 on AMD Instinct MI355X", section "Fusion cut
+ * intermediate memory traffic": activations quantized on the fly, once):
+ *   xq = MXFP6(x) (the mx_quantize rule, bit for bit), then
+ *   out = epilogue(xq * B^T + bias) as mx_gemm (epi 0-2), or, with
+ *   MX_EPI_GATE_RESIDUAL_BF16, as mx_gemm_gate_residual (gate, residual).
+ * The quantize kernel encodes the leading rows (and zeroes the workspace's
+ * counters); the GEMM quantizes the remaining rows itself, in an extra warp per
+ * CTA, while its main loop runs, so the encoding of most of x overlaps the
+ * tensor-core work. The leading rows are those the GEMM's first two rounds of
+ * tiles read; for N < 12288 (where the extra warps would fall behind the GEMM's
+ * reads) they are all M rows, and the GEMM runs as mx_gemm. Two launches on `stream`.
+ *   x        : device BF16 [M][K] row-major, row stride ld_x elements (ld_x % 8 == 0),
+ *              16-byte aligned; must not overlap out or the workspace
+ *   b_*, bias, N, K, out, out_scales : as mx_gemm (K % 128 == 0, N % 256 == 0)
+ *   gate, residual : MX_EPI_GATE_RESIDUAL_BF16 only, as mx_gemm_gate_residual
+ *              (residual required; out may be residual itself); ignored otherwise
+ *   workspace: device, mx_quantize_gemm_workspace_bytes(M, K) bytes, 256-byte
+ *              aligned, any contents. After the call (in stream order) it holds
+ *              MXFP6(x): codes at offset 0 (mx_codes_bytes(M, K) bytes), tiled
+ *              scales at offset mx_codes_bytes(M, K) rounded up to 256, then one
+ *              counter word per 128 rows (zeroed by the call's quantize kernel).
+ * No split tail, no debug output. M == 0 or N == 0: nothing is launched.
+ * Not for two calls at once on one workspace.
+ */
+size_t mx_quantize_gemm_workspace_bytes(int64_t M, int64_t K);
+
+mx_status mx_quantize_gemm(const void* x, int64_t M, int64_t K, int64_t ld_x, const void* b_codes,
+                           const void* b_scales, const void* bias, int64_t N, mx_epilogue epi, const void* gate,
+                           const void* residual, void* out, void* out_scales, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Workspace bytes of mx_mlp, mx_gated_mlp and mx_dit_mlp_block for M tokens:
- * MXFP6 x (M x d), MXFP6 h (M x ff) and the split-tail region both GEMMs use in
- * turn (as mx_gemm_workspace_bytes, for the wider of the two). A smaller workspace
- * that still holds x and h (the first four parts) runs without the split tail.
+ * MXFP6 x (M x d), MXFP6 h (M x ff), one counter word per 128 rows (the
+ * up-projection's in-kernel quantizer) and the split-tail region both GEMMs use in
+ * turn (as mx_gemm_workspace_bytes, for the wider of the two), each part starting
+ * on a 256-byte boundary. A smaller workspace that still holds the first five
+ * parts runs without the split tail.
  */
 size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff);
 
 /*
  * mx_mlp -- the whole MXFP6 MLP block in three launches on `stream`:
  *   K1 xq = MXFP6(x); K3 hq = MXFP6(gelu_tanh(xq W1^T + b1)); K2 y = bf16(hq W2^T + b2).
+ *   As in mx_quantize_gemm, K1 encodes only the leading rows of x (those K3's
+ *   first two rounds of tiles read), and K3 encodes the rest itself while it runs
+ *   (when its width, ff or 2 ff, is at least 12288, it does not split its tail, and
+ *   the leading rows are not all of x); the result is the same bit for bit.
  *   x        : BF16 [M][d] (16-byte aligned); y: BF16 [M][d] (written)
  *   w1_*     : W1 as MXFP6, ff x d (quantized once with mx_quantize)
  *   w2_*     : W2 as MXFP6, d x ff
  *   b1, b2   : BF16 [ff], [d], or NULL
  *   d % 256 == 0, ff % 256 == 0 (both are K of one GEMM and N of the other)
  *   workspace: device, mx_mlp_workspace_bytes(M, d, ff) bytes, 256-byte aligned;
- *              holds xq, hq and the split-tail scratch (the first kernel zeroes its
- *              arrival counters, so no initialisation is needed); must not overlap
+ *              holds xq, hq, the row-block counters and the split-tail scratch (the
+ *              first kernel zeroes the counters, so no initialisation is needed); must not overlap
  *              any other argument. Without
  *              room for the split-tail region the GEMMs run unsplit; without room
  *              for xq and hq the call returns MX_ERR_WORKSPACE_TOO_SMALL.
@@ -349,7 +390,9 @@ mx_status mx_scales_from_plain(const void* plain_host, void* tiled_host, int64_t
  * mx_device_error -- synchronizes the current device and reads the device-side
  * error word of the library's kernels (0 = none; bit 0: a producer wait ran out,
  * bit 1: an MMA wait, bit 2: an epilogue wait, bit 3: draining after an abort ran
- * out, bit 4: mx_selftest_wait_timeout ran). clear != 0 resets it. Returns MX_ERR_CUDA if the read itself fails.
+ * out, bit 4: mx_selftest_wait_timeout ran, bit 5: a GEMM that quantizes its own
+ * activations (mx_quantize_gemm, mx_mlp, mx_gated_mlp) gave up waiting for a block
+ * of them). clear != 0 resets it. Returns MX_ERR_CUDA if the read itself fails.
  */
 mx_status mx_device_error(unsigned* flags_host, int clear);
 

@@ -32,6 +32,7 @@ __all__ = [
     "MX_EPI_BIAS_BF16",
     "MX_EPI_BIAS_GELU_MXFP6",
     "MX_EPI_BIAS_SWIGLU_MXFP6",
+    "MX_EPI_GATE_RESIDUAL_BF16",
     "MxTensor",
     "load",
     "library_path",
@@ -47,6 +48,9 @@ __all__ = [
     "mx_quantize_stacked",
     "mx_gemm",
     "mx_gemm_gate_residual",
+    "mx_quantize_gemm",
+    "mx_quantize_gemm_workspace_bytes",
+    "mx_quantize_gemm_xq",
     "mx_mlp",
     "mx_mlp_noalloc",
     "mx_gated_mlp",
@@ -65,6 +69,7 @@ __all__ = [
 MX_EPI_BIAS_BF16 = 0
 MX_EPI_BIAS_GELU_MXFP6 = 1
 MX_EPI_BIAS_SWIGLU_MXFP6 = 2
+MX_EPI_GATE_RESIDUAL_BF16 = 3
 MX_ACT_GELU_TANH = 0
 MX_ACT_SWIGLU = 1
 MX_GEMM_WORKSPACE_COUNTER_BYTES = 10240
@@ -90,6 +95,8 @@ EXPORTED_SYMBOLS = (
     "mx_gemm_workspace_bytes",
     "mx_gemm_launch_plan",
     "mx_quantize_stacked",
+    "mx_quantize_gemm_workspace_bytes",
+    "mx_quantize_gemm",
 )
 
 _lib = None
@@ -138,6 +145,9 @@ def load():
             "mx_mlp_noalloc": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]),
             "mx_gated_mlp": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "mx_gemm_gate_residual": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, sz, vp]),
+            "mx_quantize_gemm_workspace_bytes": (sz, [i64, i64]),
+            "mx_quantize_gemm": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, i64, ctypes.c_int, vp, vp, vp, vp,
+                                                vp, sz, vp]),
             "mx_quantize_rmsnorm_modulate": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, ctypes.c_float, vp, vp, vp,
                                                             vp]),
             "mx_dit_mlp_block": (ctypes.c_int, [vp, i64, i64, i64, vp, vp, vp, ctypes.c_float, ctypes.c_int, vp, vp,
@@ -499,6 +509,66 @@ def mx_gemm_gate_residual(a: MxTensor, b: MxTensor, bias, gate, residual, out=No
                                    _stream_handle(stream))
     _check(st, "mx_gemm_gate_residual")
     return out
+
+
+def mx_quantize_gemm_workspace_bytes(m: int, k: int) -> int:
+    return load().mx_quantize_gemm_workspace_bytes(m, k)
+
+
+def mx_quantize_gemm(x, b: MxTensor, bias=None, epilogue: int = MX_EPI_BIAS_BF16, gate=None, residual=None,
+                     out=None, workspace=None, stream=None):
+    """mx_quantize(x) and the GEMM on it in one pass: the GEMM quantizes most rows of
+    the BF16 activations itself while its main loop runs. ``epilogue`` as mx_gemm, or
+    MX_EPI_GATE_RESIDUAL_BF16 with ``gate`` / ``residual`` as mx_gemm_gate_residual
+    (out may be residual). Returns out (BF16 tensor or MxTensor); ``workspace`` (uint8,
+    mx_quantize_gemm_workspace_bytes) then holds MXFP6(x): see mx_quantize_gemm_xq."""
+    torch = _torch()
+    lib = load()
+    dev = _cuda_device(x, "x")
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a CUDA bfloat16 [M][K] tensor with unit column stride")
+    m, k = x.shape
+    n = b.rows
+    if b.k != k:
+        raise ValueError("inner dimensions differ")
+    _mx_on(b, dev, "b", n, k)
+    _vec(bias, dev, "bias", n)
+    out_scales = None
+    if epilogue == MX_EPI_GATE_RESIDUAL_BF16:
+        if residual is None or tuple(residual.shape) != (m, n):
+            raise ValueError("residual must be a contiguous bfloat16 [M][N] tensor")
+        _on(residual, dev, "residual", torch.bfloat16, m * n)
+        _vec(gate, dev, "gate", n)
+    if epilogue in (MX_EPI_BIAS_BF16, MX_EPI_GATE_RESIDUAL_BF16):
+        if out is None:
+            out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        _on(out, dev, "out", torch.bfloat16, m * n)
+        out_ptr = _ptr(out)
+    else:
+        w = n // 2 if epilogue == MX_EPI_BIAS_SWIGLU_MXFP6 else n
+        if out is None:
+            out = MxTensor(_empty_u8(lib.mx_codes_bytes(m, w), dev).view(m, -1) if m else
+                           _empty_u8(0, dev).view(0, w // 4 * 3),
+                           _empty_u8(lib.mx_scales_bytes(m, w), dev), m, w)
+        _mx_on(out, dev, "out", m, w)
+        out_ptr, out_scales = _ptr(out.codes), _ptr(out.scales)
+    if workspace is None:
+        workspace = _empty_u8(max(lib.mx_quantize_gemm_workspace_bytes(m, k), 256), dev)
+    _on(workspace, dev, "workspace", torch.uint8)
+    st = lib.mx_quantize_gemm(_ptr(x), m, k, x.stride(0), _ptr(b.codes), _ptr(b.scales), _ptr(bias), n,
+                              int(epilogue), _ptr(gate), _ptr(residual), out_ptr, out_scales, _ptr(workspace),
+                              workspace.numel(), _stream_handle(stream))
+    _check(st, "mx_quantize_gemm")
+    return out
+
+
+def mx_quantize_gemm_xq(workspace, m: int, k: int) -> MxTensor:
+    """The MXFP6(x) that mx_quantize_gemm left in its workspace, as views of it."""
+    lib = load()
+    cb, sb = lib.mx_codes_bytes(m, k), lib.mx_scales_bytes(m, k)
+    off = -(-cb // 256) * 256
+    return MxTensor(workspace[:cb].view(m, -1) if m else workspace[:0].view(0, k // 4 * 3),
+                    workspace[off:off + sb], m, k)
 
 
 def mx_gated_mlp(x, wgu: MxTensor, bgu, w2: MxTensor, b2, y=None, workspace=None, stream=None):

@@ -71,8 +71,9 @@ mx_status check_norm_quantize(const void* x, int64_t rows, int64_t K, int64_t ld
   return MX_OK;
 }
 
-// epi: an mx_epilogue value, or kEpiGateResidual for mx_gemm_gate_residual.
-constexpr int kEpiGateResidual = 3;
+// epi: an mx_epilogue value; MX_EPI_GATE_RESIDUAL_BF16 only through mx_gemm_gate_residual,
+// mx_quantize_gemm and the DiT block.
+constexpr int kEpiGateResidual = MX_EPI_GATE_RESIDUAL_BF16;
 
 bool mxfp6_out(int epi) { return epi == MX_EPI_BIAS_GELU_MXFP6 || epi == MX_EPI_BIAS_SWIGLU_MXFP6; }
 
@@ -99,12 +100,13 @@ mx_status check_gemm(const void* a_codes, const void* a_scales, const void* b_co
   return MX_OK;
 }
 
-// MLP workspace: xq | xs | hq | hs, then the split-tail region both GEMMs use in
-// turn (the first kernel zeroes its arrival counters). `base` is the smallest
-// workspace the MLP runs with (no split tail), `total` the one mx_mlp_workspace_bytes
-// reports.
+// MLP workspace: xq | xs | hq | hs | the in-kernel quantizer's row-block counters,
+// then the split-tail region both GEMMs use in turn (the first kernel zeroes the
+// counters and the split tail's arrival counters, which are contiguous). `base` is
+// the smallest workspace the MLP runs with (no split tail), `total` the one
+// mx_mlp_workspace_bytes reports.
 struct MlpLayout {
-  size_t xq, xs, hq, hs, split, base, total;
+  size_t xq, xs, hq, hs, ready, split, base, total;
 };
 
 MlpLayout mlp_layout(int64_t M, int64_t d, int64_t ff) {
@@ -113,7 +115,8 @@ MlpLayout mlp_layout(int64_t M, int64_t d, int64_t ff) {
   l.xs = align256(l.xq + static_cast<size_t>(mxk::codes_bytes(M, d)));
   l.hq = align256(l.xs + static_cast<size_t>(mxk::scales_bytes(M, d)));
   l.hs = align256(l.hq + static_cast<size_t>(mxk::codes_bytes(M, ff)));
-  l.split = align256(l.hs + static_cast<size_t>(mxk::scales_bytes(M, ff)));
+  l.ready = align256(l.hs + static_cast<size_t>(mxk::scales_bytes(M, ff)));
+  l.split = align256(l.ready + 4 * static_cast<size_t>(mxk::qa_counter_words(M)));
   l.base = l.split;
   // the up-projection is at most 2 ff wide (the stacked gate/up weight)
   const size_t up = mxk::split_workspace_bytes(M, 2 * ff, d), down = mxk::split_workspace_bytes(M, d, ff);
@@ -121,11 +124,21 @@ MlpLayout mlp_layout(int64_t M, int64_t d, int64_t ff) {
   return l;
 }
 
+// In-kernel quantizer of a GEMM launch (x null: none): A = MXFP6(x) goes to the
+// A operand's buffers; rows below lead_rows are there already and the counters
+// `ready` are zero.
+struct QaLaunch {
+  const void* x = nullptr;
+  int64_t ld_x = 0;
+  int64_t lead_rows = 0;
+  unsigned* ready = nullptr;
+};
+
 // split_ws: split-tail workspace (arrival counters zero) or null.
 mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_codes, const void* b_scales,
                       const void* bias, int64_t M, int64_t N, int64_t K, int epi, void* out, void* out_scales,
                       float* dbg, int num_sms, cudaStream_t stream, void* split_ws, size_t split_bytes,
-                      const void* gate = nullptr, const void* residual = nullptr) {
+                      const void* gate = nullptr, const void* residual = nullptr, const QaLaunch& qa = QaLaunch()) {
   if (M == 0 || N == 0) return MX_OK;
   mxk::GemmArgs a;
   a.a_codes = a_codes;
@@ -144,6 +157,10 @@ mx_status gemm_launch(const void* a_codes, const void* a_scales, const void* b_c
   a.epilogue = epi;
   a.workspace = split_ws;
   a.workspace_bytes = split_ws != nullptr ? split_bytes : 0;
+  a.x = qa.x;
+  a.ld_x = qa.ld_x;
+  a.lead_rows = qa.lead_rows;
+  a.ready = qa.ready;
   bool encode_failed = false;
   cudaError_t e = mxk::launch_gemm(a, num_sms, stream, &encode_failed);
   if (encode_failed) return MX_ERR_CUDA;
@@ -157,9 +174,10 @@ struct MlpWorkspace {
   void* xs;
   void* hq;
   void* hs;
+  unsigned* ready;      // the in-kernel quantizer's row-block counters
   void* split;          // null: the GEMMs run unsplit
   size_t split_bytes;
-  unsigned* zero;       // the counter words the first kernel zeroes (null with no split region)
+  unsigned* zero;       // the counter words the first kernel zeroes
   int zero_count;
 };
 
@@ -175,10 +193,13 @@ mx_status slice_mlp_workspace(int64_t M, int64_t d, int64_t ff, void* workspace,
   w->hq = ws + l.hq;
   w->hs = ws + l.hs;
   // the split tail runs when the workspace holds its region (mx_mlp_workspace_bytes)
+  w->ready = reinterpret_cast<unsigned*>(ws + l.ready);
   w->split = workspace_bytes >= l.total && l.total > l.base ? ws + l.split : nullptr;
   w->split_bytes = w->split != nullptr ? workspace_bytes - l.split : 0;
-  w->zero = static_cast<unsigned*>(w->split);
-  w->zero_count = static_cast<int>(mxk::kArrivalsBytes / sizeof(unsigned));
+  // the row-block counters, and the split tail's arrival counters right after them
+  w->zero = w->ready;
+  w->zero_count = static_cast<int>(((w->split != nullptr ? l.split + mxk::kArrivalsBytes : l.split) - l.ready) /
+                                   sizeof(unsigned));
   return MX_OK;
 }
 
@@ -203,10 +224,24 @@ mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, 
   if (st != MX_OK) return st;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
-  if (mxk::launch_quantize_bf16(x, M, d, d, w.xq, w.xs, sms, stream, w.zero, w.zero_count) != cudaSuccess)
+  // the up-projection quantizes x itself beyond the rows its first two rounds of
+  // tiles read, which the quantize kernel encodes first (unless the up-projection
+  // splits its tail, or those rows are all of x)
+  QaLaunch qa;
+  int clusters = 0;
+  if (mxk::gemm_max_clusters(&clusters) != cudaSuccess) return MX_ERR_CUDA;
+  const int64_t lead = mxk::qa_lead_rows(M, n_up, clusters);
+  if (lead < M && mxk::plan_gemm(M, n_up, d, clusters, w.split, w.split_bytes).sk_tiles == 0) {
+    qa.x = x;
+    qa.ld_x = d;
+    qa.lead_rows = lead;
+    qa.ready = w.ready;
+  }
+  if (mxk::launch_quantize_bf16(x, qa.x != nullptr ? lead : M, d, d, w.xq, w.xs, sms, stream, w.zero,
+                                w.zero_count) != cudaSuccess)
     return MX_ERR_CUDA;
   st = gemm_launch(w.xq, w.xs, w_up_codes, w_up_scales, b_up, M, n_up, d, up_epi, w.hq, w.hs, nullptr, sms, stream,
-                   w.split, w.split_bytes);
+                   w.split, w.split_bytes, nullptr, nullptr, qa);
   if (st != MX_OK) return st;
   // the up-projection leaves the arrival counters at zero again
   return gemm_launch(w.hq, w.hs, w2_codes, w2_scales, b2, M, d, ff, MX_EPI_BIAS_BF16, y, nullptr, nullptr, sms,
@@ -251,6 +286,24 @@ mx_status dit_block_impl(const void* x, int64_t M, int64_t d, int64_t ff, const 
   if (st != MX_OK) return st;
   return gemm_launch(w.hq, w.hs, w2_codes, w2_scales, b2, M, d, ff, kEpiGateResidual, y, nullptr, nullptr, sms,
                      stream, w.split, w.split_bytes, gate, x);
+}
+
+// mx_quantize_gemm's workspace: MXFP6(x) codes | tiled scales | row-block counters.
+struct QgLayout {
+  size_t xs, ready, total;
+};
+
+QgLayout qg_layout(int64_t M, int64_t K) {
+  QgLayout l;
+  l.xs = align256(static_cast<size_t>(mxk::codes_bytes(M, K)));
+  l.ready = align256(l.xs + static_cast<size_t>(mxk::scales_bytes(M, K)));
+  l.total = align256(l.ready + 4 * static_cast<size_t>(mxk::qa_counter_words(M)));
+  return l;
+}
+
+bool overlaps(const void* a, uintptr_t a_bytes, const void* b, uintptr_t b_bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
 }
 
 }  // namespace
@@ -425,6 +478,67 @@ mx_status mx_gemm_launch_plan(int64_t M, int64_t N, int64_t K, size_t workspace_
   *pairs = p.clusters;
   *split_tiles = p.sk_tiles;
   return MX_OK;
+}
+
+size_t mx_quantize_gemm_workspace_bytes(int64_t M, int64_t K) {
+  if (M < 0 || K < 0) return 0;
+  return qg_layout(M, K).total;
+}
+
+mx_status mx_quantize_gemm(const void* x, int64_t M, int64_t K, int64_t ld_x, const void* b_codes,
+                           const void* b_scales, const void* bias, int64_t N, mx_epilogue epi, const void* gate,
+                           const void* residual, void* out, void* out_scales, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  const int e = static_cast<int>(epi);
+  if (e < MX_EPI_BIAS_BF16 || e > MX_EPI_GATE_RESIDUAL_BF16) return MX_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || ld_x < K) return MX_ERR_INVALID_ARG;
+  const QgLayout l = qg_layout(M, K);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // the shape and pointer rules of mx_quantize and of the GEMM, on the workspace's parts
+  const bool empty = M == 0 || N == 0;
+  void* xq = empty ? nullptr : ws;
+  void* xs = empty ? nullptr : ws + l.xs;
+  mx_status st = check_quantize(x, empty ? 0 : M, K, ld_x, xq, xs);
+  if (st != MX_OK) return st;
+  st = check_gemm(xq, xs, b_codes, b_scales, bias, M, N, K, e, out, out_scales, nullptr);
+  if (st != MX_OK || empty) return st;
+  if (workspace == nullptr) return MX_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
+  if (workspace_bytes < l.total) return MX_ERR_WORKSPACE_TOO_SMALL;
+  const uintptr_t x_bytes = static_cast<uintptr_t>((M - 1) * ld_x + K) * 2u;
+  const uintptr_t out_bytes = static_cast<uintptr_t>(mxfp6_out(e) ? mxk::codes_bytes(M, e == MX_EPI_BIAS_SWIGLU_MXFP6 ? N / 2 : N)
+                                                                   : M * N * 2);
+  if (e == MX_EPI_GATE_RESIDUAL_BF16) {
+    if (residual == nullptr) return MX_ERR_INVALID_ARG;
+    if (!aligned(residual, 16) || (gate != nullptr && !aligned(gate, 16))) return MX_ERR_MISALIGNED;
+    // the residual may be the output itself (in-place update), but not overlap it otherwise
+    if (residual != out && overlaps(residual, out_bytes, out, out_bytes)) return MX_ERR_INVALID_ARG;
+  }
+  // x is read while the output and the workspace are written
+  if (overlaps(x, x_bytes, out, out_bytes) || overlaps(x, x_bytes, workspace, l.total) ||
+      overlaps(out, out_bytes, workspace, l.total))
+    return MX_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_check(&sms)) != MX_OK) return st;
+  int clusters = 0;
+  if (mxk::gemm_max_clusters(&clusters) != cudaSuccess) return MX_ERR_CUDA;
+  // the quantize kernel encodes the rows the first two rounds of tiles read and
+  // zeroes the counters; the GEMM encodes the rest itself
+  QaLaunch qa;
+  const int64_t lead = mxk::qa_lead_rows(M, N, clusters);
+  unsigned* ready = reinterpret_cast<unsigned*>(ws + l.ready);
+  if (lead < M) {
+    qa.x = x;
+    qa.ld_x = ld_x;
+    qa.lead_rows = lead;
+    qa.ready = ready;
+  }
+  if (mxk::launch_quantize_bf16(x, lead, K, ld_x, xq, xs, sms, stream, ready,
+                                static_cast<int>(mxk::qa_counter_words(M))) != cudaSuccess)
+    return MX_ERR_CUDA;
+  const bool gr = e == MX_EPI_GATE_RESIDUAL_BF16;
+  return gemm_launch(xq, xs, b_codes, b_scales, bias, M, N, K, e, out, mxfp6_out(e) ? out_scales : nullptr, nullptr,
+                     sms, stream, nullptr, 0, gr ? gate : nullptr, gr ? residual : nullptr, qa);
 }
 
 size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff) {

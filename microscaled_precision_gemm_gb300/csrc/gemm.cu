@@ -45,6 +45,11 @@
 //               32 rows. Each thread storing its own row instead (a 16- or 8-byte
 //               piece of 32 rows per store instruction) kept busy the
 //               shared-memory pipe that the main loop's operand traffic needs.
+//   warp 11     (QA instance only, each CTA) the in-kernel quantizer: encodes A's
+//               BF16 rows to MXFP6 (the quantizer's rule and layout) while the
+//               main loop runs, and publishes each 128-row block on a counter in
+//               global memory; producers wait for a block's counter before their
+//               first load of it (see QaArgs below).
 // Every mbarrier wait suspends the waiting thread until its phase completes (a
 // try_wait suspend-time hint: spinning waits took issue slots from the MMA and
 // TMA threads) and is bounded (2 s on the global timer); on expiry the kernel
@@ -86,6 +91,8 @@ constexpr int kEpiWarps = 8;                     // 2 per tensor-memory lane qua
 constexpr int kEpiCols = BN * 4 / kEpiWarps;     // accumulator columns each epilogue warp drains
 constexpr int kEpiChunks = kEpiCols / 32;        // 32-column MX blocks per epilogue thread
 constexpr int kThreads = (3 + kEpiWarps) * 32;  // + scale-copy warp
+constexpr int kQaWarp = 3 + kEpiWarps;           // the QA instance's quantizer warp
+constexpr int kThreadsQa = kThreads + 32;
 constexpr uint32_t kABytes = BM * BK;  // 16-byte shared slot per 16 codes -> 1 byte per element
 constexpr uint32_t kBBytes = kBHalfRows * BK;   // this CTA's half of the B tile
 constexpr uint32_t kSfaBytes = kAtomBytes;
@@ -262,6 +269,132 @@ __device__ __forceinline__ bool cursor_next(const Plan& pl, Cursor& k, Unit& u) 
   return false;
 }
 
+// In-kernel quantizer (QA instance). The rows of row blocks [0, first_block) were
+// encoded before the launch; the rest -- rows up to M rounded up to 128, padding
+// rows getting zero scales -- are cut into items of one row's 1024-column strip
+// (one 32-element block per lane, as the quantize kernel encodes them), groups of
+// kQaGroup items in row order, group g done by the quantizer warp of CTA
+// g mod #CTAs. Each group is published on its 128-row block's counter (release
+// after the stores); a producer acquires the counter of its A row block, until it
+// reads 128 x strips, before the first TMA load of that block. The counters are
+// zero at the launch (the quantize kernel before it zeroes them). Every CTA's
+// quantizer warp runs without waiting on anything, so every block is published
+// whatever the other roles do; producers of CTAs that are resident wait only on
+// warps that are resident too or will be once the previous kernel has left.
+struct QaArgs {
+  const uint16_t* x;   // BF16 A [M][K], row stride ld_x elements
+  int64_t ld_x;
+  uint8_t* codes;      // the A operand the tensor maps read
+  uint8_t* scales;
+  unsigned* ready;     // one counter per 128-row block
+  int first_block;
+  int strips;          // 1024-column strips per row
+  int wide;            // x and its row stride 32-byte aligned: 32-byte loads
+};
+
+// Producer side: acquire the counter of A row block mb until it reads 128 x strips
+// (every item of the block published), then a proxy fence so that the tensor loads
+// that follow read the block. False when the wait gave up.
+__device__ __forceinline__ bool acquire_quantized(const QaArgs& qa, int mb, volatile int* abort_flag) {
+  const uint32_t target = 128u * static_cast<uint32_t>(qa.strips);
+  const unsigned* c = qa.ready + mb;
+  if (ld_acquire_gpu(c) < target) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; ld_acquire_gpu(c) < target; ++i) {
+      sleep_ns(200);
+      if ((i & 15) == 0) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kTimeoutNs) {
+          *abort_flag = 1;
+          atomicOr(&g_error_word, kErrWaitQuant);
+          return false;
+        }
+      }
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
+// The quantizer warp (all 32 lanes). An item is one row's 1024-column strip (2 KB
+// of BF16); lane l encodes its K-block 32 s + l (64 contiguous bytes) with the
+// quantize kernel's block encoder. Memory instructions per item are kept few
+// (they share the SM's memory pipeline with the main loop): two 32-byte loads per
+// lane where x allows them (wide: 32-byte aligned rows), else four 16-byte loads;
+// the lane's 24 code bytes as one 16-byte and one 8-byte store (which comes first
+// depends on the lane's 8-byte phase); one 4-byte scale word per four lanes. Loads
+// of a group's kQaGroup items are issued together.
+__device__ __forceinline__ void run_quantizer(const QaArgs& qa, int m_total, int k_total, int lane) {
+  const uint32_t strips = static_cast<uint32_t>(qa.strips);
+  const uint32_t kblocks = static_cast<uint32_t>(k_total / kBlock);
+  const uint32_t first = static_cast<uint32_t>(qa.first_block) * 128u * strips;
+  const uint32_t items = static_cast<uint32_t>(pad_rows(m_total)) * strips;
+  const uint32_t groups = items > first ? (items - first) / kQaGroup : 0u;
+  const int64_t pitch = static_cast<int64_t>(k_total) / 4 * 3;
+  const bool odd = (lane & 1) != 0;   // the lane's codes start 8 bytes into a 16-byte unit
+  for (uint32_t q = blockIdx.x; q < groups; q += gridDim.x) {
+    const uint32_t i0 = first + q * kQaGroup;
+    uint4 raw[kQaGroup][4];
+    uint32_t row[kQaGroup], kb[kQaGroup];
+#pragma unroll
+    for (int g = 0; g < kQaGroup; ++g) {
+      row[g] = (i0 + g) / strips;
+      kb[g] = ((i0 + g) - row[g] * strips) * 32u + lane;
+      const bool live = row[g] < static_cast<uint32_t>(m_total) && kb[g] < kblocks;
+      const uint16_t* src = qa.x + static_cast<int64_t>(row[g]) * qa.ld_x + kb[g] * 32u;
+      if (!live) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) raw[g][j] = make_uint4(0, 0, 0, 0);
+      } else if (qa.wide) {
+        ld_nc_v8(src, raw[g][0], raw[g][1]);
+        ld_nc_v8(src + 16, raw[g][2], raw[g][3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) raw[g][j] = ld_nc(src + 8 * j);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kQaGroup; ++g) {
+      // BF16 -> fp32 is exact, so the fp32 block encoder gives the BF16 rule's result;
+      // a padding row's zeros give a zero scale
+      float f[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t v[4] = {raw[g][j].x, raw[g][j].y, raw[g][j].z, raw[g][j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          f[8 * j + 2 * i] = __uint_as_float(v[i] << 16);
+          f[8 * j + 2 * i + 1] = __uint_as_float(v[i] & 0xFFFF0000u);
+        }
+      }
+      uint32_t w[6];
+      const uint32_t sc = quant_block32(f, w);
+      // four consecutive lanes (K-blocks 4c .. 4c + 3 of the row) -> one tiled scale word;
+      // the strip's valid lanes come in whole fours (K % 128 == 0)
+      const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
+      const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
+      const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
+      if (kb[g] < kblocks) {
+        if ((lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(qa.scales + scale_word_offset(row[g], kb[g] / 4, k_total)) =
+              sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        if (row[g] < static_cast<uint32_t>(m_total)) {
+          // 24 bytes at 24 kb: 16-byte aligned for an even lane (16 + 8 bytes), 8 bytes
+          // past a 16-byte boundary for an odd one (8 + 16 bytes)
+          uint8_t* d = qa.codes + static_cast<int64_t>(row[g]) * pitch + kb[g] * 24u;
+          *reinterpret_cast<uint4*>(d + (odd ? 8 : 0)) =
+              odd ? make_uint4(w[2], w[3], w[4], w[5]) : make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint2*>(d + (odd ? 0 : 16)) = odd ? make_uint2(w[0], w[1]) : make_uint2(w[4], w[5]);
+        }
+      }
+    }
+    // the group's four items lie in one 128-row block (128 x strips is a multiple of 4)
+    fence_proxy_async_global();
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(qa.ready + i0 / strips / 128u, kQaGroup);
+  }
+}
+
 __device__ __forceinline__ void pair_tile(const Plan& pl, int tile, int rank, int* mb, int* nb) {
   const int pm = tile / pl.num_n;
   *nb = tile - pm * pl.num_n;
@@ -271,19 +404,35 @@ __device__ __forceinline__ void pair_tile(const Plan& pl, int tile, int rank, in
 // gated: B is the stacked [gate; up] weight of 2 * n_out rows; CTA 0 of the pair
 // stages gate rows [128 nb, 128 nb + 128) and CTA 1 the up rows n_out rows further,
 // and both SMs' tensor memory gets the scale atoms of both row groups.
-template <bool SPLIT>
+template <bool SPLIT, bool QA>
 __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap* ta, const CUtensorMap* tb,
                                              const CUtensorMap* tsa, const CUtensorMap* tsb, const Plan& pl,
-                                             int cluster, int rank, bool gated, int n_out,
-                                             volatile int* abort_flag) {
+                                             int cluster, int rank, bool gated, int n_out, const QaArgs& qa,
+                                             int num_m, volatile int* abort_flag) {
   const int kblocks = pl.kblocks;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t filled = 0, fill_parity = 0;
   bool ok = true;
+  // QA: the A row block acquired last. A tile's block is acquired right before the
+  // tile's first load (measured: an acquire read issued a tile ahead, after the
+  // first load, drained the ring; batched relaxed reads with one acquire fence cost
+  // more than this read). Blocks below first_block were encoded before the launch;
+  // a block past M has no rows.
+  int acquired_mb = -1;
+  auto quantized = [&](int mb) { return mb < qa.first_block || mb >= num_m || mb == acquired_mb; };
   auto load_unit = [&](int tile, int kb0, int kb1) {
     int mb, nb;
     pair_tile(pl, tile, rank, &mb, &nb);
+    if constexpr (QA) {
+      if (!quantized(mb)) {
+        if (!acquire_quantized(qa, mb, abort_flag)) {
+          ok = false;
+          return;
+        }
+        acquired_mb = mb;
+      }
+    }
     for (int kb = kb0; kb < kb1; ++kb) {
       if (!wait_bounded(&s.empty[stage], phase ^ 1u, abort_flag, kErrWaitProducer)) {
         ok = false;
@@ -784,14 +933,16 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
 }
 
 // SPLIT: the launch divides its first sk_tiles tiles along K (a separate instance,
-// so the whole-tile kernel carries none of that code).
-template <int EPI, bool DBG, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1)
+// so the whole-tile kernel carries none of that code). QA: the kernel quantizes A
+// itself from BF16 (an extra warp; never with SPLIT).
+template <int EPI, bool DBG, bool SPLIT, bool QA>
+__global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sb,
                    const __grid_constant__ CUtensorMap tmap_out, const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate, const uint16_t* residual,
                    void* out, uint8_t* __restrict__ out_scales, float* __restrict__ dbg, int m_total, int n_total,
-                   int k_total, SplitArgs split) {
+                   int k_total, SplitArgs split, QaArgs qa) {
+  static_assert(!(QA && SPLIT), "the in-kernel quantizer runs without the split tail");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   SharedStorage& s =
@@ -847,12 +998,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0)
-      run_producer<SPLIT>(s, &tmap_a, &tmap_b, &tmap_sa, &tmap_sb, plan, cluster, rank, EPI == kEpiSwiglu, n_total / 2,
-                   abort_flag);
+      run_producer<SPLIT, QA>(s, &tmap_a, &tmap_b, &tmap_sa, &tmap_sb, plan, cluster, rank, EPI == kEpiSwiglu,
+                              n_total / 2, qa, num_m, abort_flag);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) run_mma<SPLIT>(s, tmem, plan, cluster, abort_flag);
   } else if (warp == 2 + kEpiWarps) {
     if (lane == 0 && rank == 0) run_scales<SPLIT>(s, tmem, plan, cluster, abort_flag);
+  } else if (QA && warp == kQaWarp) {
+    run_quantizer(qa, m_total, k_total, lane);
   } else {
     run_epilogue<EPI, DBG, SPLIT>(s, tmem, warp, lane, plan, &tmap_out, cluster, rank, num_m, m_total, n_total, bias,
                                   gate, residual, out, out_scales, dbg, abort_flag);
@@ -970,9 +1123,9 @@ static bool make_codes_out_map(CUtensorMap* map, void* codes, int64_t m, int64_t
 // filled on a device's first call (any thread may fill them). The attribute belongs
 // to the context, so it is set again when the device's context has changed (a new
 // primary context after cudaDeviceReset).
-template <int EPI, bool DBG, bool SPLIT>
+template <int EPI, bool DBG, bool SPLIT, bool QA>
 static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) {
-  auto kern = mx_gemm_kernel<EPI, DBG, SPLIT>;
+  auto kern = mx_gemm_kernel<EPI, DBG, SPLIT, QA>;
   static std::atomic<unsigned long long> configured[64];   // context ID + 1 the attribute was set in; 0: none
   static std::atomic<int> cached[64];
   const bool cacheable = dev >= 0 && dev < 64;
@@ -996,7 +1149,7 @@ static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) 
   return cudaSuccess;
 }
 
-template <int EPI, bool DBG>
+template <int EPI, bool DBG, bool QA>
 static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                                    const CUtensorMap& tsb, const CUtensorMap& tout, const GemmArgs& a,
                                    cudaStream_t stream) {
@@ -1004,7 +1157,7 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair;
   attr[0].val.clusterDim.y = 1;
@@ -1013,35 +1166,56 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   // the stream finishes; it waits (griddepcontrol.wait) before touching memory
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  // QA: producers wait for quantizer warps of other CTAs, so all CTAs are made
+  // co-resident (a cooperative launch; the grid never exceeds the co-resident pairs)
+  attr[2].id = cudaLaunchAttributeCooperative;
+  attr[2].val.cooperative = 1;
+  cfg.blockDim = dim3(QA ? kThreadsQa : kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   int clusters = 0;
-  e = max_clusters<EPI, DBG, false>(dev, cfg, &clusters);
+  e = max_clusters<EPI, DBG, false, QA>(dev, cfg, &clusters);
   if (e != cudaSuccess) return e;
   // as many CTA pairs as are co-resident (one CTA per SM), at most one per tile
-  const GemmPlan plan = plan_gemm(a.m, a.n, a.k, clusters, a.workspace, a.workspace_bytes);
+  const GemmPlan plan = plan_gemm(a.m, a.n, a.k, clusters, QA ? nullptr : a.workspace, QA ? 0 : a.workspace_bytes);
   SplitArgs split = {};
   if (plan.sk_tiles > 0) {
     split.sk_tiles = plan.sk_tiles;
     split.arrivals = static_cast<unsigned*>(a.workspace);
     split.partial = reinterpret_cast<float4*>(static_cast<uint8_t*>(a.workspace) + kArrivalsBytes);
   }
-  cfg.gridDim = dim3(kPair * plan.clusters, 1, 1);
-  if (plan.sk_tiles > 0) {
-    // the split instance has the same resources; its attribute is set on first use
-    int same = 0;
-    e = max_clusters<EPI, DBG, true>(dev, cfg, &same);
-    if (e != cudaSuccess) return e;
-    if (same != clusters) return cudaErrorLaunchOutOfResources;
+  QaArgs qa = {};
+  if constexpr (QA) {
+    qa.x = static_cast<const uint16_t*>(a.x);
+    qa.ld_x = a.ld_x;
+    qa.codes = static_cast<uint8_t*>(const_cast<void*>(a.a_codes));
+    qa.scales = static_cast<uint8_t*>(const_cast<void*>(a.a_scales));
+    qa.ready = a.ready;
+    qa.first_block = static_cast<int>(a.lead_rows / 128);
+    qa.strips = static_cast<int>(qa_strips(a.k));
+    qa.wide = (reinterpret_cast<uintptr_t>(a.x) % 32 == 0 && a.ld_x % 16 == 0) ? 1 : 0;
+    cfg.numAttrs = 3;
   }
-  auto kern = plan.sk_tiles > 0 ? mx_gemm_kernel<EPI, DBG, true> : mx_gemm_kernel<EPI, DBG, false>;
+  cfg.gridDim = dim3(kPair * plan.clusters, 1, 1);
+  if constexpr (!QA) {
+    if (plan.sk_tiles > 0) {
+      // the split instance has the same resources; its attribute is set on first use
+      int same = 0;
+      e = max_clusters<EPI, DBG, true, false>(dev, cfg, &same);
+      if (e != cudaSuccess) return e;
+      if (same != clusters) return cudaErrorLaunchOutOfResources;
+    }
+  }
+  decltype(&mx_gemm_kernel<EPI, DBG, false, QA>) kern = mx_gemm_kernel<EPI, DBG, false, QA>;
+  if constexpr (!QA) {
+    if (plan.sk_tiles > 0) kern = mx_gemm_kernel<EPI, DBG, true, false>;
+  }
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tout, static_cast<const uint16_t*>(a.bias),
                          static_cast<const uint16_t*>(a.gate), static_cast<const uint16_t*>(a.residual), a.out,
                          static_cast<uint8_t*>(a.out_scales), a.debug_prequant, static_cast<int>(a.m),
-                         static_cast<int>(a.n), static_cast<int>(a.k), split);
+                         static_cast<int>(a.n), static_cast<int>(a.k), split, qa);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1060,15 +1234,26 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, boo
   }
   (void)num_sms;
   const bool dbg = a.debug_prequant != nullptr;
+  if (a.x != nullptr) {
+    // the in-kernel quantizer: no debug output, no split tail
+    if (dbg) return cudaErrorInvalidValue;
+    switch (a.epilogue) {
+      case kEpiBf16: return launch_instance<kEpiBf16, false, true>(ta, tb, tsa, tsb, tout, a, stream);
+      case kEpiGelu: return launch_instance<kEpiGelu, false, true>(ta, tb, tsa, tsb, tout, a, stream);
+      case kEpiSwiglu: return launch_instance<kEpiSwiglu, false, true>(ta, tb, tsa, tsb, tout, a, stream);
+      case kEpiGateRes: return launch_instance<kEpiGateRes, false, true>(ta, tb, tsa, tsb, tout, a, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.epilogue) {
-    case kEpiBf16: return launch_instance<kEpiBf16, false>(ta, tb, tsa, tsb, tout, a, stream);
+    case kEpiBf16: return launch_instance<kEpiBf16, false, false>(ta, tb, tsa, tsb, tout, a, stream);
     case kEpiGelu:
-      return dbg ? launch_instance<kEpiGelu, true>(ta, tb, tsa, tsb, tout, a, stream)
-                 : launch_instance<kEpiGelu, false>(ta, tb, tsa, tsb, tout, a, stream);
+      return dbg ? launch_instance<kEpiGelu, true, false>(ta, tb, tsa, tsb, tout, a, stream)
+                 : launch_instance<kEpiGelu, false, false>(ta, tb, tsa, tsb, tout, a, stream);
     case kEpiSwiglu:
-      return dbg ? launch_instance<kEpiSwiglu, true>(ta, tb, tsa, tsb, tout, a, stream)
-                 : launch_instance<kEpiSwiglu, false>(ta, tb, tsa, tsb, tout, a, stream);
-    case kEpiGateRes: return launch_instance<kEpiGateRes, false>(ta, tb, tsa, tsb, tout, a, stream);
+      return dbg ? launch_instance<kEpiSwiglu, true, false>(ta, tb, tsa, tsb, tout, a, stream)
+                 : launch_instance<kEpiSwiglu, false, false>(ta, tb, tsa, tsb, tout, a, stream);
+    case kEpiGateRes: return launch_instance<kEpiGateRes, false, false>(ta, tb, tsa, tsb, tout, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1087,7 +1272,7 @@ cudaError_t gemm_max_clusters(int* clusters) {
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return max_clusters<kEpiBf16, false, false>(dev, cfg, clusters);
+  return max_clusters<kEpiBf16, false, false, false>(dev, cfg, clusters);
 }
 
 // A wait that nothing will ever satisfy: it must give up after the bound, set

@@ -16,6 +16,7 @@ enum : unsigned {
   kErrWaitEpilogue = 1u << 2,   // epilogue gave up waiting for the accumulator
   kErrDrain = 1u << 3,          // copies or MMAs still in flight after an abort
   kErrSelfTest = 1u << 4,       // the deliberate timeout of mx_selftest_wait_timeout
+  kErrWaitQuant = 1u << 5,      // TMA producer gave up waiting for in-kernel quantized A rows
 };
 
 // zero_words / zero_count: a buffer the kernel also sets to zero (after the previous
@@ -101,6 +102,35 @@ inline GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int max_clusters, con
   return p;
 }
 
+// ---------------------------------------------------------- in-kernel quantizer
+// With BF16 activations, the GEMM can quantize A itself (gemm.cu): a quantize
+// kernel first encodes the rows the first two rounds of tiles read (and zeroes the
+// row-block counters), then one extra warp per CTA of the GEMM encodes the rest,
+// in row order, while the main loop runs, publishing each 128-row block on a
+// counter that the TMA producers wait for before loading that block. The leading
+// rows: those of the row tiles of tiles [0, 2 pairs). The quantizer warps (one per
+// SM) encode about 0.19 G elements per ms in all (measured on GB300), enough to stay
+// ahead of a GEMM that reads its A rows no faster than a 12288-wide one does; a
+// narrower GEMM (the attention output projection, N = 3072, measured) gains
+// nothing from encoding part of its rows in-kernel, so below kQaMinN all rows are
+// encoded up front and the GEMM runs without its quantizer warp.
+constexpr int kQaStrip = 1024;     // columns of one in-kernel quantize item (one per lane: 32 blocks)
+constexpr int kQaGroup = 4;        // items a quantize warp loads at once (divides 128 rows x strips)
+constexpr int64_t kQaMinN = 12288;
+
+inline int64_t qa_strips(int64_t k) { return (k + kQaStrip - 1) / kQaStrip; }
+
+inline int64_t qa_lead_rows(int64_t m, int64_t n, int clusters) {
+  if (n < kQaMinN) return m;
+  const int64_t tiles = gemm_pair_tiles(m, n), num_n = n / kPairTileCols;
+  const int64_t lead = 2 * static_cast<int64_t>(clusters) < tiles ? 2 * static_cast<int64_t>(clusters) : tiles;
+  const int64_t rows = lead > 0 ? ((lead - 1) / num_n + 1) * kPairTileRows : 0;
+  return rows < m ? rows : m;
+}
+
+// Counter words of the in-kernel quantizer: one per 128-row block.
+inline int64_t qa_counter_words(int64_t m) { return (m + 127) / 128; }
+
 struct GemmArgs {
   const void* a_codes;
   const void* a_scales;
@@ -117,6 +147,13 @@ struct GemmArgs {
                            // (F = N/2 outputs), 3: residual + gate * (C + bias), BF16
   void* workspace;         // split-tail workspace (256-byte aligned, counters zero) or null
   size_t workspace_bytes;
+  // in-kernel quantizer (x null: A is already quantized): A = MXFP6(x) is written to
+  // a_codes / a_scales; rows below qa_lead_rows are already there, and `ready`
+  // (qa_counter_words words) is zero at the launch. No split tail with it.
+  const void* x;           // bf16 [M][K], row stride ld_x elements
+  int64_t ld_x;
+  int64_t lead_rows;       // a multiple of 256 below M
+  unsigned* ready;
 };
 
 // Returns cudaSuccess or the first CUDA error; `encode_failed` is set when the

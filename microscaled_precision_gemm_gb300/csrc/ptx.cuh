@@ -93,6 +93,46 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------------------------ flags in global memory
+// A counter that warps of other CTAs increase once their global writes are done
+// (release), read by a thread that then reads those writes (acquire).
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's global-memory accesses of the generic proxy with its
+// accesses of the async proxy (TMA): on the writing side before the release, on
+// the reading side after the acquire and before the tensor loads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// 16 bytes through the read-only (non-coherent) path: only for data no kernel
+// writes while this one runs.
+__device__ __forceinline__ uint4 ld_nc(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 32 bytes through the read-only path (sm_100 and later); p must be 32-byte aligned.
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+               : "l"(p));
+}
+
+__device__ __forceinline__ void sleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
+
 // ------------------------------------------------------------------ TMA tensor loads
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

@@ -23,14 +23,6 @@ namespace mxk {
 
 constexpr int kQuantThreads = 256;
 
-__device__ __forceinline__ uint4 ld_nc(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Quotient of n by an invariant divisor d with a precomputed magic number
 // (division by invariant integers using multiplication, round-up variant):
 // m = floor(2^32 (2^l - d) / d) + 1 with l = ceil(log2 d); q = (mulhi(n, m) + n) >> l.

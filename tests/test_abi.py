@@ -60,7 +60,8 @@ def test_size_queries(lib):
     assert lib.mx_scales_bytes(0, 256) == 0
     assert lib.mx_codes_bytes(-1, 256) == 0
     ws = lib.mx_mlp_workspace_bytes(20480, 3072, 12288)
-    need = 20480 * 3072 * 3 // 4 + 20480 * 96 + 20480 * 12288 * 3 // 4 + 20480 * 384
+    # MXFP6 x and h, then one counter word per 128 rows (160 words, 640 -> 768 bytes)
+    need = 20480 * 3072 * 3 // 4 + 20480 * 96 + 20480 * 12288 * 3 // 4 + 20480 * 384 + 768
     assert _mlp_base(lib, 20480, 3072, 12288) == need
     # plus the split-tail region the larger of the two GEMMs needs (here the
     # down-projection; the up-projection's 24 K-steps never split)
@@ -70,9 +71,11 @@ def test_size_queries(lib):
 
 
 def _mlp_base(lib, M, d, ff):
-    """Smallest MLP workspace: MXFP6 x and h, each part 256-byte aligned."""
+    """Smallest MLP workspace: MXFP6 x and h and the row-block counters (a 32-bit
+    word per 128 rows), each part 256-byte aligned."""
     return sum(-(-n // 256) * 256 for n in (lib.mx_codes_bytes(M, d), lib.mx_scales_bytes(M, d),
-                                            lib.mx_codes_bytes(M, ff), lib.mx_scales_bytes(M, ff)))
+                                            lib.mx_codes_bytes(M, ff), lib.mx_scales_bytes(M, ff),
+                                            4 * (-(-M // 128))))
 
 
 def _q(lib, x=A32, rows=128, k=256, ld=256, codes=A32b, scales=A32c):
@@ -160,6 +163,45 @@ def test_gate_residual_rejects_bad_arguments(lib):
     assert _gr(lib, res=0x200000 + 8) == MISALIGNED
     assert _gr(lib, out=0x200000 + 1024) == INVALID    # partial overlap with the residual
     assert _gr(lib, M=0, res=None, out=None) == OK
+
+
+def test_quantize_gemm_rejects_bad_arguments(lib):
+    """mx_quantize_gemm: the quantizer's and the GEMM's rules on the workspace's
+    parts, the workspace size, the gate/residual rules, and no overlap of x with
+    the output or the workspace -- all on the host, before the device is touched."""
+    X, OUT, WS = 0x1000000, 0x2000000, 0x4000000
+    need = lib.mx_quantize_gemm_workspace_bytes(128, 256)
+    # codes, scales (both 256-aligned), then a counter word per 128 rows
+    assert need == 128 * 192 + 128 * 8 + 256
+
+    def call(x=X, M=128, K=256, ld=256, b=A32b, bs=A32c, bias=None, N=512, epi=BF16, gate=None, res=None,
+             out=OUT, out_sc=None, ws=WS, wsb=need):
+        return lib.mx_quantize_gemm(x, M, K, ld, b, bs, bias, N, epi, gate, res, out, out_sc, ws, wsb, None)
+
+    assert call(epi=4) == INVALID
+    assert call(epi=-1) == INVALID
+    assert call(M=-1) == INVALID
+    assert call(ld=128) == INVALID                   # ld_x < K
+    assert call(K=96, ld=96) == SHAPE
+    assert call(N=384) == SHAPE
+    assert call(ld=260) == MISALIGNED                # row stride % 8
+    assert call(x=None) == INVALID
+    assert call(x=X + 2) == MISALIGNED
+    assert call(b=None) == INVALID
+    assert call(out=None) == INVALID
+    assert call(epi=GELU) == INVALID                 # MXFP6 output needs its scales
+    assert call(ws=None) == INVALID
+    assert call(ws=WS + 64) == MISALIGNED
+    assert call(wsb=need - 1) == WS_SMALL
+    assert call(epi=3) == INVALID                    # the gate/residual epilogue needs a residual
+    assert call(epi=3, res=OUT + 8) == MISALIGNED
+    assert call(epi=3, res=OUT + 1024) == INVALID    # partial overlap with the output
+    assert call(out=X + 4096) == INVALID             # x overlaps the output
+    assert call(ws=X - 256) == INVALID               # x overlaps the workspace
+    assert call(M=0, x=None, b=None, out=None, ws=None) == OK
+    assert call(N=0, x=None, b=None, out=None, ws=None) == OK
+    for ok in (call(), call(epi=3, res=OUT), call(epi=GELU, out_sc=0x3000000)):
+        assert ok not in (OK, WS_SMALL, INVALID, SHAPE, MISALIGNED)   # valid: stops at the device
 
 
 def test_gated_mlp_rejects_bad_arguments(lib):

@@ -15,17 +15,24 @@ if ROOT not in sys.path:
 import bench  # noqa: E402
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("name", sorted(bench.CONFIGS))
-def test_bf16_context_shapes_carry_the_step_flops(name):
-    """The BF16 context times the same contractions the step's MXFP6 GEMM stages do."""
+def test_bf16_context_shapes_carry_the_step_flops(name, fused):
+    """The BF16 context times the same contractions the step's MXFP6 GEMM stages do,
+    with the quantizer in its own stage or inside the GEMM's; a fused stage carries
+    the quantizer's bytes, so the step's algorithmic bytes do not change."""
     cfg = bench.CONFIGS[name]
     M = cfg["M"]
     shapes = bench.gemm_shapes(cfg, M)
-    work = bench.stage_work(cfg, M)
+    work = bench.stage_work(cfg, M, fused=fused)
     gemm_flops = sum(w["flops"] for w in work.values())
     assert shapes, name
     assert sum(2.0 * m * n * k for m, n, k in shapes) == pytest.approx(gemm_flops, rel=1e-12)
     assert all(m == M for m, _, _ in shapes)
+    plain = bench.stage_work(cfg, M)
+    assert sum(w["bytes"] for w in work.values()) == pytest.approx(sum(w["bytes"] for w in plain.values()))
+    if fused and bench.S_K1 in plain:
+        assert bench.S_K1 not in work and any(n in bench.FUSED_STAGES for n in work)
 
 
 class _FakeSmi:

@@ -31,7 +31,10 @@ def test_bench_line_contract(lib):
         assert key in d, key
     assert d["n_gpus"] == 1 and d["steps"] == 4 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
-    assert d["gpu_launches"] == 4 * len(d["stages"])
+    # pr1's step is one stage, the quantizer fused into the GEMM: two launches
+    assert list(d["stages"]) == ["K1 lead rows + GEMM (in-kernel quantizer)+bias+BF16"]
+    assert d["gpu_launches"] == 4 * 2 and d["config"]["quantizer_in_gemm"] is True
+    assert d["quantize_isolated"]["gbs"] > 0 and d["quantize_gbs"] == d["quantize_isolated"]["gbs"]
     assert d["config"]["workload"].startswith("single MXFP6 GEMM")
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] == 128 * 256 * 2 and e2e["d2h_bytes_per_step"] == 128 * 512 * 2
@@ -40,8 +43,16 @@ def test_bench_line_contract(lib):
     assert set(d["roofline"]) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
     assert d["sustained"]["steps"] >= 1 and d["sustained"]["ms_per_step"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
-    iso = d["gemms_isolated"]["K2 GEMM+bias+BF16"]
+    iso = d["gemms_isolated"]["K1 lead rows + GEMM (in-kernel quantizer)+bias+BF16"]
     assert iso["us"] > 0 and iso["launches"] == 20
+
+
+def test_bench_unfused_stages(lib):
+    """--unfused: the quantizer in its own stage before the GEMM."""
+    d = _run("--config", "pr1", "--steps", "4", "--warmup", "3", "--sustain-s", "0", "--no-cpu-baseline",
+             "--unfused")
+    assert list(d["stages"]) == ["K1 quantize", "K2 GEMM+bias+BF16"]
+    assert d["gpu_launches"] == 4 * 2 and d["config"]["quantizer_in_gemm"] is False
 
 
 def test_reference_arm_line(lib):

@@ -208,7 +208,8 @@ def test_mlp_split_tail(lib):
     b2 = bf16_to_device(synth.bf16_round(rng.standard_normal(d).astype(np.float32) * 0.01))
     full = lib.mx_mlp_workspace_bytes(M, d, ff)
     base = sum(-(-n // 256) * 256 for n in (lib.mx_codes_bytes(M, d), lib.mx_scales_bytes(M, d),
-                                            lib.mx_codes_bytes(M, ff), lib.mx_scales_bytes(M, ff)))
+                                            lib.mx_codes_bytes(M, ff), lib.mx_scales_bytes(M, ff),
+                                            4 * (-(-M // 128))))   # + a counter word per 128 rows
     assert full > base
     y = lib.mx_mlp(x, w1, b1, w2, b2)
     ws = torch.full((full,), 0xFF, dtype=torch.uint8, device="cuda")
