@@ -91,7 +91,7 @@ S_GEMM = "K2 GEMM+bias+BF16"
 S_QKV = "QKV+gate GEMM+bias+BF16"
 S_OUT = "out-proj GEMM+bias+gate+residual"
 # the quantizer fused into the GEMM (mx_quantize_gemm: the quantize kernel encodes the
-# rows of the first two rounds of tiles, the GEMM the rest while it runs): two launches
+# rows of the first round of tiles, the GEMM the rest while it runs): two launches
 S_QUP = "K1 lead rows + K3 up GEMM (in-kernel quantizer)+GELU+requant"
 S_QGU = "K1 lead rows + K3 gate/up GEMM (in-kernel quantizer)+SwiGLU+requant"
 S_QGEMM = "K1 lead rows + GEMM (in-kernel quantizer)+bias+BF16"
@@ -755,7 +755,7 @@ def run_gpu(args) -> dict | None:
         line["quantize_gbs"] = k1_isolated["gbs"]
         line["quantize_frac_hbm"] = k1_isolated["gbs"] / peaks["hbm_gbs"]
         line["quantize_note"] = ("the timed step quantizes the activations inside the GEMM (the quantize kernel "
-                                 "encodes only the rows of the first two rounds of tiles); quantize_gbs is the "
+                                 "encodes only the rows of the first round of tiles); quantize_gbs is the "
                                  "standalone quantizer over all rows, launched alone")
     if k1_isolated is not None:
         k1_isolated["frac_hbm"] = k1_isolated["gbs"] / peaks["hbm_gbs"]

@@ -251,8 +251,8 @@ mx_status mx_gemm_launch_plan(int64_t M, int64_t N, int64_t K, size_t workspace_
  * The quantize kernel encodes the leading rows (and zeroes the workspace's
  * counters); the GEMM quantizes the remaining rows itself, in an extra warp per
  * CTA, while its main loop runs, so the encoding of most of x overlaps the
- * tensor-core work. The leading rows are those the GEMM's first two rounds of
- * tiles read; for N < 12288 (where the extra warps would fall behind the GEMM's
+ * tensor-core work. The leading rows are those the GEMM's first round of tiles
+ * reads; for N < 12288 (where the extra warps would fall behind the GEMM's
  * reads) they are all M rows, and the GEMM runs as mx_gemm. Two launches on `stream`.
  *   x        : device BF16 [M][K] row-major, row stride ld_x elements (ld_x % 8 == 0),
  *              16-byte aligned; must not overlap out or the workspace
@@ -288,7 +288,7 @@ size_t mx_mlp_workspace_bytes(int64_t M, int64_t d, int64_t ff);
  * mx_mlp -- the whole MXFP6 MLP block in three launches on `stream`:
  *   K1 xq = MXFP6(x); K3 hq = MXFP6(gelu_tanh(xq W1^T + b1)); K2 y = bf16(hq W2^T + b2).
  *   As in mx_quantize_gemm, K1 encodes only the leading rows of x (those K3's
- *   first two rounds of tiles read), and K3 encodes the rest itself while it runs
+ *   first round of tiles reads), and K3 encodes the rest itself while it runs
  *   (when its width, ff or 2 ff, is at least 12288, it does not split its tail, and
  *   the leading rows are not all of x); the result is the same bit for bit.
  *   x        : BF16 [M][d] (16-byte aligned); y: BF16 [M][d] (written)

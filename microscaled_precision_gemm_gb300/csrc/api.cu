@@ -224,8 +224,8 @@ mx_status mlp_impl(const void* x, int64_t M, int64_t d, int64_t ff, int up_epi, 
   if (st != MX_OK) return st;
   int sms = 0;
   if ((st = device_check(&sms)) != MX_OK) return st;
-  // the up-projection quantizes x itself beyond the rows its first two rounds of
-  // tiles read, which the quantize kernel encodes first (unless the up-projection
+  // the up-projection quantizes x itself beyond the rows its first round of
+  // tiles reads, which the quantize kernel encodes first (unless the up-projection
   // splits its tail, or those rows are all of x)
   QaLaunch qa;
   int clusters = 0;
@@ -522,7 +522,7 @@ mx_status mx_quantize_gemm(const void* x, int64_t M, int64_t K, int64_t ld_x, co
   if ((st = device_check(&sms)) != MX_OK) return st;
   int clusters = 0;
   if (mxk::gemm_max_clusters(&clusters) != cudaSuccess) return MX_ERR_CUDA;
-  // the quantize kernel encodes the rows the first two rounds of tiles read and
+  // the quantize kernel encodes the rows the first round of tiles reads and
   // zeroes the counters; the GEMM encodes the rest itself
   QaLaunch qa;
   const int64_t lead = mxk::qa_lead_rows(M, N, clusters);

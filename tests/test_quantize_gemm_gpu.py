@@ -1,10 +1,10 @@
 """The GEMM that quantizes its own BF16 activations (mx_quantize_gemm, and the
 up-projection inside mx_mlp / mx_gated_mlp).
 
-The quantize kernel encodes the leading rows -- those the GEMM's first two rounds
-of tiles read; all rows when N < 12288 -- and the GEMM's quantizer warps the rest
+The quantize kernel encodes the leading rows -- those the GEMM's first round of
+tiles reads; all rows when N < 12288 -- and the GEMM's quantizer warps the rest
 while its main loop runs. With N = 12288 or 16384 (48 or 64 column tiles) the
-first two rounds of 76 pairs read the first 1024 or 768 rows, so on the shapes
+first round of 76 pairs reads the first 512 rows, so on the shapes
 below most rows are encoded inside the GEMM (in several 128-row blocks, the last
 one ragged, with 1, 2 or 3 column strips of 1024, the last one partial); at
 N = 3072 none.
@@ -61,8 +61,8 @@ def _check_xq(lib, ws, x, x_bits, rows):
 
 
 def _rows(M):
-    # the lead rows' last, the first encoded in-kernel, a block boundary, the last
-    return np.unique(np.array([0, 767, 768, 1023, 1024, 1151, 1152, M // 2, M - 2, M - 1]).clip(0, M - 1))
+    # the lead rows' last, the first encoded in-kernel, block boundaries, the last
+    return np.unique(np.array([0, 511, 512, 639, 640, 1023, 1024, M // 2, M - 2, M - 1]).clip(0, M - 1))
 
 
 # ld_pad 8: a row stride of 8 mod 16 elements, so the quantizer warp takes its
@@ -145,7 +145,7 @@ def test_gate_residual_epilogue(lib, gated, in_place, N):
 
 
 def test_rows_all_in_the_lead(lib):
-    """N = 512: the first two rounds read every row, so the quantize kernel encodes
+    """N = 512: the first round reads every row, so the quantize kernel encodes
     all of x and the GEMM runs without its quantizer warp."""
     import torch
 
@@ -171,7 +171,7 @@ def test_empty(lib):
 @pytest.mark.parametrize("gated", [False, True])
 def test_mlp_up_projection_quantizes_in_kernel(lib, gated):
     """mx_mlp / mx_gated_mlp at M = 2048, ff = 12288: the up-projection encodes rows
-    1024.. of x itself. The workspace's MXFP6 x equals mx_quantize(x), and the
+    512.. of x itself. The workspace's MXFP6 x equals mx_quantize(x), and the
     result equals the three stages run one by one."""
     import torch
 
