@@ -371,6 +371,26 @@ class Workload:
                                    device=dev)
         torch.cuda.synchronize()
 
+    def gemm_alone(self, mx):
+        """{fused stage name: callable}: the stage's GEMM on activations already in MXFP6
+        (xq, filled here once by the quantize kernel), without the quantizer."""
+        kind = self.cfg["kind"]
+        if not self.fused or kind not in ("mlp", "gated_mlp", "up", "gemm", "qkv", "attn_out"):
+            return {}
+        src = self.a if kind == "attn_out" else self.x
+        mx.mx_quantize(src, out=self.xq)
+        swiglu = kind == "gated_mlp"
+        if kind in ("mlp", "gated_mlp", "up"):
+            epi = mx.MX_EPI_BIAS_SWIGLU_MXFP6 if swiglu else mx.MX_EPI_BIAS_GELU_MXFP6
+            return {S_QGU if swiglu else S_QUP: lambda: mx.mx_gemm(self.xq, self.w1, self.b1, epi, out=self.hq,
+                                                                    workspace=self.ws)}
+        if kind in ("gemm", "qkv"):
+            return {S_QQKV if kind == "qkv" else S_QGEMM: lambda: mx.mx_gemm(self.xq, self.w1, self.b1,
+                                                                          mx.MX_EPI_BIAS_BF16, out=self.y,
+                                                                          workspace=self.ws)}
+        return {S_QOUT: lambda: mx.mx_gemm_gate_residual(self.xq, self.w2, self.b2, self.gate, self.x, out=self.y,
+                                                         workspace=self.ws)}
+
     def quantizer(self, mx):
         """(name, callable) of the step's whole quantizer, launched on its own."""
         kind = self.cfg["kind"]
@@ -643,6 +663,22 @@ def run_gpu(args) -> dict | None:
         tf = work[name]["flops"] / (g_ms * 1e-3) / 1e12
         gemms_isolated[name] = {"us": g_ms * 1e3, "tflops": tf, "frac_fp6_peak_spec": tf / FP6_SPEC_PEAK_TFLOPS,
                                 "launches": n_iso}
+        # a fused stage's GEMM alone, on activations already quantized (the GEMM's own rate)
+        alone = [c.gemm_alone(mx).get(name) for c in copies]
+        if alone[0] is not None:
+            for i in range(3):
+                alone[i % len(alone)]()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for i in range(n_iso):
+                alone[i % len(alone)]()
+            b.record(stream)
+            torch.cuda.synchronize()
+            g_ms = a.elapsed_time(b) / n_iso
+            tf = work[name]["flops"] / (g_ms * 1e-3) / 1e12
+            gemms_isolated[name]["gemm_alone"] = {"us": g_ms * 1e3, "tflops": tf,
+                                                  "frac_fp6_peak_spec": tf / FP6_SPEC_PEAK_TFLOPS,
+                                                  "note": "the same GEMM on activations already in MXFP6"}
 
     # sustained leg: the same rotation of steps, back to back for a few seconds after
     # the timed region (and after the quantizer's isolated timing, which would
@@ -763,6 +799,8 @@ def run_gpu(args) -> dict | None:
     if gemms_isolated:
         for rep in gemms_isolated.values():
             rep["frac_fp6_peak_measured"] = rep["tflops"] / fp6_peak
+            if "gemm_alone" in rep:
+                rep["gemm_alone"]["frac_fp6_peak_measured"] = rep["gemm_alone"]["tflops"] / fp6_peak
         line["gemms_isolated"] = gemms_isolated
         line["gemms_isolated_note"] = ("each GEMM stage launched alone 20 times back to back over the input copies, "
                                        "outside the timed region")

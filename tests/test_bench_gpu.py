@@ -44,7 +44,7 @@ def test_bench_line_contract(lib):
     assert d["sustained"]["steps"] >= 1 and d["sustained"]["ms_per_step"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     iso = d["gemms_isolated"]["K1 lead rows + GEMM (in-kernel quantizer)+bias+BF16"]
-    assert iso["us"] > 0 and iso["launches"] == 20
+    assert iso["us"] > 0 and iso["launches"] == 20 and iso["gemm_alone"]["us"] > 0
 
 
 def test_bench_unfused_stages(lib):
