@@ -130,6 +130,38 @@ def test_norm_quantize_beyond_32bit_offsets(lib):
     _free()
 
 
+def test_quantize_gemm_beyond_32bit_offsets(lib):
+    """The GEMM that quantizes its own activations, on the quantizers' 6.0 GB input
+    (x offsets past 2^31 elements and 2^32 bytes; its MXFP6 codes, written into the
+    workspace, past 2^31 bytes), N = 12288, so every row past the first 512 is
+    encoded by the GEMM's quantizer warps; the BF16 output holds 32 GB (store
+    offsets past 2^34 bytes). The in-kernel codes and scales are bit-exact against
+    the oracle on the boundary rows, padding-row scales zero, and the output within
+    the GEMM tolerance."""
+    import torch
+
+    rng = np.random.default_rng(14)
+    w_bits = synth.bf16_round(rng.standard_normal((GN, QK)).astype(np.float32) * 0.02)
+    bias = synth.bf16_round((rng.standard_normal(GN) * 0.01).astype(np.float32))
+    wq = lib.mx_quantize(bf16_to_device(w_bits))
+    x = _hash_input(seed=14)
+    ws = torch.empty(lib.mx_quantize_gemm_workspace_bytes(QR, QK), dtype=torch.uint8, device="cuda")
+    y = lib.mx_quantize_gemm(x, wq, bf16_to_device(bias), lib.MX_EPI_BIAS_BF16, workspace=ws)
+    del x
+    xq = lib.mx_quantize_gemm_xq(ws, QR, QK)
+    rows = _rows(QR, [_crossing_row(1 << 31, QK), _crossing_row(1 << 32, 2 * QK),
+                      _crossing_row(1 << 31, QK * 3 // 4), _crossing_row(1 << 34, 2 * GN)], seed=4)
+    rq, rs = O.quantize_bf16(synth.hash_bf16_rows(rows, QK, seed=14))
+    assert_codes_equal(_codes_rows(xq, rows), rq, _scale_rows(xq, rows), rs, "in-kernel MXFP6(x)")
+    _padding_scales_zero(xq)
+    got = f32_from_bf16_bits(bf16_from_device(y.index_select(0, torch.as_tensor(rows, device="cuda"))))
+    del y, xq, ws
+    r_wq, r_ws = O.quantize_bf16(w_bits)
+    assert_gemm_close(got.astype(np.float64), O.gemm(rq, rs, r_wq, r_ws, bias), "fused quantize + GEMM")
+    assert lib.mx_device_error() == 0
+    _free()
+
+
 def _gemm_operands(seed: int):
     rng = np.random.default_rng(seed)
     a = rng.integers(0, 64, size=(GM, GK), dtype=np.uint8)
