@@ -233,10 +233,15 @@ size_t mx_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * mx_gemm_launch_plan -- what a GEMM of this shape does on the current device:
- *   pairs       (host, written): CTA pairs launched (co-resident pairs, at most one per tile)
+ *   pairs       (host, written): CTA pairs of the whole-tile plan (co-resident pairs,
+ *                                at most one per tile)
  *   split_tiles (host, written): leading tiles divided along K when called with a
  *                                workspace of workspace_bytes bytes (0: no split)
- * Shape rules as mx_gemm; M == 0 or N == 0 gives 0 and 0.
+ * Shape rules as mx_gemm; M == 0 or N == 0 gives 0 and 0. Without a split, a GEMM
+ * with an epilogue other than MX_EPI_BIAS_SWIGLU_MXFP6 and no debug output also
+ * runs its last round's tiles as two 128-column halves each when they fit in one
+ * round (tiles mod pairs <= pairs / 2), and all its tiles as halves, on twice as
+ * many pairs, when it has at most pairs / 2 tiles; the result is the same.
  */
 mx_status mx_gemm_launch_plan(int64_t M, int64_t N, int64_t K, size_t workspace_bytes, int* pairs,
                               int* split_tiles);

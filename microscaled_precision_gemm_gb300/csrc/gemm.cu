@@ -157,10 +157,13 @@ __device__ __forceinline__ uint64_t desc_scale_atom(uint32_t saddr) {
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: A, B = E2M3, K-major,
 // fp32 accumulate, E8M0 scales, M = 256 (the pair), N = 256; j selects the scale byte
 // (K-block) inside each 32-bit tensor-memory scale column, for A and B alike.
-__host__ __device__ constexpr uint32_t idesc_mx(uint32_t j) {
-  return (j << 4) | (3u << 7) | (3u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t j, uint32_t n = BN) {
+  return (j << 4) | (3u << 7) | (3u << 10) | ((n >> 3) << 17) | (1u << 23) |
          (static_cast<uint32_t>((kPair * BM) >> 4) << 24) | (j << 29);
 }
+constexpr int kHalfCols = BN / 2;   // a half tile's output columns
+// A half tile's stage: all of this CTA's A rows, half of its B rows.
+constexpr uint32_t kStageTxHalf = (kABytes + kBBytes / 2) / 4 * 3 + kSfaBytes + kSfbBytes;
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              unsigned err_bit) {
@@ -225,6 +228,8 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
 // commutative, so the result does not depend on which one that is.
 struct Plan {
   int tiles, num_n, kblocks, clusters, sk_tiles;
+  int whole;        // tiles run whole (tiles - half_tiles)
+  int half_tiles;   // trailing tiles run as two halves: half unit c < 2 half_tiles of cluster c
   float4* partial;     // split tiles: 2 slots per cluster, each 2 CTAs x 128 rows x 256 fp32
   unsigned* arrivals;  // split tiles: arrivals per (tile, CTA rank, epilogue warp); zero before the launch
 };
@@ -404,11 +409,13 @@ __device__ __forceinline__ void pair_tile(const Plan& pl, int tile, int rank, in
 // gated: B is the stacked [gate; up] weight of 2 * n_out rows; CTA 0 of the pair
 // stages gate rows [128 nb, 128 nb + 128) and CTA 1 the up rows n_out rows further,
 // and both SMs' tensor memory gets the scale atoms of both row groups.
-template <bool SPLIT, bool QA>
+// HALF: half units (the cluster's after its whole tiles) load half of this CTA's B
+// rows through tbh (64-row boxes) and the one scale atom of the half's 128 rows.
+template <bool SPLIT, bool QA, bool HALF>
 __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap* ta, const CUtensorMap* tb,
-                                             const CUtensorMap* tsa, const CUtensorMap* tsb, const Plan& pl,
-                                             int cluster, int rank, bool gated, int n_out, const QaArgs& qa,
-                                             int num_m, volatile int* abort_flag) {
+                                             const CUtensorMap* tbh, const CUtensorMap* tsa, const CUtensorMap* tsb,
+                                             const Plan& pl, int cluster, int rank, bool gated, int n_out,
+                                             const QaArgs& qa, int num_m, volatile int* abort_flag) {
   const int kblocks = pl.kblocks;
   int stage = 0;
   uint32_t phase = 0;
@@ -421,7 +428,8 @@ __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap
   // a block past M has no rows.
   int acquired_mb = -1;
   auto quantized = [&](int mb) { return mb < qa.first_block || mb >= num_m || mb == acquired_mb; };
-  auto load_unit = [&](int tile, int kb0, int kb1) {
+  auto load_unit = [&](int tile, int kb0, int kb1, int half) {
+    const bool is_half = HALF && half >= 0;
     int mb, nb;
     pair_tile(pl, tile, rank, &mb, &nb);
     if constexpr (QA) {
@@ -441,8 +449,15 @@ __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap
       // both CTAs' stage bytes complete on the leader's full barrier, which
       // expects them all; a row tile past M reads zeros (A and its scales)
       const uint32_t full_leader = mapa_shared(smem_u32(&s.full[stage]), 0);
-      if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], kPair * kStageTx);
+      if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], kPair * (is_half ? kStageTxHalf : kStageTx));
       tma_load_2d_pair(s.a[stage], ta, full_leader, kb * BK, mb * BM);
+      if (is_half) {
+        // CTA r: rows [64 r, 64 r + 64) of the half's 128 B rows; the second atom of
+        // the two-atom scale box is the next half's (zeros past N), unused
+        tma_load_2d_pair(s.b[stage], tbh, full_leader, kb * BK, nb * BN + half * kHalfCols + rank * (kHalfCols / 2));
+        tma_load_2d_pair(s.sfa[stage], tsa, full_leader, 0, mb * kblocks + kb);
+        tma_load_3d_pair(s.sfb[stage], tsb, full_leader, 0, kb, 2 * nb + half);
+      } else {
       const int b_row = gated ? rank * n_out + nb * kBHalfRows : nb * BN + rank * kBHalfRows;
       tma_load_2d_pair(s.b[stage], tb, full_leader, kb * BK, b_row);
       tma_load_2d_pair(s.sfa[stage], tsa, full_leader, 0, mb * kblocks + kb);
@@ -451,6 +466,7 @@ __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap
         tma_load_3d_pair(s.sfb[stage] + kAtomBytes, tsb, full_leader, 0, kb, n_out / kBHalfRows + nb);
       } else {
         tma_load_3d_pair(s.sfb[stage], tsb, full_leader, 0, kb, 2 * nb);
+      }
       }
       filled |= 1u << stage;
       fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
@@ -463,9 +479,13 @@ __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap
   if constexpr (SPLIT) {
     Cursor cur = cursor_begin(pl, cluster);
     Unit u;
-    while (ok && cursor_next(pl, cur, u)) load_unit(u.tile, u.kb0, u.kb1);
+    while (ok && cursor_next(pl, cur, u)) load_unit(u.tile, u.kb0, u.kb1, -1);
   }
-  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; ok && p < pl.tiles; p += pl.clusters) load_unit(p, 0, kblocks);
+  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; ok && p < (HALF ? pl.whole : pl.tiles); p += pl.clusters)
+    load_unit(p, 0, kblocks, -1);
+  if constexpr (HALF) {
+    if (ok && cluster < 2 * pl.half_tiles) load_unit(pl.whole + cluster / 2, 0, kblocks, cluster % 2);
+  }
   if (ok) {
     // every stage this CTA filled has been consumed by the pair's MMAs, so no
     // completion arrival from the leader is still heading here
@@ -477,13 +497,16 @@ __device__ __forceinline__ void run_producer(SharedStorage& s, const CUtensorMap
   }
 }
 
-template <bool SPLIT>
+// HALF: a half unit's MMAs are N = 128 (accumulator columns 0-127; the B scales
+// of its 128 rows are the first atom of the stage's scale slot).
+template <bool SPLIT, bool HALF>
 __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const Plan& pl, int cluster,
                                         volatile int* abort_flag) {
   int stage = 0;
   uint32_t phase = 0, acc_phase = 0;
   bool ok = true, issued = false;
-  auto mma_unit = [&](int kb0, int kb1) {
+  auto mma_unit = [&](int kb0, int kb1, bool half) {
+    const uint32_t n = HALF && half ? static_cast<uint32_t>(kHalfCols) : static_cast<uint32_t>(BN);
     // both CTAs' epilogues have drained the previous tile's accumulators
     if (!wait_bounded_cluster(&s.tmem_empty, acc_phase ^ 1u, abort_flag, kErrWaitMma)) {
       ok = false;
@@ -509,7 +532,7 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const P
 #pragma unroll
         for (uint32_t j = 0; j < 4; ++j) {
           // K step j: 32 elements = 32 bytes further along the swizzled 128-byte row
-          tc_mma_mx_pair(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j), sf_a, sf_b, (kb != kb0) || j != 0);
+          tc_mma_mx_pair(tmem, ad + 2u * j, bd + 2u * j, idesc_mx(j, n), sf_a, sf_b, (kb != kb0) || j != 0);
         }
         tc_commit_pair(&s.empty[stage], kPairMask);  // frees the stage in both CTAs
         issued = true;
@@ -526,9 +549,13 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const P
   if constexpr (SPLIT) {
     Cursor cur = cursor_begin(pl, cluster);
     Unit u;
-    while (ok && cursor_next(pl, cur, u)) mma_unit(u.kb0, u.kb1);
+    while (ok && cursor_next(pl, cur, u)) mma_unit(u.kb0, u.kb1, false);
   }
-  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; ok && p < pl.tiles; p += pl.clusters) mma_unit(0, pl.kblocks);
+  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; ok && p < (HALF ? pl.whole : pl.tiles); p += pl.clusters)
+    mma_unit(0, pl.kblocks, false);
+  if constexpr (HALF) {
+    if (ok && cluster < 2 * pl.half_tiles) mma_unit(0, pl.kblocks, true);
+  }
   if (!ok && issued) {
     tc_commit_pair(&s.drain, 0x1);
     wait_drain(&s.drain, 0);
@@ -537,14 +564,16 @@ __device__ __forceinline__ void run_mma(SharedStorage& s, uint32_t tmem, const P
 
 // Leader CTA, scale warp: copies each stage's scale atoms into both SMs' tensor
 // memory in its own tcgen05 stream and signals sfready[stage] when they landed.
-template <bool SPLIT>
+template <bool SPLIT, bool HALF>
 __device__ __forceinline__ void run_scales(SharedStorage& s, uint32_t tmem, const Plan& pl, int cluster,
                                            volatile int* abort_flag) {
-  // the split range's K-steps, then kblocks per whole tile
+  // the split range's K-steps, then kblocks per whole tile, then per half unit
   const int first_whole = (SPLIT ? pl.sk_tiles : 0) + cluster;
-  const int64_t whole = first_whole < pl.tiles ? (pl.tiles - first_whole + pl.clusters - 1) / pl.clusters : 0;
+  const int end = HALF ? pl.whole : pl.tiles;
+  const int64_t whole = first_whole < end ? (end - first_whole + pl.clusters - 1) / pl.clusters : 0;
   int64_t steps = whole * pl.kblocks;
   if constexpr (SPLIT) steps += split_start(pl, cluster + 1) - split_start(pl, cluster);
+  if constexpr (HALF) steps += cluster < 2 * pl.half_tiles ? pl.kblocks : 0;
   int stage = 0;
   uint32_t phase = 0;
   for (int64_t g = 0; g < steps; ++g) {
@@ -708,8 +737,11 @@ struct EpiCtx {
 // drain the accumulator, release it, then the fused epilogue. Returns false when
 // a wait gave up. n_total: the GEMM's N (rows of B; stacked 2 F for kEpiSwiglu);
 // output width F = n_total / 2 for kEpiSwiglu, else n_total.
+// col_tile: the unit's first output column (nb * BN for a whole tile; a half tile's
+// 128 columns are drained by the warps of column group 0).
 template <int EPI, bool DBG, bool SPLIT>
-__device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e, int mb, int nb, uint32_t& acc_phase,
+__device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e, int mb, int nb, int col_tile,
+                                              uint32_t& acc_phase,
                                               const Plan& pl, const Unit& u, const uint16_t* __restrict__ bias,
                                               const uint16_t* __restrict__ gate, const uint16_t* residual, void* out,
                                               uint8_t* __restrict__ out_scales, float* __restrict__ dbg,
@@ -720,7 +752,7 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
   float* bw = e.bw;
   float* gw = e.gw;
   // first output column of this warp: 64 of them (kEpiSwiglu) or 128
-  const int col0 = (EPI == kEpiSwiglu) ? nb * kBHalfRows + 64 * h : nb * BN + h * kEpiCols;
+  const int col0 = (EPI == kEpiSwiglu) ? nb * kBHalfRows + 64 * h : col_tile + h * kEpiCols;
   if constexpr (EPI == kEpiSwiglu)
     stage_vec(bw, bias, col0, n_out + col0, lane, 0.f);
   else
@@ -884,7 +916,23 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
   return true;
 }
 
-template <int EPI, bool DBG, bool SPLIT>
+// The warps of column group 1 during a half tile: nothing to drain; they release
+// the accumulator (the barrier counts every epilogue warp) once it is full.
+__device__ __forceinline__ bool epilogue_skip(SharedStorage& s, const EpiCtx& e, uint32_t& acc_phase,
+                                              volatile int* abort_flag) {
+  int ok = 0;
+  if (e.lane == 0) ok = wait_bounded(&s.tmem_full, acc_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return false;
+  tc_fence_after();
+  tc_fence_before();
+  __syncwarp();
+  if (e.lane == 0) mbar_arrive_remote_relaxed(e.tmem_empty_leader);
+  acc_phase ^= 1u;
+  return true;
+}
+
+template <int EPI, bool DBG, bool SPLIT, bool HALF>
 __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, const Plan& pl,
                                              const CUtensorMap* tmap_out, int cluster, int rank, int num_m,
                                              int m_total, int n_total,
@@ -917,32 +965,46 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
     while (cursor_next(pl, cur, u)) {
       int mb, nb;
       pair_tile(pl, u.tile, rank, &mb, &nb);
-      if (!epilogue_tile<EPI, DBG, true>(s, e, mb, nb, acc_phase, pl, u, bias, gate, residual, out, out_scales, dbg,
-                                         abort_flag))
+      if (!epilogue_tile<EPI, DBG, true>(s, e, mb, nb, nb * BN, acc_phase, pl, u, bias, gate, residual, out,
+                                         out_scales, dbg, abort_flag))
         return;
     }
   }
   const Unit whole = {0, 0, 0};
-  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; p < pl.tiles; p += pl.clusters) {
+  for (int p = (SPLIT ? pl.sk_tiles : 0) + cluster; p < (HALF ? pl.whole : pl.tiles); p += pl.clusters) {
     int mb, nb;
     pair_tile(pl, p, rank, &mb, &nb);
-    if (!epilogue_tile<EPI, DBG, false>(s, e, mb, nb, acc_phase, pl, whole, bias, gate, residual, out, out_scales,
-                                        dbg, abort_flag))
+    if (!epilogue_tile<EPI, DBG, false>(s, e, mb, nb, nb * BN, acc_phase, pl, whole, bias, gate, residual, out,
+                                        out_scales, dbg, abort_flag))
       return;
+  }
+  if constexpr (HALF) {
+    if (cluster < 2 * pl.half_tiles) {
+      int mb, nb;
+      pair_tile(pl, pl.whole + cluster / 2, rank, &mb, &nb);
+      if (e.h == 0)
+        epilogue_tile<EPI, DBG, false>(s, e, mb, nb, nb * BN + (cluster % 2) * kHalfCols, acc_phase, pl, whole, bias,
+                                       gate, residual, out, out_scales, dbg, abort_flag);
+      else
+        epilogue_skip(s, e, acc_phase, abort_flag);
+    }
   }
 }
 
 // SPLIT: the launch divides its first sk_tiles tiles along K (a separate instance,
 // so the whole-tile kernel carries none of that code). QA: the kernel quantizes A
-// itself from BF16 (an extra warp; never with SPLIT).
-template <int EPI, bool DBG, bool SPLIT, bool QA>
+// itself from BF16 (an extra warp; never with SPLIT). HALF: the last half_tiles
+// tiles run as two 128-column halves on two pairs each (a separate instance too).
+template <int EPI, bool DBG, bool SPLIT, bool QA, bool HALF>
 __global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   const __grid_constant__ CUtensorMap tmap_bh,
                    const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sb,
                    const __grid_constant__ CUtensorMap tmap_out, const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate, const uint16_t* residual,
                    void* out, uint8_t* __restrict__ out_scales, float* __restrict__ dbg, int m_total, int n_total,
                    int k_total, SplitArgs split, QaArgs qa) {
   static_assert(!(QA && SPLIT), "the in-kernel quantizer runs without the split tail");
+  static_assert(!(HALF && (SPLIT || DBG || EPI == kEpiSwiglu)), "half tiles: whole-tile epilogues without debug output");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   SharedStorage& s =
@@ -957,6 +1019,8 @@ __global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
   plan.kblocks = k_total / BK;
   plan.clusters = static_cast<int>(cluster_count_x());
   plan.sk_tiles = split.sk_tiles;
+  plan.half_tiles = HALF ? split.half_tiles : 0;
+  plan.whole = plan.tiles - plan.half_tiles;
   plan.partial = split.partial;
   plan.arrivals = split.arrivals;
   const int cluster = static_cast<int>(cluster_id_x());
@@ -982,6 +1046,7 @@ __global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmap_a);
     prefetch_tensormap(&tmap_b);
+    if (HALF) prefetch_tensormap(&tmap_bh);
     prefetch_tensormap(&tmap_sa);
     prefetch_tensormap(&tmap_sb);
     prefetch_tensormap(&tmap_out);
@@ -998,16 +1063,17 @@ __global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0)
-      run_producer<SPLIT, QA>(s, &tmap_a, &tmap_b, &tmap_sa, &tmap_sb, plan, cluster, rank, EPI == kEpiSwiglu,
-                              n_total / 2, qa, num_m, abort_flag);
+      run_producer<SPLIT, QA, HALF>(s, &tmap_a, &tmap_b, &tmap_bh, &tmap_sa, &tmap_sb, plan, cluster, rank,
+                                    EPI == kEpiSwiglu, n_total / 2, qa, num_m, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) run_mma<SPLIT>(s, tmem, plan, cluster, abort_flag);
+    if (lane == 0 && rank == 0) run_mma<SPLIT, HALF>(s, tmem, plan, cluster, abort_flag);
   } else if (warp == 2 + kEpiWarps) {
-    if (lane == 0 && rank == 0) run_scales<SPLIT>(s, tmem, plan, cluster, abort_flag);
+    if (lane == 0 && rank == 0) run_scales<SPLIT, HALF>(s, tmem, plan, cluster, abort_flag);
   } else if (QA && warp == kQaWarp) {
     run_quantizer(qa, m_total, k_total, lane);
   } else {
-    run_epilogue<EPI, DBG, SPLIT>(s, tmem, warp, lane, plan, &tmap_out, cluster, rank, num_m, m_total, n_total, bias,
+    run_epilogue<EPI, DBG, SPLIT, HALF>(s, tmem, warp, lane, plan, &tmap_out, cluster, rank, num_m, m_total, n_total,
+                                        bias,
                                   gate, residual, out, out_scales, dbg, abort_flag);
     // the stores' writes are complete (and their shared sources read) before the
     // CTA leaves, also after a wait gave up
@@ -1123,9 +1189,9 @@ static bool make_codes_out_map(CUtensorMap* map, void* codes, int64_t m, int64_t
 // filled on a device's first call (any thread may fill them). The attribute belongs
 // to the context, so it is set again when the device's context has changed (a new
 // primary context after cudaDeviceReset).
-template <int EPI, bool DBG, bool SPLIT, bool QA>
+template <int EPI, bool DBG, bool SPLIT, bool QA, bool HALF>
 static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) {
-  auto kern = mx_gemm_kernel<EPI, DBG, SPLIT, QA>;
+  auto kern = mx_gemm_kernel<EPI, DBG, SPLIT, QA, HALF>;
   static std::atomic<unsigned long long> configured[64];   // context ID + 1 the attribute was set in; 0: none
   static std::atomic<int> cached[64];
   const bool cacheable = dev >= 0 && dev < 64;
@@ -1150,9 +1216,10 @@ static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) 
 }
 
 template <int EPI, bool DBG, bool QA>
-static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                                   const CUtensorMap& tsb, const CUtensorMap& tout, const GemmArgs& a,
-                                   cudaStream_t stream) {
+static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
+                                   const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& tout,
+                                   const GemmArgs& a, cudaStream_t stream) {
+  constexpr bool kHalvesOk = !DBG && EPI != kEpiSwiglu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1176,11 +1243,13 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   int clusters = 0;
-  e = max_clusters<EPI, DBG, false, QA>(dev, cfg, &clusters);
+  e = max_clusters<EPI, DBG, false, QA, false>(dev, cfg, &clusters);
   if (e != cudaSuccess) return e;
-  // as many CTA pairs as are co-resident (one CTA per SM), at most one per tile
-  const GemmPlan plan = plan_gemm(a.m, a.n, a.k, clusters, QA ? nullptr : a.workspace, QA ? 0 : a.workspace_bytes);
+  // as many CTA pairs as are co-resident (one CTA per SM), at most one per tile or half tile
+  const GemmPlan plan =
+      plan_gemm(a.m, a.n, a.k, clusters, QA ? nullptr : a.workspace, QA ? 0 : a.workspace_bytes, kHalvesOk);
   SplitArgs split = {};
+  split.half_tiles = plan.half_tiles;
   if (plan.sk_tiles > 0) {
     split.sk_tiles = plan.sk_tiles;
     split.arrivals = static_cast<unsigned*>(a.workspace);
@@ -1199,20 +1268,25 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
     cfg.numAttrs = 3;
   }
   cfg.gridDim = dim3(kPair * plan.clusters, 1, 1);
+  // the split and half-tile instances have the same resources; their attribute is
+  // set on first use
+  int same = clusters;
+  decltype(&mx_gemm_kernel<EPI, DBG, false, QA, false>) kern = mx_gemm_kernel<EPI, DBG, false, QA, false>;
   if constexpr (!QA) {
     if (plan.sk_tiles > 0) {
-      // the split instance has the same resources; its attribute is set on first use
-      int same = 0;
-      e = max_clusters<EPI, DBG, true, false>(dev, cfg, &same);
-      if (e != cudaSuccess) return e;
-      if (same != clusters) return cudaErrorLaunchOutOfResources;
+      e = max_clusters<EPI, DBG, true, false, false>(dev, cfg, &same);
+      kern = mx_gemm_kernel<EPI, DBG, true, false, false>;
     }
   }
-  decltype(&mx_gemm_kernel<EPI, DBG, false, QA>) kern = mx_gemm_kernel<EPI, DBG, false, QA>;
-  if constexpr (!QA) {
-    if (plan.sk_tiles > 0) kern = mx_gemm_kernel<EPI, DBG, true, false>;
+  if constexpr (kHalvesOk) {
+    if (plan.half_tiles > 0) {
+      e = max_clusters<EPI, DBG, false, QA, true>(dev, cfg, &same);
+      kern = mx_gemm_kernel<EPI, DBG, false, QA, true>;
+    }
   }
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tout, static_cast<const uint16_t*>(a.bias),
+  if (e != cudaSuccess) return e;
+  if (same != clusters) return cudaErrorLaunchOutOfResources;
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tsa, tsb, tout, static_cast<const uint16_t*>(a.bias),
                          static_cast<const uint16_t*>(a.gate), static_cast<const uint16_t*>(a.residual), a.out,
                          static_cast<uint8_t*>(a.out_scales), a.debug_prequant, static_cast<int>(a.m),
                          static_cast<int>(a.n), static_cast<int>(a.k), split, qa);
@@ -1222,11 +1296,12 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, bool* encode_failed) {
   *encode_failed = false;
-  CUtensorMap ta, tb, tsa, tsb, tout;
+  CUtensorMap ta, tb, tbh, tsa, tsb, tout;
   const bool bf16_out = a.epilogue == kEpiBf16 || a.epilogue == kEpiGateRes;
   const int64_t w_out = a.epilogue == kEpiSwiglu ? a.n / 2 : a.n;
   if (!make_codes_map(&ta, a.a_codes, a.m, a.k, BM) ||
       !make_codes_map(&tb, a.b_codes, a.n, a.k, kBHalfRows) ||
+      !make_codes_map(&tbh, a.b_codes, a.n, a.k, kHalfCols / kPair) ||
       !make_scale_maps(&tsa, &tsb, a.a_scales, a.b_scales, a.m, a.n, a.k, a.epilogue == kEpiSwiglu ? 1u : 2u) ||
       !(bf16_out ? make_bf16_out_map(&tout, a.out, a.m, a.n) : make_codes_out_map(&tout, a.out, a.m, w_out))) {
     *encode_failed = true;
@@ -1238,22 +1313,22 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, boo
     // the in-kernel quantizer: no debug output, no split tail
     if (dbg) return cudaErrorInvalidValue;
     switch (a.epilogue) {
-      case kEpiBf16: return launch_instance<kEpiBf16, false, true>(ta, tb, tsa, tsb, tout, a, stream);
-      case kEpiGelu: return launch_instance<kEpiGelu, false, true>(ta, tb, tsa, tsb, tout, a, stream);
-      case kEpiSwiglu: return launch_instance<kEpiSwiglu, false, true>(ta, tb, tsa, tsb, tout, a, stream);
-      case kEpiGateRes: return launch_instance<kEpiGateRes, false, true>(ta, tb, tsa, tsb, tout, a, stream);
+      case kEpiBf16: return launch_instance<kEpiBf16, false, true>(ta, tb, tbh, tsa, tsb, tout, a, stream);
+      case kEpiGelu: return launch_instance<kEpiGelu, false, true>(ta, tb, tbh, tsa, tsb, tout, a, stream);
+      case kEpiSwiglu: return launch_instance<kEpiSwiglu, false, true>(ta, tb, tbh, tsa, tsb, tout, a, stream);
+      case kEpiGateRes: return launch_instance<kEpiGateRes, false, true>(ta, tb, tbh, tsa, tsb, tout, a, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (a.epilogue) {
-    case kEpiBf16: return launch_instance<kEpiBf16, false, false>(ta, tb, tsa, tsb, tout, a, stream);
+    case kEpiBf16: return launch_instance<kEpiBf16, false, false>(ta, tb, tbh, tsa, tsb, tout, a, stream);
     case kEpiGelu:
-      return dbg ? launch_instance<kEpiGelu, true, false>(ta, tb, tsa, tsb, tout, a, stream)
-                 : launch_instance<kEpiGelu, false, false>(ta, tb, tsa, tsb, tout, a, stream);
+      return dbg ? launch_instance<kEpiGelu, true, false>(ta, tb, tbh, tsa, tsb, tout, a, stream)
+                 : launch_instance<kEpiGelu, false, false>(ta, tb, tbh, tsa, tsb, tout, a, stream);
     case kEpiSwiglu:
-      return dbg ? launch_instance<kEpiSwiglu, true, false>(ta, tb, tsa, tsb, tout, a, stream)
-                 : launch_instance<kEpiSwiglu, false, false>(ta, tb, tsa, tsb, tout, a, stream);
-    case kEpiGateRes: return launch_instance<kEpiGateRes, false, false>(ta, tb, tsa, tsb, tout, a, stream);
+      return dbg ? launch_instance<kEpiSwiglu, true, false>(ta, tb, tbh, tsa, tsb, tout, a, stream)
+                 : launch_instance<kEpiSwiglu, false, false>(ta, tb, tbh, tsa, tsb, tout, a, stream);
+    case kEpiGateRes: return launch_instance<kEpiGateRes, false, false>(ta, tb, tbh, tsa, tsb, tout, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1272,7 +1347,7 @@ cudaError_t gemm_max_clusters(int* clusters) {
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return max_clusters<kEpiBf16, false, false, false>(dev, cfg, clusters);
+  return max_clusters<kEpiBf16, false, false, false, false>(dev, cfg, clusters);
 }
 
 // A wait that nothing will ever satisfy: it must give up after the bound, set

@@ -64,13 +64,24 @@ struct SplitArgs {
   int sk_tiles;          // tiles divided along K (0: none)
   float4* partial;       // partial-accumulator slots
   unsigned* arrivals;    // arrival counters
+  int half_tiles;        // trailing tiles run as two 128-column halves (0: none)
 };
 
 struct GemmPlan {
   int64_t tiles;    // pair tiles
   int clusters;     // CTA pairs launched
   int sk_tiles;     // leading tiles divided along K
+  int half_tiles;   // trailing tiles run as two 128-column halves
 };
+
+// ---------------------------------------------------------------- half tiles
+// Without a split tail, the last round's tiles (tiles mod pairs of them, or all
+// tiles when there are fewer than pairs) can run as two 128-column halves each,
+// on twice as many pairs: a half moves 3/4 of a tile's operand bytes (all of its
+// A rows, half of its B rows) for half the work, so a nearly empty last round
+// ends sooner and its last epilogue is half as long. Taken when the halves fit in
+// one round (at most pairs / 2 such tiles), for the epilogues with one output
+// column per accumulator column (not the stacked SwiGLU weight).
 
 inline int64_t gemm_pair_tiles(int64_t m, int64_t n) {
   return ((m + kPairTileRows - 1) / kPairTileRows) * (n / kPairTileCols);
@@ -87,18 +98,28 @@ inline size_t split_workspace_bytes(int64_t m, int64_t n, int64_t k) {
   return kArrivalsBytes + static_cast<size_t>(2 * pairs) * kSplitSlotBytes;
 }
 
-// Launch plan: CTA pairs (co-resident ones, at most one per tile) and the split tail.
+// Launch plan: CTA pairs (co-resident ones, at most one per tile or half tile),
+// the split tail, and the half tiles when halves_ok.
 inline GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int max_clusters, const void* workspace,
-                          size_t workspace_bytes) {
+                          size_t workspace_bytes, bool halves_ok = false) {
   GemmPlan p;
   p.tiles = gemm_pair_tiles(m, n);
   p.clusters = static_cast<int>(max_clusters < p.tiles ? max_clusters : p.tiles);
   p.sk_tiles = 0;
+  p.half_tiles = 0;
   const int64_t rem = p.clusters > 0 ? p.tiles % p.clusters : 0;
   if (workspace != nullptr && p.tiles > p.clusters && rem != 0 && rem * kMaxSplitLeftoverDiv <= p.clusters &&
       k / kStepK >= kMinSplitKSteps && p.clusters <= kMaxSplitClusters && (p.clusters + rem) * (k / kStepK) < (int64_t{1} << 31) &&
       workspace_bytes >= kArrivalsBytes + static_cast<size_t>(2 * p.clusters) * kSplitSlotBytes)
     p.sk_tiles = static_cast<int>(p.clusters + rem);
+  if (halves_ok && p.sk_tiles == 0 && p.tiles > 0) {
+    if (p.tiles > max_clusters) {
+      if (rem != 0 && 2 * rem <= p.clusters) p.half_tiles = static_cast<int>(rem);
+    } else if (2 * p.tiles <= max_clusters) {
+      p.half_tiles = static_cast<int>(p.tiles);
+      p.clusters = static_cast<int>(2 * p.tiles);
+    }
+  }
   return p;
 }
 

@@ -1,6 +1,7 @@
-// Prints the GEMM launch plan (pair tiles, CTA pairs, leading tiles divided along K)
-// and the split-tail workspace size for shapes read from standard input, one
-// "m n k max_clusters workspace_bytes" per line (workspace_bytes < 0: no workspace).
+// Prints the GEMM launch plan (pair tiles, CTA pairs, leading tiles divided along K),
+// the split-tail workspace size and the tiles run as halves, for shapes read from
+// standard input, one "m n k max_clusters workspace_bytes halves_ok" per line
+// (workspace_bytes < 0: no workspace).
 // Host code only: the plan is inline in the library's internal header.
 #include <cstdio>
 
@@ -8,13 +9,13 @@
 
 int main() {
   long long m, n, k, ws;
-  int clusters;
+  int clusters, halves;
   static unsigned char dummy[1];
-  while (std::scanf("%lld %lld %lld %d %lld", &m, &n, &k, &clusters, &ws) == 5) {
+  while (std::scanf("%lld %lld %lld %d %lld %d", &m, &n, &k, &clusters, &ws, &halves) == 6) {
     const mxk::GemmPlan p = mxk::plan_gemm(m, n, k, clusters, ws < 0 ? nullptr : dummy,
-                                           ws < 0 ? 0 : static_cast<size_t>(ws));
-    std::printf("%lld %d %d %zu\n", static_cast<long long>(p.tiles), p.clusters, p.sk_tiles,
-                mxk::split_workspace_bytes(m, n, k));
+                                           ws < 0 ? 0 : static_cast<size_t>(ws), halves != 0);
+    std::printf("%lld %d %d %zu %d\n", static_cast<long long>(p.tiles), p.clusters, p.sk_tiles,
+                mxk::split_workspace_bytes(m, n, k), p.half_tiles);
   }
   return 0;
 }

@@ -28,12 +28,13 @@ def plan(tmp_path_factory):
     subprocess.run([cxx, "-std=c++17", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", CSRC,
                     "-I", cuda_inc, os.path.join(ROOT, "tests", "helpers", "plan_probe.cpp"), "-o", exe], check=True)
 
-    def run(m, n, k, clusters=76, ws=None):
+    def run(m, n, k, clusters=76, ws=None, halves=False):
         full = COUNTERS + 2 * min(80, max(1, ((m + 255) // 256) * (n // 256) - 1)) * SLOT
         ws_bytes = full if ws is None else ws
-        out = subprocess.run([exe], input=f"{m} {n} {k} {clusters} {ws_bytes}\n", capture_output=True, text=True,
-                             check=True).stdout.split()
-        return tuple(int(v) for v in out)
+        out = subprocess.run([exe], input=f"{m} {n} {k} {clusters} {ws_bytes} {int(halves)}\n", capture_output=True,
+                             text=True, check=True).stdout.split()
+        vals = tuple(int(v) for v in out)
+        return vals if halves else vals[:4]
 
     return run
 
@@ -78,3 +79,24 @@ def test_workspace_bytes_query(plan):
     assert plan(256, 256, 8192)[3] == 0                     # one tile
     assert plan(512, 256, 8192)[3] == COUNTERS + 2 * 1 * SLOT
     assert plan(20480, 3072, 12288)[3] == COUNTERS + 2 * 80 * SLOT
+
+
+def test_half_tiles(plan):
+    """Without a split, the last round's tiles run as halves when at most pairs / 2
+    are left over, and a GEMM of at most pairs / 2 tiles runs all of them as halves
+    on twice as many pairs; never where the split tail is taken, nor when the
+    epilogue cannot (halves_ok false). Output: tiles, pairs, split, ws, half tiles."""
+    # M = 4096 up-projection: 768 tiles = 10 rounds + 8 (K = 3072: no split)
+    assert plan(4096, 12288, 3072, halves=True)[:3] + plan(4096, 12288, 3072, halves=True)[4:] == (768, 76, 0, 8)
+    assert plan(4096, 12288, 3072, halves=False)[:3] == (768, 76, 0)
+    # 38 left over of 76: halves; 39: not
+    assert plan(256 * 114, 256, 3072, halves=True)[4] == 38
+    assert plan(256 * 115, 256, 3072, halves=True)[4] == 0
+    # a round's worth exactly: nothing left over
+    assert plan(256 * 152, 256, 3072, halves=True)[4] == 0
+    # few tiles: all halves on twice the pairs (PR1: 1 x 2 tiles)
+    assert plan(128, 512, 256, halves=True) == (2, 4, 0, 0, 2)
+    assert plan(256 * 38, 256, 3072, halves=True)[1:] == (76, 0, 0, 38)
+    assert plan(256 * 39, 256, 3072, halves=True)[1:] == (39, 0, 0, 0)
+    # the split tail wins where it applies (DiT down-projection)
+    assert plan(16384, 3072, 12288, halves=True)[2:] == (84, COUNTERS + 2 * 80 * SLOT, 0)
