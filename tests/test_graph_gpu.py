@@ -82,3 +82,36 @@ def test_quantize_then_gemm_graph_many_replays(lib):
         lib.mx_gemm(q, wq, b, lib.MX_EPI_BIAS_BF16, out=yi)
 
     _replays_match(lib, run, lambda s: bf16_to_device(synth.pr1(seed=s, M=256, K=512, N=512)["x"]), x, y, n=20)
+
+
+def test_fused_quantizer_graph_replay(lib):
+    """The GEMM that quantizes its own activations under capture: mx_mlp at a width
+    whose up-projection encodes rows 512.. in-kernel (ff = 12288), and
+    mx_quantize_gemm on its own, captured (the cooperative launch becomes a graph
+    node) and replayed on fresh inputs; the captured quantize kernel zeroes the
+    row-block counters on every replay, so each replay equals the eager call."""
+    import torch
+
+    M, d, ff = 1536, 256, 12288
+    w = synth.full_mlp(M=M, d=d, ff=ff)
+    w1 = lib.mx_quantize(bf16_to_device(w["w1"]))
+    w2 = lib.mx_quantize(bf16_to_device(w["w2"]))
+    b1, b2 = bf16_to_device(w["b1"]), bf16_to_device(w["b2"])
+    ws = torch.empty(lib.mx_mlp_workspace_bytes(M, d, ff), dtype=torch.uint8, device="cuda")
+    x = bf16_to_device(w["x"])
+    y = torch.empty_like(x)
+
+    def mlp(xi, yi):
+        lib.mx_mlp(xi, w1, b1, w2, b2, y=yi, workspace=ws)
+
+    mlp(x, y)
+    _replays_match(lib, mlp, lambda s: bf16_to_device(synth.full_mlp(seed=s, M=M, d=d, ff=ff)["x"]), x, y)
+
+    qws = torch.empty(lib.mx_quantize_gemm_workspace_bytes(M, d), dtype=torch.uint8, device="cuda")
+    h = torch.empty((M, ff), dtype=torch.bfloat16, device="cuda")
+
+    def up(xi, hi):
+        lib.mx_quantize_gemm(xi, w1, b1, lib.MX_EPI_BIAS_BF16, out=hi, workspace=qws)
+
+    up(x, h)
+    _replays_match(lib, up, lambda s: bf16_to_device(synth.full_mlp(seed=60 + s, M=M, d=d, ff=ff)["x"]), x, h)
