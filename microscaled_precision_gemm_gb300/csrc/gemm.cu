@@ -55,7 +55,10 @@
 // TMA threads) and is bounded (2 s on the global timer); on expiry the kernel
 // records an error bit, drains its in-flight copies and MMAs (again bounded), frees
 // tensor memory and returns. A second instance of the kernel (SPLIT) divides a
-// nearly empty last round of tiles along K across all pairs (see Plan below).
+// nearly empty last round of tiles along K across all pairs (see Plan below);
+// another (HALF) runs such a round's tiles as 128-column halves on twice the pairs
+// (N = 128 pair MMAs), where the split tail is not taken. The QA instance (warp 11
+// above) is a cooperative launch, since its producers wait on other CTAs' warps.
 // Launched with programmatic dependent launch: the
 // prologue (barriers, tensor memory, tensor-map prefetch) may overlap the previous
 // kernel in the stream, and griddepcontrol.wait holds every access to global
@@ -284,8 +287,8 @@ __device__ __forceinline__ bool cursor_next(const Plan& pl, Cursor& k, Unit& u) 
 // reads 128 x strips, before the first TMA load of that block. The counters are
 // zero at the launch (the quantize kernel before it zeroes them). Every CTA's
 // quantizer warp runs without waiting on anything, so every block is published
-// whatever the other roles do; producers of CTAs that are resident wait only on
-// warps that are resident too or will be once the previous kernel has left.
+// whatever the other roles do, and the launch is cooperative, so every CTA whose
+// quantizer warp a producer waits on is resident.
 struct QaArgs {
   const uint16_t* x;   // BF16 A [M][K], row stride ld_x elements
   int64_t ld_x;
