@@ -263,7 +263,8 @@ mx_status mx_gemm_launch_plan(int64_t M, int64_t N, int64_t K, size_t workspace_
  *              16-byte aligned; must not overlap out or the workspace
  *   b_*, bias, N, K, out, out_scales : as mx_gemm (K % 128 == 0, N % 256 == 0)
  *   gate, residual : MX_EPI_GATE_RESIDUAL_BF16 only, as mx_gemm_gate_residual
- *              (residual required; out may be residual itself); ignored otherwise
+ *              (residual required; out may be residual itself; neither may overlap
+ *              the workspace); ignored otherwise
  *   workspace: device, mx_quantize_gemm_workspace_bytes(M, K) bytes, 256-byte
  *              aligned, any contents. After the call (in stream order) it holds
  *              MXFP6(x): codes at offset 0 (mx_codes_bytes(M, K) bytes), tiled

@@ -511,8 +511,10 @@ mx_status mx_quantize_gemm(const void* x, int64_t M, int64_t K, int64_t ld_x, co
   if (e == MX_EPI_GATE_RESIDUAL_BF16) {
     if (residual == nullptr) return MX_ERR_INVALID_ARG;
     if (!aligned(residual, 16) || (gate != nullptr && !aligned(gate, 16))) return MX_ERR_MISALIGNED;
-    // the residual may be the output itself (in-place update), but not overlap it otherwise
+    // the residual may be the output itself (in-place update), but not overlap it
+    // otherwise, nor the workspace the GEMM writes MXFP6(x) into
     if (residual != out && overlaps(residual, out_bytes, out, out_bytes)) return MX_ERR_INVALID_ARG;
+    if (overlaps(residual, out_bytes, workspace, l.total)) return MX_ERR_INVALID_ARG;
   }
   // x is read while the output and the workspace are written
   if (overlaps(x, x_bytes, out, out_bytes) || overlaps(x, x_bytes, workspace, l.total) ||

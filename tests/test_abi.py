@@ -198,6 +198,7 @@ def test_quantize_gemm_rejects_bad_arguments(lib):
     assert call(epi=3, res=OUT + 1024) == INVALID    # partial overlap with the output
     assert call(out=X + 4096) == INVALID             # x overlaps the output
     assert call(ws=X - 256) == INVALID               # x overlaps the workspace
+    assert call(epi=3, res=WS + 1024, out=WS + 1024 + (1 << 20)) == INVALID   # residual inside the workspace
     assert call(M=0, x=None, b=None, out=None, ws=None) == OK
     assert call(N=0, x=None, b=None, out=None, ws=None) == OK
     for ok in (call(), call(epi=3, res=OUT), call(epi=GELU, out_sc=0x3000000)):
