@@ -95,6 +95,7 @@ constexpr int kEpiCols = BN * 4 / kEpiWarps;     // accumulator columns each epi
 constexpr int kEpiChunks = kEpiCols / 32;        // 32-column MX blocks per epilogue thread
 constexpr int kThreads = (3 + kEpiWarps) * 32;  // + scale-copy warp
 constexpr int kQaWarp = 3 + kEpiWarps;           // the QA instance's quantizer warp
+constexpr uint32_t kQaPauseNs = 1000;              // the quantizer warp's pause between groups
 constexpr int kThreadsQa = kThreads + 32;
 constexpr uint32_t kABytes = BM * BK;  // 16-byte shared slot per 16 codes -> 1 byte per element
 constexpr uint32_t kBBytes = kBHalfRows * BK;   // this CTA's half of the B tile
@@ -400,6 +401,11 @@ __device__ __forceinline__ void run_quantizer(const QaArgs& qa, int m_total, int
     fence_proxy_async_global();
     __syncwarp();
     if (lane == 0) red_release_gpu_add(qa.ready + i0 / strips / 128u, kQaGroup);
+    // a pause between groups spreads the warp's memory instructions over more of the
+    // main loop, which shares the SM's memory pipeline with them: 1 us took 1 and 2.7
+    // us off the M = 4096 and 20480 up-projections; 1.5 us and more fell behind the
+    // GEMM's reads (measured)
+    sleep_ns(kQaPauseNs);
   }
 }
 
