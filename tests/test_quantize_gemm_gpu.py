@@ -236,3 +236,32 @@ def test_threads_on_separate_streams(lib):
     for i in range(n_threads):
         assert torch.equal(outs[i], ref[i]), f"thread {i} differs from the serial result"
     assert lib.mx_device_error() == 0
+
+
+def test_nan_and_inf_blocks_in_kernel(lib):
+    """NaN and Inf in rows the GEMM encodes itself: those blocks get the E8M0 NaN
+    scale and zero codes exactly as the quantize kernel writes them, and the output
+    equals K1 followed by mx_gemm bit for bit (NaN rows included)."""
+    import torch
+
+    M, K, N = 1400, 512, 12288
+    x_bits, x, w_bits, bias = _inputs(13, M, K, N)
+    nan, inf, ninf = 0x7FC0, 0x7F80, 0xFF80
+    x_bits = x_bits.copy()
+    x_bits[700, 5] = nan          # in-kernel rows (the lead is the first 512)
+    x_bits[901, 300] = inf
+    x_bits[1399, 511] = ninf
+    x_bits[100, 64] = nan         # a lead row, for comparison
+    x = bf16_to_device(x_bits)
+    wq = lib.mx_quantize(bf16_to_device(w_bits))
+    b = bf16_to_device(bias)
+    ws = torch.empty(lib.mx_quantize_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    y = lib.mx_quantize_gemm(x, wq, b, lib.MX_EPI_BIAS_BF16, workspace=ws)
+    rows = np.array([100, 700, 901, 1399, 1398])
+    xq = _check_xq(lib, ws, x, x_bits, rows)
+    ref = lib.mx_gemm(xq, wq, b, lib.MX_EPI_BIAS_BF16)
+    assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+    got = bf16_from_device(y)
+    assert np.isnan(f32_from_bf16_bits(got[[100, 700, 901, 1399]])).all()
+    assert not np.isnan(f32_from_bf16_bits(got[1398])).any()
+    assert lib.mx_device_error() == 0
