@@ -303,7 +303,16 @@ QgLayout qg_layout(int64_t M, int64_t K) {
 
 bool overlaps(const void* a, uintptr_t a_bytes, const void* b, uintptr_t b_bytes) {
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-  return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+  const uintptr_t a1 = a_bytes > UINTPTR_MAX - a0 ? UINTPTR_MAX : a0 + a_bytes;
+  const uintptr_t b1 = b_bytes > UINTPTR_MAX - b0 ? UINTPTR_MAX : b0 + b_bytes;
+  return a0 < b1 && b0 < a1;
+}
+
+// x * y (both >= 0), saturated at UINTPTR_MAX: a byte span that cannot exist
+// overlaps everything rather than wrapping around.
+uintptr_t mul_sat(uint64_t x, uint64_t y) {
+  if (x != 0 && y > UINTPTR_MAX / x) return UINTPTR_MAX;
+  return static_cast<uintptr_t>(x * y);
 }
 
 }  // namespace
@@ -505,9 +514,12 @@ mx_status mx_quantize_gemm(const void* x, int64_t M, int64_t K, int64_t ld_x, co
   if (workspace == nullptr) return MX_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return MX_ERR_MISALIGNED;
   if (workspace_bytes < l.total) return MX_ERR_WORKSPACE_TOO_SMALL;
-  const uintptr_t x_bytes = static_cast<uintptr_t>((M - 1) * ld_x + K) * 2u;
-  const uintptr_t out_bytes = static_cast<uintptr_t>(mxfp6_out(e) ? mxk::codes_bytes(M, e == MX_EPI_BIAS_SWIGLU_MXFP6 ? N / 2 : N)
-                                                                   : M * N * 2);
+  // byte spans of x (rows of ld_x elements, the last one K) and of the output
+  const uintptr_t x_rows = mul_sat(static_cast<uint64_t>(M - 1), static_cast<uint64_t>(ld_x));
+  const uintptr_t x_bytes = mul_sat(x_rows > UINTPTR_MAX - static_cast<uint64_t>(K) ? UINTPTR_MAX : x_rows + K, 2);
+  const uint64_t w_out = e == MX_EPI_BIAS_SWIGLU_MXFP6 ? N / 2 : N;
+  const uintptr_t out_bytes = mxfp6_out(e) ? mul_sat(mul_sat(static_cast<uint64_t>(M), w_out), 3) / 4
+                                           : mul_sat(mul_sat(static_cast<uint64_t>(M), static_cast<uint64_t>(N)), 2);
   if (e == MX_EPI_GATE_RESIDUAL_BF16) {
     if (residual == nullptr) return MX_ERR_INVALID_ARG;
     if (!aligned(residual, 16) || (gate != nullptr && !aligned(gate, 16))) return MX_ERR_MISALIGNED;
