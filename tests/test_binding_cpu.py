@@ -39,6 +39,11 @@ CALLS = {
     "mx_gated_mlp": lambda: mx.mx_gated_mlp(_bf16(256, 256), _mx(1024, 256), None, _mx(256, 512), None),
     "mx_dit_mlp_block": lambda: mx.mx_dit_mlp_block(_bf16(256, 256), None, None, None, _mx(512, 256), None,
                                                     _mx(256, 512), None),
+    "mx_quantize_gemm": lambda: mx.mx_quantize_gemm(_bf16(256, 256), _mx(512, 256)),
+    "mx_quantize_gemm gate residual": lambda: mx.mx_quantize_gemm(_bf16(256, 256), _mx(512, 256), None,
+                                                                  mx.MX_EPI_GATE_RESIDUAL_BF16,
+                                                                  residual=_bf16(256, 512)),
+    "mx_mlp_noalloc": lambda: mx.mx_mlp_noalloc(_bf16(256, 256), _mx(512, 256), None, _mx(256, 512), None),
 }
 
 

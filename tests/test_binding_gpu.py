@@ -104,3 +104,37 @@ def test_fused_entry_points_refuse_bad_buffers(lib):
     with pytest.raises(ValueError):
         lib.mx_gemm_gate_residual(a, b, None, None, _bf16(M, d), out=_bf16(M, d - 1))
     assert lib.mx_device_error() == 0
+
+
+def test_quantize_gemm_refuses_bad_buffers(lib):
+    """mx_quantize_gemm: the activations, the weight, the bias, the gate and residual,
+    the output and the workspace are checked as the other entry points check them."""
+    import torch
+
+    M, K, N = 300, 256, 512
+    x, b = _bf16(M, K), _mx(lib, N, K)
+    need = lib.mx_quantize_gemm_workspace_bytes(M, K)
+    bad = [
+        dict(x=_bf16(K, M).t()),                                     # strided activations
+        dict(x=torch.zeros((M, K), device="cuda")),                  # fp32 activations
+        dict(b=_mx(lib, N, K, short_scales=1)),
+        dict(b=_mx(lib, N, K + 128)),                                # inner dimensions differ
+        dict(bias=_bf16(N - 1)),
+        dict(out=_bf16(M * N - 1)),
+        dict(workspace=torch.zeros(need, dtype=torch.int32, device="cuda")),
+        dict(epi=lib.MX_EPI_GATE_RESIDUAL_BF16),                    # no residual
+        dict(epi=lib.MX_EPI_GATE_RESIDUAL_BF16, residual=_bf16(M + 1, N)),
+        dict(epi=lib.MX_EPI_GATE_RESIDUAL_BF16, residual=_bf16(M, N), gate=_bf16(N + 1)),
+        dict(epi=lib.MX_EPI_BIAS_GELU_MXFP6, out=_mx(lib, M, N, short_scales=1)),
+        dict(epi=lib.MX_EPI_BIAS_SWIGLU_MXFP6, out=_mx(lib, M, N)),  # SwiGLU writes N/2
+    ]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            lib.mx_quantize_gemm(kw.get("x", x), kw.get("b", b), kw.get("bias"), kw.get("epi", lib.MX_EPI_BIAS_BF16),
+                                 gate=kw.get("gate"), residual=kw.get("residual"), out=kw.get("out"),
+                                 workspace=kw.get("workspace"))
+    # a workspace below mx_quantize_gemm_workspace_bytes is refused by the library
+    with pytest.raises(lib.MxError):
+        lib.mx_quantize_gemm(x, b, None, lib.MX_EPI_BIAS_BF16,
+                             workspace=torch.zeros(need - 256, dtype=torch.uint8, device="cuda"))
+    assert lib.mx_device_error() == 0
