@@ -93,6 +93,22 @@ def test_noalloc_binding_matches_mx_mlp(lib):
     assert lib.mx_device_error() == 0
 
 
+def test_noalloc_with_the_quantizer_inside_the_gemm(lib):
+    """At ff = 12288 the up-projection encodes x in-kernel (rows 512 onwards), with
+    its row-block counters in the static scratch too: mx_mlp's result bit for bit,
+    on two calls in a row (the second smaller and ragged)."""
+    import torch
+
+    d, ff = 512, 12288
+    w = synth.full_mlp(M=2048, d=d, ff=ff)
+    w1, w2 = lib.mx_quantize(bf16_to_device(w["w1"])), lib.mx_quantize(bf16_to_device(w["w2"]))
+    b1, b2 = bf16_to_device(w["b1"]), bf16_to_device(w["b2"])
+    for rows in (slice(0, 2048), slice(37, 1837)):
+        x = bf16_to_device(w["x"][rows])
+        assert torch.equal(lib.mx_mlp_noalloc(x, w1, b1, w2, b2), lib.mx_mlp(x, w1, b1, w2, b2))
+    assert lib.mx_device_error() == 0
+
+
 def test_noalloc_refuses_sizes_beyond_its_scratch(lib):
     fn = _noalloc_fn(lib)
     # 5591 tokens of a d=3072, ff=12288 block need more than the 64 MiB scratch;
