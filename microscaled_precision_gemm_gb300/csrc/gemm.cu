@@ -69,6 +69,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -1224,6 +1225,23 @@ static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) 
   return cudaSuccess;
 }
 
+// Nsight Compute's captures of the QA instance's cooperative cluster launch fail at the
+// launch; the same grid launched without the cooperative attribute profiles normally.
+// MXFP6_PROFILE_PLAIN_LAUNCH=1 in the environment launches it that way, for profiling
+// runs. The grid never exceeds the co-resident pairs, so with no other stream's kernels
+// on the GPU every CTA becomes resident, as in the cooperative launch: the previous
+// kernel in the stream leaves the SMs, and the next one may start only once every CTA
+// of this one has started. If other kernels hold SMs, a producer's wait for quantized
+// rows gives up after its bound (error bit 5) and the output is not valid; nothing
+// hangs.
+static bool plain_launch_requested() {
+  static const bool requested = [] {
+    const char* v = std::getenv("MXFP6_PROFILE_PLAIN_LAUNCH");
+    return v != nullptr && v[0] == '1' && v[1] == '\0';
+  }();
+  return requested;
+}
+
 template <int EPI, bool DBG, bool QA>
 static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
                                    const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& tout,
@@ -1274,7 +1292,7 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
     qa.first_block = static_cast<int>(a.lead_rows / 128);
     qa.strips = static_cast<int>(qa_strips(a.k));
     qa.wide = (reinterpret_cast<uintptr_t>(a.x) % 32 == 0 && a.ld_x % 16 == 0) ? 1 : 0;
-    cfg.numAttrs = 3;
+    cfg.numAttrs = plain_launch_requested() ? 2 : 3;
   }
   cfg.gridDim = dim3(kPair * plan.clusters, 1, 1);
   // the split and half-tile instances have the same resources; their attribute is
