@@ -100,13 +100,18 @@ S_QOUT = "K1 lead rows + out-proj GEMM (in-kernel quantizer)+bias+gate+residual"
 FUSED_STAGES = (S_QUP, S_QGU, S_QGEMM, S_QQKV, S_QOUT)
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the current kernels, keyed by (config, kernel); None where no
-# capture of the current kernel exists. Copied by hand from the ncu traffic
-# captures of the full DiT MLP block and of the SwiGLU DiT sub-block.
+# ncu capture of the current kernels, keyed by (config, stage); None where no
+# capture of the current kernel exists. A stage of two launches (the quantize
+# kernel on the leading rows, then the GEMM that quantizes the rest) carries both
+# launches' traffic. Copied by hand from the ncu traffic captures of the full DiT
+# MLP block (the step with the quantizer inside the up-projection, profiled with
+# MXFP6_PROFILE_PLAIN_LAUNCH=1, and the three-kernel step) and of the SwiGLU DiT
+# sub-block.
 NCU_TRAFFIC_BYTES: dict = {
+    ("full_mlp", S_QUP): 3172352 + 0 + 165177344 + 203372288,
     ("full_mlp", "K1 quantize"): 125857280 + 22170112,
     ("full_mlp", "K3 up GEMM+GELU+requant"): 80503296 + 152273408,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 256534016 + 108329472,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 255449088 + 108047872,
     ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125879040 + 24282368,
     ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 91800320 + 104683520,
     ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 284166656 + 104840960,
@@ -114,11 +119,13 @@ NCU_TRAFFIC_BYTES: dict = {
 
 
 # sm__pipe_tensor_cycles_active as a fraction of elapsed cycles, from one ncu capture
-# of the current kernel (its full-set capture); None where no capture of the current
-# kernel exists.
+# of the current kernel (a full-set or a traffic capture; for a stage of two
+# launches, its GEMM's); None where no capture of the current kernel exists.
 NCU_TENSOR_PIPE_ACTIVE: dict = {
+    ("full_mlp", S_QUP): 0.798,
+    ("dit_up", S_QUP): 0.661,
     ("full_mlp", "K3 up GEMM+GELU+requant"): 0.816,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 0.857,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 0.845,
     ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 0.845,
     ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 0.805,
     ("attn_out", "out-proj GEMM+bias+gate+residual"): 0.663,
