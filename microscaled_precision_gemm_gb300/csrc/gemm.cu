@@ -128,6 +128,7 @@ struct __align__(1024) SharedStorage {
   int abort_flag;
   alignas(16) float bias_s[kEpiWarps][kEpiCols];   // each epilogue warp's bias values (read as float4)
   alignas(16) float gate_s[kEpiWarps][kEpiCols];   // kEpiGateRes: each epilogue warp's gate values
+  uint64_t res_full[kEpiWarps];   // kEpiGateRes: each epilogue warp's residual box has landed
   // each epilogue warp's output box (BF16 32 x 32 with a 64-byte swizzle, or 32
   // rows of 48 code bytes), the source of its TMA stores
   alignas(1024) uint8_t out_stage[kEpiWarps][kOutStageBytes];
@@ -740,7 +741,10 @@ struct EpiCtx {
   float* gw;
   const CUtensorMap* tmap_out;   // the output: BF16 boxes of 32 x 32 (64-byte swizzle) or
                                  // 6-bit codes in boxes of 32 rows x 48 bytes
-  uint8_t* ostage;               // this warp's TMA store source
+  const CUtensorMap* tmap_res;   // kEpiGateRes: the residual, boxes as the BF16 output's
+  uint8_t* ostage;               // this warp's TMA store source (and residual box)
+  uint64_t* res_bar;             // kEpiGateRes: completes when the residual box has landed
+  uint32_t res_phase;            // its next phase parity
 };
 
 // The epilogue of one output tile (or, SPLIT, of one unit of the split region):
@@ -750,7 +754,7 @@ struct EpiCtx {
 // col_tile: the unit's first output column (nb * BN for a whole tile; a half tile's
 // 128 columns are drained by the warps of column group 0).
 template <int EPI, bool DBG, bool SPLIT>
-__device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e, int mb, int nb, int col_tile,
+__device__ __forceinline__ bool epilogue_tile(SharedStorage& s, EpiCtx& e, int mb, int nb, int col_tile,
                                               uint32_t& acc_phase,
                                               const Plan& pl, const Unit& u, const uint16_t* __restrict__ bias,
                                               const uint16_t* __restrict__ gate, const uint16_t* residual, void* out,
@@ -767,11 +771,34 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
     stage_vec(bw, bias, col0, n_out + col0, lane, 0.f);
   else
     stage_vec(bw, bias, col0, col0 + 64, lane, 0.f);
-  if constexpr (EPI == kEpiGateRes) stage_vec(gw, gate, col0, col0 + 64, lane, 1.f);
+  if constexpr (EPI == kEpiGateRes) {
+    stage_vec(gw, gate, col0, col0 + 64, lane, 1.f);
+    // the residual boxes this warp loads after the drain: its row's 128 columns into
+    // L2 now, while the tile's main loop runs
+    const int64_t prow = static_cast<int64_t>(mb) * BM + 32 * q + lane;
+    if (prow < m_total) prefetch_l2_bulk(residual + prow * n_total + col0, kEpiCols * 2);
+  }
+  // kEpiGateRes: the first residual box is loaded while the warp waits for the
+  // accumulator (once the previous tile's last store has read the slot)
+  const bool box_live = static_cast<int64_t>(mb) * BM + 32 * q < m_total;
+  bool res_pending = false;
+  if constexpr (EPI == kEpiGateRes) {
+    if (box_live) {
+      if (lane == 0) {
+        bulk_wait_read_all();
+        mbar_arrive_expect_tx(e.res_bar, kOutStageBytes);
+        tma_load_2d(e.ostage, e.tmap_res, e.res_bar, col0, static_cast<int32_t>(static_cast<int64_t>(mb) * BM + 32 * q));
+      }
+      res_pending = true;
+    }
+  }
   int ok = 0;
   if (lane == 0) ok = wait_bounded(&s.tmem_full, acc_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (!ok) return false;
+  if (!ok) {
+    if (res_pending && lane == 0) wait_drain(e.res_bar, e.res_phase);   // not in flight when the CTA leaves
+    return false;
+  }
   tc_fence_after();
   uint32_t r[kEpiChunks][32];
   const uint32_t t0 = tmem + (static_cast<uint32_t>(32 * q) << 16);
@@ -787,7 +814,13 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
   acc_phase ^= 1u;
   if constexpr (SPLIT) {
     // a split tile's first contributor only stores its partial sum
-    if ((u.kb0 != 0 || u.kb1 != pl.kblocks) && !split_exchange(pl, cluster, rank, warp - 2, lane, u, r)) return true;
+    if ((u.kb0 != 0 || u.kb1 != pl.kblocks) && !split_exchange(pl, cluster, rank, warp - 2, lane, u, r)) {
+      if (res_pending) {   // the first residual box is not used: let it land
+        if (lane == 0) wait_drain(e.res_bar, e.res_phase);
+        e.res_phase ^= 1u;
+      }
+      return true;
+    }
   }
 
   const int64_t row0 = static_cast<int64_t>(mb) * BM + 32 * q;   // the warp's first row
@@ -798,24 +831,45 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
     for (int c = 0; c < kEpiChunks; ++c) {
       const int n = col0 + 32 * c;
       uint32_t rw[16];  // kEpiGateRes: the residual's 32 BF16 values, two per word
+      // 16-byte piece j of row `lane` sits at piece j ^ ((lane >> 1) & 3) of the row in
+      // the warp's box (the 64-byte swizzle of the TMA boxes)
+      uint4* srow = reinterpret_cast<uint4*>(e.ostage + lane * (kOutBoxCols * 2));
       if constexpr (EPI == kEpiGateRes) {
-        uint4 res[4] = {};
-        if (live) {
-          // plain coherent loads, not the read-only (non-coherent) path: the output
-          // may be this very residual, written by this kernel (in-place update).
-          // They allocate in L1, so the four 16-byte loads of a thread's 64 bytes
-          // share their two 32-byte sectors (loads that skip L1 fetch each sector
-          // twice: 77% slower at K = 3072)
-          const uint4* src = reinterpret_cast<const uint4*>(residual + row * n_total + n);
+        // The residual box (these 32 rows x 32 columns) arrives by TMA in the warp's
+        // store slot, once the previous store has read it, and is read back by rows:
+        // per-row 16-byte global loads would touch 32 lines per warp instruction in
+        // the SM's data pipe, which the main loop's operand traffic shares. The
+        // output may be this very residual (in place): the box is read before the
+        // same warp stores it.
+        if (c > 0 && lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) res[j] = src[j];
-        }
+        for (int j = 0; j < 16; ++j) rw[j] = 0u;
+        if (box_live) {
+          int got = 0;
+          if (lane == 0) {
+            if (c > 0) {   // chunk 0's box was loaded before the drain
+              mbar_arrive_expect_tx(e.res_bar, kOutStageBytes);
+              tma_load_2d(e.ostage, e.tmap_res, e.res_bar, n, static_cast<int32_t>(row0));
+            }
+            got = wait_bounded(e.res_bar, e.res_phase, abort_flag, kErrWaitEpilogue) ? 1 : 0;
+            if (!got) wait_drain(e.res_bar, e.res_phase);   // the box is not in flight when the CTA leaves
+          }
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) return false;
+          // every lane observes the completed phase (lane 0 has seen it complete, and it
+          // cannot advance before lane 0 arms it again) before reading the box
+          for (int i = 0; i < 64 && !mbar_try_wait(smem_u32(e.res_bar), e.res_phase); ++i) {
+          }
+          e.res_phase ^= 1u;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          rw[4 * j] = res[j].x;
-          rw[4 * j + 1] = res[j].y;
-          rw[4 * j + 2] = res[j].z;
-          rw[4 * j + 3] = res[j].w;
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = srow[j ^ ((lane >> 1) & 3)];
+            rw[4 * j] = v.x;
+            rw[4 * j + 1] = v.y;
+            rw[4 * j + 2] = v.z;
+            rw[4 * j + 3] = v.w;
+          }
         }
       }
       uint32_t pk[16];
@@ -839,12 +893,13 @@ __device__ __forceinline__ bool epilogue_tile(SharedStorage& s, const EpiCtx& e,
         pk[2 * v] = cvt_bf16x2(x1, x0);
         pk[2 * v + 1] = cvt_bf16x2(x3, x2);
       }
-      // the slot is free once the warp's previous store has read it
-      if (lane == 0) bulk_wait_read_all();
+      if constexpr (EPI != kEpiGateRes) {
+        // the slot is free once the warp's previous store has read it
+        if (lane == 0) bulk_wait_read_all();
+      }
+      // (kEpiGateRes: every lane has read its row of the residual box)
       __syncwarp();
-      // 16-byte piece j of row `lane` at piece j ^ ((lane >> 1) & 3) of the row (the
-      // 64-byte swizzle), so the warp's 16-byte writes fall on distinct banks
-      uint4* srow = reinterpret_cast<uint4*>(e.ostage + lane * (kOutBoxCols * 2));
+      // the swizzle puts the warp's 16-byte writes on distinct banks
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         srow[j ^ ((lane >> 1) & 3)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
@@ -944,7 +999,8 @@ __device__ __forceinline__ bool epilogue_skip(SharedStorage& s, const EpiCtx& e,
 
 template <int EPI, bool DBG, bool SPLIT, bool HALF>
 __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, int warp, int lane, const Plan& pl,
-                                             const CUtensorMap* tmap_out, int cluster, int rank, int num_m,
+                                             const CUtensorMap* tmap_out, const CUtensorMap* tmap_res, int cluster,
+                                             int rank, int num_m,
                                              int m_total, int n_total,
                                              const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate,
                                              const uint16_t* residual, void* out, uint8_t* __restrict__ out_scales,
@@ -966,7 +1022,10 @@ __device__ __forceinline__ void run_epilogue(SharedStorage& s, uint32_t tmem, in
   e.bw = s.bias_s[warp - 2];
   e.gw = s.gate_s[warp - 2];
   e.tmap_out = tmap_out;
+  e.tmap_res = tmap_res;
   e.ostage = s.out_stage[warp - 2];
+  e.res_bar = &s.res_full[warp - 2];
+  e.res_phase = 0;
   uint32_t acc_phase = 0;
   // the split region first, in its own loop
   if constexpr (SPLIT) {
@@ -1010,7 +1069,8 @@ __global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_bh,
                    const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sb,
-                   const __grid_constant__ CUtensorMap tmap_out, const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate, const uint16_t* residual,
+                   const __grid_constant__ CUtensorMap tmap_out, const __grid_constant__ CUtensorMap tmap_res,
+                   const uint16_t* __restrict__ bias, const uint16_t* __restrict__ gate, const uint16_t* residual,
                    void* out, uint8_t* __restrict__ out_scales, float* __restrict__ dbg, int m_total, int n_total,
                    int k_total, SplitArgs split, QaArgs qa) {
   static_assert(!(QA && SPLIT), "the in-kernel quantizer runs without the split tail");
@@ -1045,6 +1105,7 @@ __global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
     mbar_init(&s.tmem_full, 1);
     mbar_init(&s.tmem_empty, kPair * kEpiWarps);
     mbar_init(&s.drain, 1);
+    for (int i = 0; i < kEpiWarps; ++i) mbar_init(&s.res_full[i], 1);
     s.abort_flag = 0;
     fence_barrier_init();
   }
@@ -1060,6 +1121,7 @@ __global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
     prefetch_tensormap(&tmap_sa);
     prefetch_tensormap(&tmap_sb);
     prefetch_tensormap(&tmap_out);
+    if (EPI == kEpiGateRes) prefetch_tensormap(&tmap_res);
   }
   // both CTAs' barriers and tensor memory exist before either touches the other's
   cluster_sync();
@@ -1082,7 +1144,8 @@ __global__ void __launch_bounds__(QA ? kThreadsQa : kThreads, 1)
   } else if (QA && warp == kQaWarp) {
     run_quantizer(qa, m_total, k_total, lane);
   } else {
-    run_epilogue<EPI, DBG, SPLIT, HALF>(s, tmem, warp, lane, plan, &tmap_out, cluster, rank, num_m, m_total, n_total,
+    run_epilogue<EPI, DBG, SPLIT, HALF>(s, tmem, warp, lane, plan, &tmap_out, &tmap_res, cluster, rank, num_m,
+                                        m_total, n_total,
                                         bias,
                                   gate, residual, out, out_scales, dbg, abort_flag);
     // the stores' writes are complete (and their shared sources read) before the
@@ -1163,8 +1226,9 @@ static bool make_scale_maps(CUtensorMap* sa, CUtensorMap* sb, const void* a_scal
   return r == CUDA_SUCCESS;
 }
 
-// Tensor map over a BF16 output [m][n] for the epilogues' TMA stores: box 32
-// columns x 32 rows (one epilogue warp's block), 64-byte swizzle.
+// Tensor map over a BF16 [m][n] matrix in the epilogues' boxes: 32 columns x 32 rows
+// (one epilogue warp's block), 64-byte swizzle. The output's, for the TMA stores,
+// and kEpiGateRes's residual, for its TMA loads.
 static bool make_bf16_out_map(CUtensorMap* map, void* out, int64_t m, int64_t n) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
@@ -1245,7 +1309,7 @@ static bool plain_launch_requested() {
 template <int EPI, bool DBG, bool QA>
 static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
                                    const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& tout,
-                                   const GemmArgs& a, cudaStream_t stream) {
+                                   const CUtensorMap& tres, const GemmArgs& a, cudaStream_t stream) {
   constexpr bool kHalvesOk = !DBG && EPI != kEpiSwiglu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1313,7 +1377,7 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   }
   if (e != cudaSuccess) return e;
   if (same != clusters) return cudaErrorLaunchOutOfResources;
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tsa, tsb, tout, static_cast<const uint16_t*>(a.bias),
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tsa, tsb, tout, tres, static_cast<const uint16_t*>(a.bias),
                          static_cast<const uint16_t*>(a.gate), static_cast<const uint16_t*>(a.residual), a.out,
                          static_cast<uint8_t*>(a.out_scales), a.debug_prequant, static_cast<int>(a.m),
                          static_cast<int>(a.n), static_cast<int>(a.k), split, qa);
@@ -1323,14 +1387,18 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, bool* encode_failed) {
   *encode_failed = false;
-  CUtensorMap ta, tb, tbh, tsa, tsb, tout;
+  CUtensorMap ta, tb, tbh, tsa, tsb, tout, tres;
   const bool bf16_out = a.epilogue == kEpiBf16 || a.epilogue == kEpiGateRes;
   const int64_t w_out = a.epilogue == kEpiSwiglu ? a.n / 2 : a.n;
   if (!make_codes_map(&ta, a.a_codes, a.m, a.k, BM) ||
       !make_codes_map(&tb, a.b_codes, a.n, a.k, kBHalfRows) ||
       !make_codes_map(&tbh, a.b_codes, a.n, a.k, kHalfCols / kPair) ||
       !make_scale_maps(&tsa, &tsb, a.a_scales, a.b_scales, a.m, a.n, a.k, a.epilogue == kEpiSwiglu ? 1u : 2u) ||
-      !(bf16_out ? make_bf16_out_map(&tout, a.out, a.m, a.n) : make_codes_out_map(&tout, a.out, a.m, w_out))) {
+      !(bf16_out ? make_bf16_out_map(&tout, a.out, a.m, a.n) : make_codes_out_map(&tout, a.out, a.m, w_out)) ||
+      // kEpiGateRes reads the residual [M][N] in the output's boxes; other epilogues
+      // pass the output's map, unused
+      !(a.epilogue == kEpiGateRes ? make_bf16_out_map(&tres, const_cast<void*>(a.residual), a.m, a.n)
+                                  : (tres = tout, true))) {
     *encode_failed = true;
     return cudaSuccess;
   }
@@ -1340,22 +1408,22 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t stream, boo
     // the in-kernel quantizer: no debug output, no split tail
     if (dbg) return cudaErrorInvalidValue;
     switch (a.epilogue) {
-      case kEpiBf16: return launch_instance<kEpiBf16, false, true>(ta, tb, tbh, tsa, tsb, tout, a, stream);
-      case kEpiGelu: return launch_instance<kEpiGelu, false, true>(ta, tb, tbh, tsa, tsb, tout, a, stream);
-      case kEpiSwiglu: return launch_instance<kEpiSwiglu, false, true>(ta, tb, tbh, tsa, tsb, tout, a, stream);
-      case kEpiGateRes: return launch_instance<kEpiGateRes, false, true>(ta, tb, tbh, tsa, tsb, tout, a, stream);
+      case kEpiBf16: return launch_instance<kEpiBf16, false, true>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream);
+      case kEpiGelu: return launch_instance<kEpiGelu, false, true>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream);
+      case kEpiSwiglu: return launch_instance<kEpiSwiglu, false, true>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream);
+      case kEpiGateRes: return launch_instance<kEpiGateRes, false, true>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (a.epilogue) {
-    case kEpiBf16: return launch_instance<kEpiBf16, false, false>(ta, tb, tbh, tsa, tsb, tout, a, stream);
+    case kEpiBf16: return launch_instance<kEpiBf16, false, false>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream);
     case kEpiGelu:
-      return dbg ? launch_instance<kEpiGelu, true, false>(ta, tb, tbh, tsa, tsb, tout, a, stream)
-                 : launch_instance<kEpiGelu, false, false>(ta, tb, tbh, tsa, tsb, tout, a, stream);
+      return dbg ? launch_instance<kEpiGelu, true, false>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream)
+                 : launch_instance<kEpiGelu, false, false>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream);
     case kEpiSwiglu:
-      return dbg ? launch_instance<kEpiSwiglu, true, false>(ta, tb, tbh, tsa, tsb, tout, a, stream)
-                 : launch_instance<kEpiSwiglu, false, false>(ta, tb, tbh, tsa, tsb, tout, a, stream);
-    case kEpiGateRes: return launch_instance<kEpiGateRes, false, false>(ta, tb, tbh, tsa, tsb, tout, a, stream);
+      return dbg ? launch_instance<kEpiSwiglu, true, false>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream)
+                 : launch_instance<kEpiSwiglu, false, false>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream);
+    case kEpiGateRes: return launch_instance<kEpiGateRes, false, false>(ta, tb, tbh, tsa, tsb, tout, tres, a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
