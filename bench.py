@@ -104,17 +104,18 @@ FUSED_STAGES = (S_QUP, S_QGU, S_QGEMM, S_QQKV, S_QOUT)
 # capture of the current kernel exists. A stage of two launches (the quantize
 # kernel on the leading rows, then the GEMM that quantizes the rest) carries both
 # launches' traffic. Copied by hand from the ncu traffic captures of the full DiT
-# MLP block (the step with the quantizer inside the up-projection, profiled with
-# MXFP6_PROFILE_PLAIN_LAUNCH=1, and the three-kernel step) and of the SwiGLU DiT
-# sub-block.
+# MLP block and of the M = 4096 up-projection (the steps with the quantizer inside
+# the up-projection, profiled with MXFP6_PROFILE_PLAIN_LAUNCH=1; the full block's
+# three-kernel step) and of the SwiGLU DiT sub-block.
 NCU_TRAFFIC_BYTES: dict = {
     ("full_mlp", S_QUP): 3172352 + 0 + 165177344 + 203372288,
     ("full_mlp", "K1 quantize"): 125857280 + 22170112,
     ("full_mlp", "K3 up GEMM+GELU+requant"): 80503296 + 152273408,
     ("full_mlp", "K2 down GEMM+bias+BF16"): 255449088 + 108047872,
-    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125879040 + 24282368,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 91800320 + 104683520,
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 284166656 + 104840960,
+    ("dit_up", S_QUP): 3166464 + 0 + 52898048 + 10911744,
+    ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125882112 + 24203264,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89456640 + 105300224,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 281890048 + 105528064,
 }
 
 
@@ -126,9 +127,10 @@ NCU_TENSOR_PIPE_ACTIVE: dict = {
     ("dit_up", S_QUP): 0.661,
     ("full_mlp", "K3 up GEMM+GELU+requant"): 0.816,
     ("full_mlp", "K2 down GEMM+bias+BF16"): 0.845,
-    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 0.845,
-    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 0.805,
-    ("attn_out", "out-proj GEMM+bias+gate+residual"): 0.663,
+    ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 0.837,
+    ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 0.800,
+    ("attn_out", "out-proj GEMM+bias+gate+residual"): 0.682,
+    ("attn_out", S_QOUT): 0.682,
 }
 
 
