@@ -272,13 +272,9 @@ mx_status mx_gemm_launch_plan(int64_t M, int64_t N, int64_t K, size_t workspace_
  *              counter word per 128 rows (zeroed by the call's quantize kernel).
  * No split tail, no debug output. M == 0 or N == 0: nothing is launched.
  * Not for two calls at once on one workspace.
- * The GEMM that quantizes rows itself (here and in mx_mlp / mx_gated_mlp) is a
- * cooperative launch: its CTAs wait for one another's quantized rows. Profilers
- * that cannot launch it that way (Nsight Compute's captures fail at the launch)
- * may set MXFP6_PROFILE_PLAIN_LAUNCH=1 in the environment: the same grid is then
- * launched without the cooperative attribute, which is only valid while no other
- * stream's kernels run on the GPU (otherwise a wait gives up, error bit 5, and the
- * output is not valid).
+ * The GEMM's CTAs wait for rows that other CTAs' quantizer warps encode; those
+ * warps claim their rows from a counter, so a CTA that has not started holds
+ * none, and the call runs correctly beside other streams' kernels.
  */
 size_t mx_quantize_gemm_workspace_bytes(int64_t M, int64_t K);
 

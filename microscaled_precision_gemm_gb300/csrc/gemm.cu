@@ -57,8 +57,9 @@
 // tensor memory and returns. A second instance of the kernel (SPLIT) divides a
 // nearly empty last round of tiles along K across all pairs (see Plan below);
 // another (HALF) runs such a round's tiles as 128-column halves on twice the pairs
-// (N = 128 pair MMAs), where the split tail is not taken. The QA instance (warp 11
-// above) is a cooperative launch, since its producers wait on other CTAs' warps.
+// (N = 128 pair MMAs), where the split tail is not taken. In the QA instance
+// (warp 11 above) producers wait on other CTAs' quantizer warps, which claim their
+// work from a counter, so only running CTAs hold any (see QaArgs below).
 // Launched with programmatic dependent launch: the
 // prologue (barriers, tensor memory, tensor-map prefetch) may overlap the previous
 // kernel in the stream, and griddepcontrol.wait holds every access to global
@@ -69,7 +70,6 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -284,14 +284,16 @@ __device__ __forceinline__ bool cursor_next(const Plan& pl, Cursor& k, Unit& u) 
 // encoded before the launch; the rest -- rows up to M rounded up to 128, padding
 // rows getting zero scales -- are cut into items of one row's 1024-column strip
 // (one 32-element block per lane, as the quantize kernel encodes them), groups of
-// kQaGroup items in row order, group g done by the quantizer warp of CTA
-// g mod #CTAs. Each group is published on its 128-row block's counter (release
-// after the stores); a producer acquires the counter of its A row block, until it
-// reads 128 x strips, before the first TMA load of that block. The counters are
-// zero at the launch (the quantize kernel before it zeroes them). Every CTA's
-// quantizer warp runs without waiting on anything, so every block is published
-// whatever the other roles do, and the launch is cooperative, so every CTA whose
-// quantizer warp a producer waits on is resident.
+// kQaGroup items in row order. The quantizer warps claim groups in turn from a
+// work counter (an atomic add on counter word 0: block 0 lies in the leading rows,
+// first_block >= 2, so no producer reads it). Each group is published on its
+// 128-row block's counter (release after the stores); a producer acquires the
+// counter of its A row block, until it reads 128 x strips, before the first TMA
+// load of that block. The counters are zero at the launch (the quantize kernel
+// before it zeroes them). A quantizer warp waits on nothing and claims groups until
+// none is left, so every claimed group is published whatever the other roles do,
+// and a group is claimed only by a CTA that is running: no producer waits on a CTA
+// that has not started, and the launch needs no co-residency guarantee.
 struct QaArgs {
   const uint16_t* x;   // BF16 A [M][K], row stride ld_x elements
   int64_t ld_x;
@@ -343,7 +345,11 @@ __device__ __forceinline__ void run_quantizer(const QaArgs& qa, int m_total, int
   const uint32_t groups = items > first ? (items - first) / kQaGroup : 0u;
   const int64_t pitch = static_cast<int64_t>(k_total) / 4 * 3;
   const bool odd = (lane & 1) != 0;   // the lane's codes start 8 bytes into a 16-byte unit
-  for (uint32_t q = blockIdx.x; q < groups; q += gridDim.x) {
+  // the next group is claimed while the current one is encoded (a warp claims one
+  // past the end before it stops)
+  unsigned claim = lane == 0 ? atomicAdd(qa.ready, 1u) : 0u;
+  for (uint32_t q = __shfl_sync(0xffffffffu, claim, 0); q < groups; q = __shfl_sync(0xffffffffu, claim, 0)) {
+    claim = lane == 0 ? atomicAdd(qa.ready, 1u) : 0u;
     const uint32_t i0 = first + q * kQaGroup;
     uint4 raw[kQaGroup][4];
     uint32_t row[kQaGroup], kb[kQaGroup];
@@ -1289,23 +1295,6 @@ static cudaError_t max_clusters(int dev, cudaLaunchConfig_t cfg, int* clusters) 
   return cudaSuccess;
 }
 
-// Nsight Compute's captures of the QA instance's cooperative cluster launch fail at the
-// launch; the same grid launched without the cooperative attribute profiles normally.
-// MXFP6_PROFILE_PLAIN_LAUNCH=1 in the environment launches it that way, for profiling
-// runs. The grid never exceeds the co-resident pairs, so with no other stream's kernels
-// on the GPU every CTA becomes resident, as in the cooperative launch: the previous
-// kernel in the stream leaves the SMs, and the next one may start only once every CTA
-// of this one has started. If other kernels hold SMs, a producer's wait for quantized
-// rows gives up after its bound (error bit 5) and the output is not valid; nothing
-// hangs.
-static bool plain_launch_requested() {
-  static const bool requested = [] {
-    const char* v = std::getenv("MXFP6_PROFILE_PLAIN_LAUNCH");
-    return v != nullptr && v[0] == '1' && v[1] == '\0';
-  }();
-  return requested;
-}
-
 template <int EPI, bool DBG, bool QA>
 static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
                                    const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& tout,
@@ -1315,7 +1304,7 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[3];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair;
   attr[0].val.clusterDim.y = 1;
@@ -1324,10 +1313,6 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
   // the stream finishes; it waits (griddepcontrol.wait) before touching memory
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  // QA: producers wait for quantizer warps of other CTAs, so all CTAs are made
-  // co-resident (a cooperative launch; the grid never exceeds the co-resident pairs)
-  attr[2].id = cudaLaunchAttributeCooperative;
-  attr[2].val.cooperative = 1;
   cfg.blockDim = dim3(QA ? kThreadsQa : kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -1354,9 +1339,10 @@ static cudaError_t launch_instance(const CUtensorMap& ta, const CUtensorMap& tb,
     qa.scales = static_cast<uint8_t*>(const_cast<void*>(a.a_scales));
     qa.ready = a.ready;
     qa.first_block = static_cast<int>(a.lead_rows / 128);
+    // counter word 0 is the quantizer warps' work counter: block 0 must be a leading one
+    if (qa.first_block < 1) return cudaErrorInvalidValue;
     qa.strips = static_cast<int>(qa_strips(a.k));
     qa.wide = (reinterpret_cast<uintptr_t>(a.x) % 32 == 0 && a.ld_x % 16 == 0) ? 1 : 0;
-    cfg.numAttrs = plain_launch_requested() ? 2 : 3;
   }
   cfg.gridDim = dim3(kPair * plan.clusters, 1, 1);
   // the split and half-tile instances have the same resources; their attribute is

@@ -87,9 +87,9 @@ def test_quantize_then_gemm_graph_many_replays(lib):
 def test_fused_quantizer_graph_replay(lib):
     """The GEMM that quantizes its own activations under capture: mx_mlp at a width
     whose up-projection encodes rows 512.. in-kernel (ff = 12288), and
-    mx_quantize_gemm on its own, captured (the cooperative launch becomes a graph
-    node) and replayed on fresh inputs; the captured quantize kernel zeroes the
-    row-block counters on every replay, so each replay equals the eager call."""
+    mx_quantize_gemm on its own, captured and replayed on fresh inputs; the
+    captured quantize kernel zeroes the row-block counters (and the quantizer warps'
+    work counter) on every replay, so each replay equals the eager call."""
     import torch
 
     M, d, ff = 1536, 256, 12288

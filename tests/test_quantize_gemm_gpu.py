@@ -198,7 +198,9 @@ def test_mlp_up_projection_quantizes_in_kernel(lib, gated):
 
 def test_threads_on_separate_streams(lib):
     """Three host threads, each on its own stream and workspace, run the fused GEMM
-    five times at once; every result equals the one computed alone."""
+    five times at once; every result equals the one computed alone. The calls'
+    grids cannot all be resident together, so producers wait on row groups that
+    only the running CTAs' quantizer warps have claimed."""
     import torch
 
     n_threads, M, K, N = 3, 2048, 1024, 12288
@@ -266,45 +268,3 @@ def test_nan_and_inf_blocks_in_kernel(lib):
     assert not np.isnan(f32_from_bf16_bits(got[1398])).any()
     assert lib.mx_device_error() == 0
 
-
-_PLAIN_LAUNCH_CHILD = r"""
-import sys
-import numpy as np
-import torch
-sys.path.insert(0, sys.argv[1])
-import microscaled_precision_gemm_gb300 as mx
-import synth
-
-rng = np.random.default_rng(5)
-M, K, N = 2300, 1536, 12288
-x = torch.from_numpy(synth.bf16_round(rng.standard_normal((M, K)).astype(np.float32)).view(np.int16))
-x = x.cuda().view(torch.bfloat16)
-w = torch.from_numpy(synth.bf16_round(rng.standard_normal((N, K)).astype(np.float32) * 0.02).view(np.int16))
-w = mx.mx_quantize(w.cuda().view(torch.bfloat16))
-ws = torch.empty(mx.mx_quantize_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
-got = mx.mx_quantize_gemm(x, w, None, mx.MX_EPI_BIAS_GELU_MXFP6, workspace=ws)
-ref = mx.mx_gemm(mx.mx_quantize(x), w, None, mx.MX_EPI_BIAS_GELU_MXFP6)
-err = mx.mx_device_error()
-same = torch.equal(got.codes, ref.codes) and torch.equal(got.scales, ref.scales)
-print("error word", err, "bit-identical", same)
-sys.exit(0 if err == 0 and same else 1)
-"""
-
-
-def test_plain_launch_for_profilers(lib):
-    """MXFP6_PROFILE_PLAIN_LAUNCH=1 (for profilers that cannot launch the cooperative
-    kernel) launches the same grid without the cooperative attribute: with nothing
-    else on the GPU every CTA is resident, so the bytes are the same as mx_quantize +
-    mx_gemm and no wait gives up. The variable is read once per process: a child
-    process runs it."""
-    import os
-    import subprocess
-    import sys
-
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, MXFP6_PROFILE_PLAIN_LAUNCH="1")
-    env["PYTHONPATH"] = os.pathsep.join([root, env.get("PYTHONPATH", "")])
-    r = subprocess.run([sys.executable, "-c", _PLAIN_LAUNCH_CHILD, root], env=env, capture_output=True, text=True,
-                       timeout=600)
-    assert r.returncode == 0, r.stdout + r.stderr
-    assert "bit-identical True" in r.stdout
