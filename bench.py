@@ -105,14 +105,14 @@ FUSED_STAGES = (S_QUP, S_QGU, S_QGEMM, S_QQKV, S_QOUT)
 # kernel on the leading rows, then the GEMM that quantizes the rest) carries both
 # launches' traffic. Copied by hand from the ncu traffic captures of the full DiT
 # MLP block and of the M = 4096 up-projection (the steps with the quantizer inside
-# the up-projection, profiled with MXFP6_PROFILE_PLAIN_LAUNCH=1; the full block's
-# three-kernel step) and of the SwiGLU DiT sub-block.
+# the up-projection; the full block's three-kernel step) and of the SwiGLU DiT
+# sub-block.
 NCU_TRAFFIC_BYTES: dict = {
-    ("full_mlp", S_QUP): 3172352 + 0 + 165177344 + 203372288,
+    ("full_mlp", S_QUP): 3172352 + 0 + 154721280 + 206835968,
     ("full_mlp", "K1 quantize"): 125857280 + 22170112,
     ("full_mlp", "K3 up GEMM+GELU+requant"): 80503296 + 152273408,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 255449088 + 108047872,
-    ("dit_up", S_QUP): 3166464 + 0 + 52898048 + 10911744,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 246828800 + 107906560,
+    ("dit_up", S_QUP): 3168256 + 4608 + 52893952 + 11980288,
     ("dit_block_swiglu", "K1 RMSNorm+modulate+quantize"): 125882112 + 24203264,
     ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 89456640 + 105300224,
     ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 281890048 + 105528064,
@@ -123,10 +123,10 @@ NCU_TRAFFIC_BYTES: dict = {
 # of the current kernel (a full-set or a traffic capture; for a stage of two
 # launches, its GEMM's); None where no capture of the current kernel exists.
 NCU_TENSOR_PIPE_ACTIVE: dict = {
-    ("full_mlp", S_QUP): 0.798,
-    ("dit_up", S_QUP): 0.661,
+    ("full_mlp", S_QUP): 0.786,
+    ("dit_up", S_QUP): 0.662,
     ("full_mlp", "K3 up GEMM+GELU+requant"): 0.816,
-    ("full_mlp", "K2 down GEMM+bias+BF16"): 0.845,
+    ("full_mlp", "K2 down GEMM+bias+BF16"): 0.858,
     ("dit_block_swiglu", "K3 gate/up GEMM+SwiGLU+requant"): 0.837,
     ("dit_block_swiglu", "K2 down GEMM+bias+gate+residual"): 0.800,
     ("attn_out", "out-proj GEMM+bias+gate+residual"): 0.682,
