@@ -28,13 +28,15 @@ def plan(tmp_path_factory):
     subprocess.run([cxx, "-std=c++17", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", CSRC,
                     "-I", cuda_inc, os.path.join(ROOT, "tests", "helpers", "plan_probe.cpp"), "-o", exe], check=True)
 
-    def run(m, n, k, clusters=76, ws=None, halves=False):
+    def run(m, n, k, clusters=76, ws=None, halves=False, lead=False):
         full = COUNTERS + 2 * min(80, max(1, ((m + 255) // 256) * (n // 256) - 1)) * SLOT
         ws_bytes = full if ws is None else ws
         out = subprocess.run([exe], input=f"{m} {n} {k} {clusters} {ws_bytes} {int(halves)}\n", capture_output=True,
                              text=True, check=True).stdout.split()
         vals = tuple(int(v) for v in out)
-        return vals if halves else vals[:4]
+        if lead:
+            return vals[5]
+        return vals[:5] if halves else vals[:4]
 
     return run
 
@@ -100,3 +102,24 @@ def test_half_tiles(plan):
     assert plan(256 * 39, 256, 3072, halves=True)[1:] == (39, 0, 0, 0)
     # the split tail wins where it applies (DiT down-projection)
     assert plan(16384, 3072, 12288, halves=True)[2:] == (84, COUNTERS + 2 * 80 * SLOT, 0)
+
+
+def test_leading_rows_cover_row_block_zero(plan):
+    """The GEMM that quantizes its own activations leaves the rows of its first round
+    of tiles to the quantize kernel; when it encodes any rows itself (leading rows <
+    M) they are a whole number of 256-row pair tiles, at least one, so 128-row block
+    0 always lies in the leading rows. Its counter word is then free, and the
+    quantizer warps use it as their work counter."""
+    # the full block's up-projection: 48 column tiles, 76 pairs -> row tiles 0 and 1
+    assert plan(20480, 12288, 3072, lead=True) == 512
+    assert plan(4096, 12288, 3072, lead=True) == 512
+    # 16384 wide (the SwiGLU gate/up GEMM): 64 column tiles -> row tiles 0 and 1
+    assert plan(20480, 16384, 3072, lead=True) == 512
+    # narrower than 12288: every row up front
+    assert plan(20480, 3072, 3072, lead=True) == 20480
+    assert plan(20480, 8192, 3072, lead=True) == 20480
+    # few pairs, ragged M, M inside the first round
+    for m, n, clusters in [(20480, 12288, 1), (20480, 12288, 10), (1300, 12288, 76), (300, 12288, 76),
+                           (257, 12288, 2), (100000, 65536, 76), (5000, 24576, 30)]:
+        lead_rows = plan(m, n, 3072, clusters=clusters, lead=True)
+        assert lead_rows == m or (lead_rows % 256 == 0 and 256 <= lead_rows < m), (m, n, clusters, lead_rows)
